@@ -1,0 +1,431 @@
+#!/usr/bin/env python
+"""Benchmark of the GDN-2 chunked prefill forward on one or more GB300s.
+
+One "step" is one full forward (every kernel of the launch sequence) over one
+batch of the workload, inputs resident in HBM.  Default workload: the
+long-context configuration B=4 x T=32768, H=HV=32, K=V=128 (131072 tokens per
+step), whose inputs (8.6 GB) exceed the 129 MB L2, so no flush is needed
+between steps.
+
+Prints ONE JSON line (rank 0).  Besides the throughput it reports
+ * roofline: the dominant kernel's algorithmic HBM bytes per launch over its
+   CUDA-event time on the launching stream, against the measured HBM peak;
+ * e2e: the same metric through the public API from pinned HOST buffers,
+   host->device and device->host copies inside the timed region;
+ * cpu_baseline: the FP64 oracle on the host cores over a bounded sample;
+ * clocks sampled with nvidia-smi during the timed region.
+
+``--impl reference`` times the oracle instead (the reference arm).
+Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no
+collective on the data path); time = max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN-2 prefill tokens/s at H32/D128 bf16; fraction of roofline"
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = 5
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--kernels", choices=["tc", "simt"], default=os.environ.get("GDN2_BENCH_KERNELS", "tc"))
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# byte accounting (per launch), see DESIGN.md "Roofline accounting"
+# ---------------------------------------------------------------------------
+def n_chunks(wl):
+    return sum((L + 63) // 64 for L in wl.lens)
+
+
+def fused_min_bytes(wl, has_h0, write_state=True):
+    """The whole operator's minimum HBM traffic: every input read once, the
+    output written once, states in/out."""
+    T, H, HV, K, V = wl.T_tot, wl.H, wl.HV, wl.K, wl.V
+    b = T * H * K * 2 * 2                      # q, k
+    b += T * HV * V * 2 * 3                    # v, w, o
+    b += T * HV * K * (4 + 2)                  # g fp32, beta bf16
+    st = wl.N * HV * K * V * 4
+    return b + (st if has_h0 else 0) + (st if write_state else 0)
+
+
+def stage_bytes(wl, impl, has_h0, write_state=True, l2norm=False):
+    """Algorithmic bytes each stage of the launch sequence must move: its own
+    inputs read once and outputs written once (intermediates in bf16, G in
+    fp32)."""
+    T, H, HV, K, V = wl.T_tot, wl.H, wl.HV, wl.K, wl.V
+    NC = n_chunks(wl)
+    st = wl.N * HV * K * V * 4
+    qk1 = T * H * K * 2            # one of q / k
+    kh = T * HV * K                # per-(token, value head) key-channel elements
+    vh = T * HV * V
+    hb = NC * HV * K * V * 2       # bf16 chunk states
+    out = {}
+    out["prep"] = kh * 4 * 2 + (4 * qk1 if l2norm else 0)
+    out["intra"] = qk1 + kh * 4 + kh * 2 + vh * 2 * 2 + kh * 2 + vh * 2
+    out["state"] = kh * 2 + vh * 2 + qk1 + kh * 4 + hb + vh * 2 + (st if has_h0 else 0) + (
+        st if write_state else 0)
+    out["output"] = 2 * qk1 + kh * 4 + hb + vh * 2 + vh * 2
+    return out
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return float(d["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_prefill_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(stage, impl, workload_name):
+    """DRAM bytes per launch of a stage's kernel from a committed ncu summary
+    (profiles/*.md with lines 'traffic_bytes_per_launch: <n>' and
+    'source_sha: <sha>'); None when absent or taken on other kernel sources."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    sha = kernel_source_sha()
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith(".md"):
+            continue
+        txt = open(os.path.join(pdir, f)).read()
+        m_stage = re.search(r"^stage:\s*(\S+)", txt, re.M)
+        m_impl = re.search(r"^impl:\s*(\S+)", txt, re.M)
+        m_wl = re.search(r"^workload:\s*(\S+)", txt, re.M)
+        m_b = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt, re.M)
+        m_sha = re.search(r"^source_sha:\s*(\S+)", txt, re.M)
+        if not (m_stage and m_impl and m_b and m_sha and m_wl):
+            continue
+        if m_stage.group(1) == stage and m_impl.group(1) == impl and m_wl.group(1) == workload_name:
+            return float(m_b.group(1)) if m_sha.group(1) == sha else None
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index):
+        self.dev = dev_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pc=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in rows:
+            if r["hw"].startswith("Active"):
+                reasons.add("hw_slowdown")
+            if r["hwt"].startswith("Active"):
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"].startswith("Active"):
+                reasons.add("sw_thermal_slowdown")
+            if r["pc"].startswith("Active"):
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(loaded)}
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(d, wl, n_tokens, n_units):
+    """The first n_tokens of sequence 0 for value heads 0..n_units-1, as
+    separate stand-alone units on the host."""
+    import torch
+    a = 0
+    b = a + n_tokens
+    group = wl.HV // wl.H
+    cols_v = list(range(n_units))
+    cols_k = [hv // group for hv in cols_v]
+    take = lambda x, cols: None if x is None else x[a:b][:, cols].cpu()
+    # one packed problem: unit i = head i; q/k expanded per value head
+    q = take(d["q"], cols_k); k = take(d["k"], cols_k)
+    v = take(d["v"], cols_v); g = take(d["g"], cols_v)
+    beta = take(d["beta"], cols_v); w = take(d["w"], cols_v)
+    h0 = None if d["h0"] is None else d["h0"][0:1, cols_v].cpu()
+    return dict(q=q, k=k, v=v, g=g, beta=beta, w=w, h0=h0,
+                cu_seqlens=torch.tensor([0, n_tokens]), scale=d["scale"])
+
+
+def time_oracle(sample, threads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.gdn2_forward(sample["q"], sample["k"], sample["v"], sample["g"], sample["beta"],
+                        sample["w"], scale=sample["scale"], initial_state=sample["h0"],
+                        cu_seqlens=sample["cu_seqlens"], threads=threads)
+    return time.perf_counter() - t0
+
+
+def size_oracle_sample(d, wl, seconds):
+    """Pick (tokens, units) so the oracle runs about `seconds` on the host."""
+    cores = os.cpu_count() or 1
+    units = max(1, min(wl.HV, cores))
+    probe_tokens = min(wl.lens[0], 256)
+    t = time_oracle(oracle_sample(d, wl, probe_tokens, units), units)
+    per_token = t / probe_tokens
+    n_tok = int(seconds / max(per_token, 1e-9))
+    n_tok = max(64, min(wl.lens[0], (n_tok // 64) * 64))
+    return n_tok, units
+
+
+def cpu_baseline(d, wl, seconds):
+    n_tok, units = size_oracle_sample(d, wl, seconds)
+    s = oracle_sample(d, wl, n_tok, units)
+    dt = time_oracle(s, units)
+    token_heads = n_tok * units
+    return {"value": token_heads / wl.HV / dt, "unit": "tokens/s", "cores": units, "kind": "oracle",
+            "sample": "FP64 oracle, sequence 0 tokens [0,%d) x %d of %d value heads (%d token-heads) "
+                      "in %.1f s on %d threads; tokens/s = token-heads / HV / s"
+                      % (n_tok, units, wl.HV, token_heads, dt, units)}
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    from gated_deltanet_prefill_gb300 import inputs
+    import oracle
+    oracle.build()
+    wl = inputs.workload(args.workload)
+    # a bounded host-generated slice of the workload (same recipe)
+    small_lens = (min(wl.lens[0], 16384),)
+    wl_s = inputs.Workload(wl.name + "_slice", small_lens, wl.H, wl.HV, wl.K, wl.V, g_max=wl.g_max,
+                           beta_max=wl.beta_max, h0_std=wl.h0_std, seed=wl.seed, scale=wl.scale)
+    d = inputs.generate(wl_s)
+    per_step = max(2.0, 90.0 / max(1, args.steps + args.warmup))
+    n_tok, units = size_oracle_sample(d, wl_s, per_step)
+    s = oracle_sample(d, wl_s, n_tok, units)
+    for _ in range(args.warmup):
+        time_oracle(s, units)
+    times = [time_oracle(s, units) for _ in range(args.steps)]
+    dt = sum(times) / len(times)
+    val = n_tok * units / wl.HV / dt
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.N, "T": wl.lens[0], "H": wl.H, "HV": wl.HV,
+                       "K": wl.K, "V": wl.V,
+                       "sample_per_step": "sequence 0 tokens [0,%d) x %d value heads" % (n_tok, units)},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": units, "kind": "oracle",
+                             "sample": "FP64 oracle per step: %d tokens x %d of %d value heads"
+                                       % (n_tok, units, wl.HV)},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from gated_deltanet_prefill_gb300 import build as gbuild
+    from gated_deltanet_prefill_gb300 import gdn2, inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        gbuild.build()
+    if world > 1:
+        dist.barrier()
+    gdn2.load()
+
+    wl = inputs.workload(args.workload)
+    wl_r = inputs.with_seed(wl, wl.seed + 1000 * rank)  # each rank: its own batch
+    d = inputs.generate(wl_r, device="cuda")
+    T, HV, V = wl.T_tot, wl.HV, wl.V
+    out = torch.empty((T, HV, V), dtype=torch.bfloat16, device="cuda")
+    fs = torch.empty((wl.N, HV, wl.K, V), dtype=torch.float32, device="cuda")
+    dims = gdn2.make_dims(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], out, d["cu_seqlens"],
+                          False, args.kernels)
+    ws = torch.empty(gdn2.workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+    names = gdn2.stage_names(dims)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        gdn2.chunk_gdn2_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                            initial_state=d["h0"], cu_seqlens=d["cu_seqlens"], out=out, final_state=fs,
+                            workspace=ws, impl=args.kernels, stage_events=evs)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    stage_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    for evs in stage_evs:  # materialise the CUDA events
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        start.record(stream)
+        for i in range(K):
+            step(stage_evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = start.elapsed_time(end) / K
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    stage_ms = {n: sum(ev[i].elapsed_time(ev[i + 1]) for ev in stage_evs) / K for i, n in enumerate(names)}
+
+    # roofline of the dominant kernel
+    peak, peak_kind = load_peaks()
+    sb = stage_bytes(wl, args.kernels, d["h0"] is not None, True, False)
+    dom = max(stage_ms, key=stage_ms.get)
+    ach = sb[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+            "traffic": ncu_traffic(dom, args.kernels, wl.name), "kernel": dom,
+            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
+    stages = {n: {"ms": stage_ms[n], "algorithmic_bytes": sb.get(n),
+                  "gbs": (sb[n] / (stage_ms[n] * 1e-3) / 1e9) if sb.get(n) else None,
+                  "frac_of_peak": (sb[n] / (stage_ms[n] * 1e-3) / 1e9 / peak) if sb.get(n) else None,
+                  "share": stage_ms[n] / max(sum(stage_ms.values()), 1e-12)} for n in names}
+    fmin = fused_min_bytes(wl, d["h0"] is not None)
+    whole = {"min_bytes": fmin, "achieved_gbs": fmin / (ms * 1e-3) / 1e9,
+             "frac": fmin / (ms * 1e-3) / 1e9 / peak}
+
+    # end-to-end from pinned host buffers through the public API
+    e2e = None
+    if not args.no_e2e:
+        host = {k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in d.items()}
+        runner = gdn2.HostRunner(host, impl=args.kernels)
+        runner()
+        torch.cuda.synchronize()
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        es.record(stream)
+        for _ in range(args.e2e_steps):
+            runner()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        ems = es.elapsed_time(ee) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([ems], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * T / (ems * 1e-3), "unit": "tokens/s",
+               "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
+               "ms_per_step": ems, "steps": args.e2e_steps}
+        del runner, host
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(d, wl, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": world * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+                "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if args.kernels == "tc" else "f32", "data": "synthetic",
+                "config": {"workload": wl.name, "B": wl.N, "T": wl.lens[0], "H": wl.H, "HV": wl.HV,
+                           "K": wl.K, "V": wl.V, "tokens_per_step_per_gpu": T, "kernels": args.kernels,
+                           "g": "-U(0,%g)" % wl.g_max, "beta": "U(0,%g)" % wl.beta_max,
+                           "initial_state": "N(0,%g)" % wl.h0_std if wl.h0_std else "zero",
+                           "output_final_state": True,
+                           "l2": "inputs (%.1f GB) larger than L2 (129 MB); no flush" % (fmin / 1e9),
+                           "parallelism": "replicas x%d (independent batches)" % world},
+                "roofline": roof, "stages": stages, "whole_op": whole, "e2e": e2e,
+                "cpu_baseline": cpu, "gpu_launches": gdn2.launch_count(dims) * K,
+                "clocks": clk.summary(), "source_sha": kernel_source_sha()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,297 @@
+// C ABI of the GDN-2 chunked prefill forward: argument checks, workspace
+// layout and the launch sequence.  See include/gdn2.h for the contract.
+#include <math.h>
+#include <string.h>
+
+#include "gdn2_internal.cuh"
+
+namespace gdn2 {
+
+namespace {
+
+size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int64_t nc_max(const gdn2_dims &d) { return d.T_tot / kChunk + d.N; }
+
+bool shape_ok(const gdn2_dims &d) {
+    if (d.T_tot < 0 || d.N < 0 || d.H <= 0 || d.HV <= 0 || d.HV % d.H != 0) return false;
+    if (d.K != d.V || (d.K != 64 && d.K != 128)) return false;
+    if (nc_max(d) > (1ll << 30)) return false;
+    return true;
+}
+
+// Byte range [lo, hi) covered by a strided token-major tensor.
+struct Range {
+    uintptr_t lo, hi;
+};
+
+Range tensor_range(const void *base, int64_t T, int heads, int ch, const int64_t *st, size_t esize) {
+    if (!base || T <= 0) return {0, 0};
+    const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+    const int64_t last = (T - 1) * st[0] + static_cast<int64_t>(heads - 1) * st[1] + ch;
+    return {b, b + static_cast<uintptr_t>(last) * esize};
+}
+
+Range flat_range(const void *base, size_t bytes) {
+    if (!base || bytes == 0) return {0, 0};
+    const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+    return {b, b + bytes};
+}
+
+bool overlap(Range a, Range b) { return a.hi > a.lo && b.hi > b.lo && a.lo < b.hi && b.lo < a.hi; }
+
+bool strides_ok(const void *base, const int64_t *st, size_t esize, int heads, int ch) {
+    if (!base) return true;
+    if (reinterpret_cast<uintptr_t>(base) % 16) return false;
+    if (st[0] < 0 || st[1] < 0) return false;
+    if ((st[0] * esize) % 16 || (st[1] * esize) % 16) return false;
+    (void)heads; (void)ch;
+    return true;
+}
+
+}  // namespace
+
+WsLayout workspace_layout(const gdn2_dims &d) {
+    WsLayout L;
+    const size_t T = static_cast<size_t>(d.T_tot), NC = static_cast<size_t>(nc_max(d));
+    size_t off = 0;
+    auto take = [&](size_t bytes) { const size_t o = off; off += align_up(bytes); return o; };
+    L.status = take(64);
+    L.chunk_seq = take(NC * 4);
+    L.chunk_len = take(NC * 4);
+    L.chunk_start = take(NC * 8);
+    L.seq_first = take((static_cast<size_t>(d.N) + 1) * 4);
+    L.G = take(T * d.HV * d.K * 4);
+    L.qn = take(d.use_qk_l2norm ? T * d.H * d.K * 2 : 0);
+    L.kn = take(d.use_qk_l2norm ? T * d.H * d.K * 2 : 0);
+    L.Wt = take(T * d.HV * d.K * 2);
+    L.Ut = take(T * d.HV * d.V * 2);
+    L.hbuf = take(NC * d.HV * d.K * d.V * 2);
+    L.vnew = take(T * d.HV * d.V * 2);
+    L.total = off;
+    return L;
+}
+
+}  // namespace gdn2
+
+using namespace gdn2;
+
+extern "C" {
+
+int32_t gdn2_version(void) { return (1 << 16) | 0; }
+
+const char *gdn2_status_string(int status) {
+    switch (status) {
+        case GDN2_OK: return "ok";
+        case GDN2_ERR_NULL: return "a required pointer is NULL";
+        case GDN2_ERR_SHAPE: return "unsupported sizes (need K == V in {64,128}, HV a multiple of H, N >= 0, T_tot >= 0)";
+        case GDN2_ERR_STRIDE: return "bad stride or alignment (innermost stride 1; strides and base pointers multiples of 16 bytes)";
+        case GDN2_ERR_ALIAS: return "an output overlaps an input (or final_state overlaps initial_state)";
+        case GDN2_ERR_WORKSPACE: return "workspace missing or smaller than gdn2_workspace_bytes()";
+        case GDN2_ERR_ARCH: return "current CUDA device is not compute capability 10.3 (sm_103a)";
+        case GDN2_ERR_LAUNCH: return "kernel launch failed";
+        case GDN2_ERR_DTYPE: return "unsupported dtype (q/k/v/beta/w/out bf16, g fp32)";
+        case GDN2_ERR_CU_SEQLENS: return "cu_seqlens invalid on the device (cu[0] != 0, decreasing, or cu[N] != T_tot)";
+        case GDN2_ERR_CUDA: return "CUDA runtime error";
+        case GDN2_ERR_IMPL: return "unknown implementation selector";
+        default: return "unknown status";
+    }
+}
+
+gdn2_status gdn2_dims_init(gdn2_dims *d, int64_t T_tot, int32_t N, int32_t H, int32_t HV, int32_t K,
+                           int32_t V) {
+    if (!d) return GDN2_ERR_NULL;
+    memset(d, 0, sizeof(*d));
+    d->T_tot = T_tot; d->N = N; d->H = H; d->HV = HV; d->K = K; d->V = V;
+    d->q_stride[0] = d->k_stride[0] = static_cast<int64_t>(H) * K;
+    d->q_stride[1] = d->k_stride[1] = K;
+    d->v_stride[0] = d->w_stride[0] = d->o_stride[0] = static_cast<int64_t>(HV) * V;
+    d->v_stride[1] = d->w_stride[1] = d->o_stride[1] = V;
+    d->g_stride[0] = d->beta_stride[0] = static_cast<int64_t>(HV) * K;
+    d->g_stride[1] = d->beta_stride[1] = K;
+    d->dtype_qkv = GDN2_DTYPE_BF16;
+    d->dtype_g = GDN2_DTYPE_F32;
+    d->impl = GDN2_IMPL_TC;
+    return shape_ok(*d) ? GDN2_OK : GDN2_ERR_SHAPE;
+}
+
+size_t gdn2_workspace_bytes(const gdn2_dims *d) {
+    if (!d || !shape_ok(*d)) return 0;
+    return workspace_layout(*d).total;
+}
+
+gdn2_status gdn2_check_args(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                            const void *w, const float *initial_state, const void *cu_seqlens,
+                            const void *out, const float *final_state, const gdn2_dims *d,
+                            const void *workspace, size_t workspace_bytes) {
+    if (!d) return GDN2_ERR_NULL;
+    if (d->dtype_qkv != GDN2_DTYPE_BF16 || d->dtype_g != GDN2_DTYPE_F32) return GDN2_ERR_DTYPE;
+    if (d->impl != GDN2_IMPL_TC && d->impl != GDN2_IMPL_SIMT) return GDN2_ERR_IMPL;
+    if (!shape_ok(*d)) return GDN2_ERR_SHAPE;
+    if (!cu_seqlens || !workspace) return GDN2_ERR_NULL;
+    if (d->T_tot > 0 && (!q || !k || !v || !out)) return GDN2_ERR_NULL;
+    const int64_t T = d->T_tot;
+    if (!strides_ok(q, d->q_stride, 2, d->H, d->K) || !strides_ok(k, d->k_stride, 2, d->H, d->K) ||
+        !strides_ok(v, d->v_stride, 2, d->HV, d->V) || !strides_ok(w, d->w_stride, 2, d->HV, d->V) ||
+        !strides_ok(beta, d->beta_stride, 2, d->HV, d->K) || !strides_ok(g, d->g_stride, 4, d->HV, d->K) ||
+        !strides_ok(out, d->o_stride, 2, d->HV, d->V))
+        return GDN2_ERR_STRIDE;
+    if ((initial_state && reinterpret_cast<uintptr_t>(initial_state) % 16) ||
+        (final_state && reinterpret_cast<uintptr_t>(final_state) % 16))
+        return GDN2_ERR_STRIDE;
+    // out rows must not overlap each other
+    if (T > 0 && (d->o_stride[1] < d->V || d->o_stride[0] < static_cast<int64_t>(d->HV - 1) * d->o_stride[1] + d->V))
+        return GDN2_ERR_ALIAS;
+    const size_t state_bytes = static_cast<size_t>(d->N) * d->HV * d->K * d->V * sizeof(float);
+    const Range r_out = tensor_range(out, T, d->HV, d->V, d->o_stride, 2);
+    const Range r_fs = flat_range(final_state, state_bytes);
+    const Range ins[] = {
+        tensor_range(q, T, d->H, d->K, d->q_stride, 2),     tensor_range(k, T, d->H, d->K, d->k_stride, 2),
+        tensor_range(v, T, d->HV, d->V, d->v_stride, 2),    tensor_range(w, T, d->HV, d->V, d->w_stride, 2),
+        tensor_range(beta, T, d->HV, d->K, d->beta_stride, 2), tensor_range(g, T, d->HV, d->K, d->g_stride, 4),
+        flat_range(initial_state, state_bytes),
+        flat_range(cu_seqlens, (static_cast<size_t>(d->N) + 1) * (d->cu_seqlens_i64 ? 8 : 4)),
+        flat_range(workspace, workspace_bytes)};
+    for (const Range &r : ins)
+        if (overlap(r_out, r) || overlap(r_fs, r)) return GDN2_ERR_ALIAS;
+    if (overlap(r_out, r_fs)) return GDN2_ERR_ALIAS;
+    if (workspace_bytes < workspace_layout(*d).total) return GDN2_ERR_WORKSPACE;
+    return GDN2_OK;
+}
+
+namespace {
+
+const char *const kSimtStages[] = {"prep", "intra", "state", "output"};
+constexpr int kNumSimtStages = 4;
+
+gdn2_status run(const void *q, const void *k, const void *v, const void *g, const void *beta, const void *w,
+                float scale, const float *initial_state, const void *cu_seqlens, void *out, float *final_state,
+                const gdn2_dims *d, void *workspace, size_t workspace_bytes, void *stream,
+                void *const *events, int32_t n_events) {
+    const gdn2_status st = gdn2_check_args(q, k, v, g, beta, w, initial_state, cu_seqlens, out, final_state,
+                                           d, workspace, workspace_bytes);
+    if (st != GDN2_OK) return st;
+    if (events && n_events < gdn2_num_stages(d) + 1) return GDN2_ERR_NULL;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN2_ERR_ARCH;
+    }
+    if (major != 10 || minor != 3) return GDN2_ERR_ARCH;
+    if (d->impl == GDN2_IMPL_TC) return GDN2_ERR_IMPL;  // tensor-core path not built yet
+
+    const WsLayout L = workspace_layout(*d);
+    char *ws = static_cast<char *>(workspace);
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.q = static_cast<const bf16 *>(q); p.k = static_cast<const bf16 *>(k); p.v = static_cast<const bf16 *>(v);
+    p.beta = static_cast<const bf16 *>(beta); p.w = static_cast<const bf16 *>(w);
+    p.g = static_cast<const float *>(g);
+    p.sq_t = d->q_stride[0]; p.sq_h = d->q_stride[1];
+    p.sk_t = d->k_stride[0]; p.sk_h = d->k_stride[1];
+    p.sv_t = d->v_stride[0]; p.sv_h = d->v_stride[1];
+    p.sg_t = d->g_stride[0]; p.sg_h = d->g_stride[1];
+    p.sb_t = d->beta_stride[0]; p.sb_h = d->beta_stride[1];
+    p.sw_t = d->w_stride[0]; p.sw_h = d->w_stride[1];
+    p.so_t = d->o_stride[0]; p.so_h = d->o_stride[1];
+    p.o = static_cast<bf16 *>(out);
+    p.h0 = initial_state; p.hT = final_state;
+    p.cu = cu_seqlens; p.cu64 = d->cu_seqlens_i64 ? 1 : 0;
+    p.T_tot = d->T_tot; p.N = d->N; p.H = d->H; p.HV = d->HV; p.K = d->K; p.V = d->V;
+    p.group = d->HV / d->H;
+    p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d->K));
+    p.has_g = g != nullptr; p.has_beta = beta != nullptr; p.has_w = w != nullptr;
+    p.l2norm = d->use_qk_l2norm ? 1 : 0;
+    p.NCmax = static_cast<int>(d->T_tot / kChunk + d->N);
+    p.status = reinterpret_cast<int *>(ws + L.status);
+    p.chunk_seq = reinterpret_cast<int *>(ws + L.chunk_seq);
+    p.chunk_len = reinterpret_cast<int *>(ws + L.chunk_len);
+    p.chunk_start = reinterpret_cast<int64_t *>(ws + L.chunk_start);
+    p.seq_first = reinterpret_cast<int *>(ws + L.seq_first);
+    p.G = reinterpret_cast<float *>(ws + L.G);
+    p.qn = reinterpret_cast<bf16 *>(ws + L.qn);
+    p.kn = reinterpret_cast<bf16 *>(ws + L.kn);
+    p.Wt = reinterpret_cast<bf16 *>(ws + L.Wt);
+    p.Ut = reinterpret_cast<bf16 *>(ws + L.Ut);
+    p.hbuf = reinterpret_cast<bf16 *>(ws + L.hbuf);
+    p.vnew = reinterpret_cast<bf16 *>(ws + L.vnew);
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();  // clear a stale error so the checks below see only ours
+    int stage = 0;
+    auto mark = [&]() {
+        if (events) cudaEventRecord(static_cast<cudaEvent_t>(events[stage]), s);
+        ++stage;
+    };
+    mark();
+    if (launch_chunk_map(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+    if (p.N > 0 && launch_prep(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+    mark();
+    if (p.N > 0 && launch_simt_intra(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+    mark();
+    if (p.N > 0 && launch_simt_state(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+    mark();
+    if (p.N > 0 && launch_simt_output(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+    mark();
+    if (events && cudaGetLastError() != cudaSuccess) return GDN2_ERR_CUDA;
+    return GDN2_OK;
+}
+
+}  // namespace
+
+int32_t gdn2_num_stages(const gdn2_dims *d) {
+    if (!d || !shape_ok(*d)) return 0;
+    return kNumSimtStages;
+}
+
+const char *gdn2_stage_name(const gdn2_dims *d, int32_t i) {
+    if (i < 0 || i >= gdn2_num_stages(d)) return nullptr;
+    return kSimtStages[i];
+}
+
+int32_t gdn2_launch_count(const gdn2_dims *d) {
+    if (!d || !shape_ok(*d)) return 0;
+    if (d->N == 0) return 1;
+    const int64_t ncmax = nc_max(*d);
+    int n = 1;                                          // chunk map
+    n += (d->use_qk_l2norm && d->T_tot > 0) ? 1 : 0;    // q/k L2 norm
+    n += ncmax > 0 ? 1 : 0;                             // cumsum
+    n += ncmax > 0 ? 1 : 0;                             // intra
+    n += 1;                                             // state
+    n += ncmax > 0 ? 1 : 0;                             // output
+    return n;
+}
+
+gdn2_status gdn2_chunk_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                           const void *w, float scale, const float *initial_state, const void *cu_seqlens,
+                           void *out, float *final_state, const gdn2_dims *d, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    return run(q, k, v, g, beta, w, scale, initial_state, cu_seqlens, out, final_state, d, workspace,
+               workspace_bytes, stream, nullptr, 0);
+}
+
+gdn2_status gdn2_chunk_fwd_staged(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                                  const void *w, float scale, const float *initial_state, const void *cu_seqlens,
+                                  void *out, float *final_state, const gdn2_dims *d, void *workspace,
+                                  size_t workspace_bytes, void *stream, void *const *events, int32_t n_events) {
+    if (!events) return GDN2_ERR_NULL;
+    return run(q, k, v, g, beta, w, scale, initial_state, cu_seqlens, out, final_state, d, workspace,
+               workspace_bytes, stream, events, n_events);
+}
+
+gdn2_status gdn2_device_status(const void *workspace, void *stream, int32_t *status) {
+    if (!workspace || !status) return GDN2_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t host = 0;  // the status word sits at offset 0 of the workspace
+    if (cudaMemcpyAsync(&host, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return GDN2_ERR_CUDA;
+    }
+    *status = host;
+    return GDN2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// Internal declarations shared by the library's translation units.
+// Not part of the public ABI (that is include/gdn2.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn2.h"
+
+namespace gdn2 {
+
+constexpr int kChunk = 64;     // WY chunk length (FlashRT "64-token WY blocks")
+constexpr int kSub = 16;       // sub-chunk length for decay re-referencing (burn-gdn2)
+constexpr int kNumSub = kChunk / kSub;
+
+using bf16 = __nv_bfloat16;
+
+// Everything a kernel needs, passed by value.  Token-major tensors carry
+// element strides (token, head); the channel stride is 1.
+struct Params {
+    const bf16 *q, *k, *v, *beta, *w;
+    const float *g;
+    int64_t sq_t, sq_h, sk_t, sk_h, sv_t, sv_h, sg_t, sg_h, sb_t, sb_h, sw_t, sw_h, so_t, so_h;
+    bf16 *o;
+    const float *h0;
+    float *hT;
+    const void *cu;
+    int cu64;
+    int64_t T_tot;
+    int N, H, HV, K, V, group;  // group = HV / H
+    float scale;
+    int has_g, has_beta, has_w, l2norm;
+    int NCmax;                  // upper bound on the chunk count: T_tot/64 + N
+    // ---- workspace ----
+    int *status;                // [0] status word, [1] chunk count NC
+    int *chunk_seq;             // [NCmax]  sequence of chunk c, -1 past NC
+    int *chunk_len;             // [NCmax]  tokens in chunk c (1..64)
+    int64_t *chunk_start;       // [NCmax]  first token of chunk c
+    int *seq_first;             // [N + 1]  first chunk of sequence n; [N] = NC
+    float *G;                   // [T_tot, HV, K]  chunk-local inclusive cumsum of g
+    bf16 *qn, *kn;              // [T_tot, H, K]   L2-normalised q, k (l2norm only)
+    bf16 *Wt, *Ut;              // [T_tot, HV, K], [T_tot, HV, V]  WY pseudo-keys / values
+    bf16 *hbuf;                 // [NCmax, HV, K, V] state entering each chunk (bf16)
+    bf16 *vnew;                 // [T_tot, HV, V]  u_t (v_new) per token
+};
+
+// Workspace layout (byte offsets), a function of the problem only.
+struct WsLayout {
+    size_t status, chunk_seq, chunk_len, chunk_start, seq_first, G, qn, kn, Wt, Ut, hbuf, vnew;
+    size_t total;
+};
+
+WsLayout workspace_layout(const gdn2_dims &d);
+
+__device__ __forceinline__ int64_t cu_at(const Params &p, int i) {
+    return p.cu64 ? static_cast<const int64_t *>(p.cu)[i]
+                  : static_cast<int64_t>(static_cast<const int32_t *>(p.cu)[i]);
+}
+
+// Launchers (each returns cudaGetLastError() of its launches).
+cudaError_t launch_chunk_map(const Params &p, cudaStream_t s);
+cudaError_t launch_prep(const Params &p, cudaStream_t s);
+cudaError_t launch_simt_intra(const Params &p, cudaStream_t s);
+cudaError_t launch_simt_state(const Params &p, cudaStream_t s);
+cudaError_t launch_simt_output(const Params &p, cudaStream_t s);
+
+}  // namespace gdn2

@@ -1,0 +1,244 @@
+"""ctypes binding of ``libgdn2.so`` (include/gdn2.h), argument marshalling only.
+
+Every step of the forward runs in the library's CUDA kernels; this module
+fills the ``gdn2_dims`` struct from torch tensors, allocates outputs and the
+workspace with torch when the caller does not pass them (the library itself
+never allocates), and passes raw device pointers and the current CUDA stream.
+There is no CPU path: a missing library or a non-CUDA tensor is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+GDN2_OK = 0
+STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_STRIDE", 4: "ERR_ALIAS",
+                5: "ERR_WORKSPACE", 6: "ERR_ARCH", 7: "ERR_LAUNCH", 8: "ERR_DTYPE",
+                9: "ERR_CU_SEQLENS", 10: "ERR_CUDA", 11: "ERR_IMPL"}
+IMPL = {"tc": 0, "simt": 1}
+DTYPE_BF16, DTYPE_F32 = 0, 2
+
+EXPORTS = ("gdn2_workspace_bytes", "gdn2_dims_init", "gdn2_check_args", "gdn2_chunk_fwd",
+           "gdn2_chunk_fwd_staged", "gdn2_num_stages", "gdn2_stage_name", "gdn2_launch_count",
+           "gdn2_device_status", "gdn2_status_string", "gdn2_version")
+
+
+class Gdn2Error(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        msg = "%s: %s (%s)" % (where or "gdn2", STATUS_NAMES.get(status, status), status_string(status))
+        super().__init__(msg)
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("T_tot", ctypes.c_int64), ("N", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("HV", ctypes.c_int32), ("K", ctypes.c_int32), ("V", ctypes.c_int32),
+                ("q_stride", ctypes.c_int64 * 2), ("k_stride", ctypes.c_int64 * 2),
+                ("v_stride", ctypes.c_int64 * 2), ("g_stride", ctypes.c_int64 * 2),
+                ("beta_stride", ctypes.c_int64 * 2), ("w_stride", ctypes.c_int64 * 2),
+                ("o_stride", ctypes.c_int64 * 2), ("dtype_qkv", ctypes.c_int32),
+                ("dtype_g", ctypes.c_int32), ("cu_seqlens_i64", ctypes.c_int32),
+                ("use_qk_l2norm", ctypes.c_int32), ("impl", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None):
+    """Open the library (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise RuntimeError("libgdn2.so is not built (%s); run __graft_entry__.build()" % p)
+    lib = ctypes.CDLL(p)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.gdn2_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+    lib.gdn2_workspace_bytes.restype = sz
+    lib.gdn2_dims_init.argtypes = [ctypes.POINTER(Dims), i64, i32, i32, i32, i32, i32]
+    lib.gdn2_dims_init.restype = ctypes.c_int
+    lib.gdn2_check_args.argtypes = [vp] * 10 + [ctypes.POINTER(Dims), vp, sz]
+    lib.gdn2_check_args.restype = ctypes.c_int
+    lib.gdn2_chunk_fwd.argtypes = [vp] * 6 + [ctypes.c_float, vp, vp, vp, vp,
+                                              ctypes.POINTER(Dims), vp, sz, vp]
+    lib.gdn2_chunk_fwd.restype = ctypes.c_int
+    lib.gdn2_chunk_fwd_staged.argtypes = [vp] * 6 + [ctypes.c_float, vp, vp, vp, vp,
+                                                     ctypes.POINTER(Dims), vp, sz, vp,
+                                                     ctypes.POINTER(vp), i32]
+    lib.gdn2_chunk_fwd_staged.restype = ctypes.c_int
+    lib.gdn2_num_stages.argtypes = [ctypes.POINTER(Dims)]
+    lib.gdn2_num_stages.restype = i32
+    lib.gdn2_stage_name.argtypes = [ctypes.POINTER(Dims), i32]
+    lib.gdn2_stage_name.restype = ctypes.c_char_p
+    lib.gdn2_launch_count.argtypes = [ctypes.POINTER(Dims)]
+    lib.gdn2_launch_count.restype = i32
+    lib.gdn2_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+    lib.gdn2_device_status.restype = ctypes.c_int
+    lib.gdn2_status_string.argtypes = [ctypes.c_int]
+    lib.gdn2_status_string.restype = ctypes.c_char_p
+    lib.gdn2_version.argtypes = []
+    lib.gdn2_version.restype = i32
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().gdn2_status_string(int(status)).decode()
+    except Exception:  # library not loadable: still give the name
+        return STATUS_NAMES.get(status, "?")
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _strides(t, name):
+    if t is None:
+        return (0, 0)
+    if t.stride(-1) != 1:
+        raise ValueError("%s: innermost dimension must be contiguous" % name)
+    return (t.stride(0), t.stride(1))
+
+
+def make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm=False, impl="tc") -> Dims:
+    T, H, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    d = Dims()
+    d.T_tot, d.N, d.H, d.HV, d.K, d.V = T, cu_seqlens.numel() - 1, H, HV, K, V
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("w", w), ("o", out)):
+        s = _strides(t, name)
+        getattr(d, name + "_stride")[0], getattr(d, name + "_stride")[1] = s
+    d.dtype_qkv = DTYPE_BF16 if q.dtype == torch.bfloat16 else 99
+    d.dtype_g = DTYPE_F32 if (g is None or g.dtype == torch.float32) else 99
+    for t in (k, v, beta, w):
+        if t is not None and t.dtype != q.dtype:
+            d.dtype_qkv = 99
+    d.cu_seqlens_i64 = 1 if cu_seqlens.dtype == torch.int64 else 0
+    d.use_qk_l2norm = 1 if use_qk_l2norm else 0
+    d.impl = IMPL[impl]
+    return d
+
+
+def workspace_bytes(dims: Dims) -> int:
+    return int(load().gdn2_workspace_bytes(ctypes.byref(dims)))
+
+
+def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=None,
+                   cu_seqlens=None, output_final_state=True, use_qk_l2norm=False, out=None,
+                   final_state=None, workspace=None, impl="tc", stream=None, stage_events=None):
+    """GDN-2 chunked prefill forward through ``gdn2_chunk_fwd``.
+
+    Packed layout (FlashInfer docs, chunk_gated_delta_rule2): q, k [T, H, K];
+    v, w [T, HV, V]; g, beta [T, HV, K]; initial_state [N, HV, K, V] fp32;
+    cu_seqlens [N + 1] int32/int64.  Returns (out [T, HV, V] bf16,
+    final_state [N, HV, K, V] fp32 or None).
+    """
+    lib = load()
+    if cu_seqlens is None:
+        raise ValueError("cu_seqlens is required (packed input only)")
+    for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens", cu_seqlens)):
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+    T, H, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((T, HV, V), dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, HV, K, V), dtype=torch.float32, device=q.device)
+    if initial_state is not None and not initial_state.is_contiguous():
+        raise ValueError("initial_state must be contiguous [N, HV, K, V] fp32")
+    dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, impl)
+    nbytes = workspace_bytes(dims)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(w),
+            ctypes.c_float(0.0 if scale is None else float(scale)),
+            _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+            ctypes.byref(dims), _ptr(workspace), workspace.numel(), stream)
+    if stage_events is None:
+        st = lib.gdn2_chunk_fwd(*args)
+    else:
+        arr = (ctypes.c_void_p * len(stage_events))(*[e.cuda_event for e in stage_events])
+        st = lib.gdn2_chunk_fwd_staged(*args, arr, len(stage_events))
+    if st != GDN2_OK:
+        raise Gdn2Error(st, "gdn2_chunk_fwd")
+    return out, final_state
+
+
+def device_status(workspace, stream=None) -> int:
+    """Device-side status word of the last call on ``workspace`` (syncs the stream)."""
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device).cuda_stream
+    s = ctypes.c_int32(-1)
+    st = load().gdn2_device_status(_ptr(workspace), stream, ctypes.byref(s))
+    if st != GDN2_OK:
+        raise Gdn2Error(st, "gdn2_device_status")
+    return int(s.value)
+
+
+def stage_names(dims: Dims):
+    lib = load()
+    return [lib.gdn2_stage_name(ctypes.byref(dims), i).decode()
+            for i in range(lib.gdn2_num_stages(ctypes.byref(dims)))]
+
+
+def launch_count(dims: Dims) -> int:
+    return int(load().gdn2_launch_count(ctypes.byref(dims)))
+
+
+class HostRunner:
+    """End-to-end call from HOST buffers: pinned host inputs are copied to
+    preallocated device buffers, the forward runs, and the output and final
+    state are copied back into pinned host buffers, all on one stream.  The
+    device buffers and workspace are allocated once (torch) and reused."""
+
+    def __init__(self, host: dict, impl="tc", use_qk_l2norm=False, output_final_state=True):
+        self.host = host
+        self.impl = impl
+        self.l2 = use_qk_l2norm
+        self.dev = {k: (torch.empty_like(v, device="cuda") if torch.is_tensor(v) else v)
+                    for k, v in host.items()}
+        T, HV, V = host["v"].shape
+        N = host["cu_seqlens"].numel() - 1
+        K = host["q"].shape[2]
+        self.out_host = torch.empty((T, HV, V), dtype=host["q"].dtype).pin_memory()
+        self.fs_host = (torch.empty((N, HV, K, V), dtype=torch.float32).pin_memory()
+                        if output_final_state else None)
+        self.out = torch.empty((T, HV, V), dtype=host["q"].dtype, device="cuda")
+        self.fs = torch.empty((N, HV, K, V), dtype=torch.float32, device="cuda") if output_final_state else None
+        dims = make_dims(self.dev["q"], self.dev["k"], self.dev["v"], self.dev["g"], self.dev["beta"],
+                         self.dev["w"], self.out, self.dev["cu_seqlens"], use_qk_l2norm, impl)
+        self.ws = torch.empty(max(workspace_bytes(dims), 256), dtype=torch.uint8, device="cuda")
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in host.values() if torch.is_tensor(v))
+        self.d2h_bytes = self.out_host.numel() * self.out_host.element_size() + (
+            0 if self.fs_host is None else self.fs_host.numel() * 4)
+
+    def __call__(self):
+        for k, v in self.host.items():
+            if torch.is_tensor(v):
+                self.dev[k].copy_(v, non_blocking=True)
+        d = self.dev
+        chunk_gdn2_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d.get("scale"),
+                       initial_state=d.get("h0"), cu_seqlens=d["cu_seqlens"],
+                       use_qk_l2norm=self.l2, out=self.out, final_state=self.fs,
+                       output_final_state=self.fs is not None, workspace=self.ws, impl=self.impl)
+        self.out_host.copy_(self.out, non_blocking=True)
+        if self.fs is not None:
+            self.fs_host.copy_(self.fs, non_blocking=True)
+        return self.out_host, self.fs_host

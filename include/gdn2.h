@@ -1,0 +1,210 @@
+/*
+ * gdn2.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet-2 chunked prefill
+ * forward.
+ *
+ * The operation is the GDN-2 recurrence of the FlashInfer docs page
+ * "flashinfer.gdn2_prefill.chunk_gated_delta_rule2" (op description), per
+ * sequence n and value head hv, with key head h = hv / (HV / H):
+ *
+ *     S_t   = diag(exp(g_t)) S_{t-1}
+ *     u_t   = w_t * v_t - (beta_t * k_t)^T S_t
+ *     S_t  += k_t u_t^T
+ *     o_t   = scale * q_t^T S_t
+ *
+ * S is a K x V fp32 matrix.  The library evaluates it in 64-token chunks in
+ * WY form (FlashRT gated-delta-attention page, "64-token WY blocks"; burn-gdn2
+ * README, "Fused CUDA kernels" and "Numerical stability") over packed
+ * variable-length sequences, as the FlashInfer docs' argument list describes.
+ *
+ * Conventions common to every entry point:
+ *  - All tensor pointers are DEVICE pointers unless stated otherwise.
+ *  - The caller owns every buffer, the workspace included.  The library never
+ *    allocates device memory, never synchronises the stream (except
+ *    gdn2_device_status, which says so) and never writes its inputs.
+ *  - Functions return a gdn2_status; GDN2_OK is 0.  Argument errors are found
+ *    on the host before anything is enqueued, so a non-zero return from
+ *    argument checking means nothing was launched.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    All work is enqueued asynchronously on it.
+ *  - The library is built for sm_103a only; other devices get GDN2_ERR_ARCH.
+ */
+#ifndef GDN2_H
+#define GDN2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GDN2_API __attribute__((visibility("default")))
+#else
+#define GDN2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn2_status {
+    GDN2_OK = 0,
+    GDN2_ERR_NULL = 1,        /* a required pointer is NULL                          */
+    GDN2_ERR_SHAPE = 2,       /* unsupported sizes (K, V), HV % H != 0, N < 0, ...    */
+    GDN2_ERR_STRIDE = 3,      /* innermost stride != 1, or a stride / base pointer    */
+                              /* is not a multiple of 16 bytes                        */
+    GDN2_ERR_ALIAS = 4,       /* out or final_state overlaps an input                 */
+    GDN2_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than gdn2_workspace_bytes  */
+    GDN2_ERR_ARCH = 6,        /* current device is not compute capability 10.3        */
+    GDN2_ERR_LAUNCH = 7,      /* a kernel launch failed (cudaGetLastError)            */
+    GDN2_ERR_DTYPE = 8,       /* unsupported dtype code                               */
+    GDN2_ERR_CU_SEQLENS = 9,  /* device-side: cu_seqlens[0] != 0, decreasing, or      */
+                              /* cu_seqlens[N] != T_tot (see gdn2_device_status)      */
+    GDN2_ERR_CUDA = 10,       /* another CUDA runtime error                           */
+    GDN2_ERR_IMPL = 11        /* unknown implementation selector                      */
+} gdn2_status;
+
+typedef enum gdn2_dtype {
+    GDN2_DTYPE_BF16 = 0,
+    GDN2_DTYPE_F32 = 2
+} gdn2_dtype;
+
+typedef enum gdn2_impl {
+    GDN2_IMPL_TC = 0,    /* default: tcgen05 / TMA kernels                          */
+    GDN2_IMPL_SIMT = 1   /* CUDA-core fp32 kernels of the same chunked algorithm;    */
+                         /* a second GPU path for cross-checks, never a fallback     */
+} gdn2_impl;
+
+/*
+ * Problem description.  Every token-major tensor X has element strides
+ * x_stride[0] (between tokens) and x_stride[1] (between heads); its innermost
+ * (channel) stride is 1 (FlashInfer docs: "only the innermost dimension has
+ * to be contiguous").  Strides are in ELEMENTS of that tensor's dtype and,
+ * like base pointers, must be multiples of 16 bytes.
+ *
+ *   q, k          [T_tot, H,  K]   bf16
+ *   v, w          [T_tot, HV, V]   bf16
+ *   g             [T_tot, HV, K]   fp32  (natural-log decay, <= 0)
+ *   beta          [T_tot, HV, K]   bf16  (erase gate, post-sigmoid; [0, 2] allowed)
+ *   out           [T_tot, HV, V]   bf16
+ *   initial_state [N, HV, K, V]    fp32, contiguous, K-major (row c = key channel)
+ *   final_state   [N, HV, K, V]    fp32, contiguous
+ *   cu_seqlens    [N + 1]          int32 (or int64 with cu_seqlens_i64 = 1)
+ *
+ * Supported sizes: K = V in {64, 128}; HV a positive multiple of H; N >= 0;
+ * T_tot >= 0 (T_tot = 0 writes only final_state = initial_state).
+ */
+typedef struct gdn2_dims {
+    int64_t T_tot;
+    int32_t N, H, HV, K, V;
+    int64_t q_stride[2], k_stride[2], v_stride[2], g_stride[2];
+    int64_t beta_stride[2], w_stride[2], o_stride[2];
+    int32_t dtype_qkv;      /* GDN2_DTYPE_BF16                                    */
+    int32_t dtype_g;        /* GDN2_DTYPE_F32                                     */
+    int32_t cu_seqlens_i64; /* 0: int32 cu_seqlens, 1: int64                      */
+    int32_t use_qk_l2norm;  /* 1: divide q, k rows by max(||x||_2, 1e-12) first   */
+                            /* (FlashInfer docs: use_qk_l2norm_in_kernel)         */
+    int32_t impl;           /* gdn2_impl                                          */
+    int32_t reserved;
+} gdn2_dims;
+
+/*
+ * Bytes of device workspace gdn2_chunk_fwd needs for `dims` (0 if dims is
+ * NULL or invalid).  The workspace holds the device-built chunk map, a status
+ * word and the chunk intermediates; it may be reused across calls that do
+ * not overlap on the GPU.  Host-only; no CUDA call.
+ */
+GDN2_API size_t gdn2_workspace_bytes(const gdn2_dims *dims);
+
+/*
+ * Fill `dims` for contiguous tensors of the given sizes (strides = packed
+ * row-major), dtype_qkv = bf16, dtype_g = fp32, int32 cu_seqlens, no L2
+ * norm, impl = GDN2_IMPL_TC.  Host-only.
+ */
+GDN2_API gdn2_status gdn2_dims_init(gdn2_dims *dims, int64_t T_tot, int32_t N, int32_t H, int32_t HV,
+                           int32_t K, int32_t V);
+
+/*
+ * Validate arguments exactly as gdn2_chunk_fwd does, without touching the
+ * device: pointers, sizes, strides, dtypes, aliasing and workspace size.
+ * Host-only; returns the status gdn2_chunk_fwd would return before launching.
+ */
+GDN2_API gdn2_status gdn2_check_args(const void *q, const void *k, const void *v, const void *g,
+                            const void *beta, const void *w, const float *initial_state,
+                            const void *cu_seqlens, const void *out, const float *final_state,
+                            const gdn2_dims *dims, const void *workspace,
+                            size_t workspace_bytes);
+
+/*
+ * The chunked GDN-2 prefill forward (FlashInfer docs, chunk_gated_delta_rule2:
+ * signature and parameters; the argument order follows it).
+ *
+ *   g             may be NULL: no decay (g = 0)
+ *   beta          may be NULL: beta = 1
+ *   w             may be NULL: w = 1
+ *   scale         query scale; <= 0 means 1/sqrt(K)
+ *   initial_state may be NULL: zero state
+ *   final_state   may be NULL: not written.  Must not overlap initial_state.
+ *   out           written in place; must not overlap any input
+ *   workspace     device buffer of at least gdn2_workspace_bytes(dims) bytes
+ *
+ * Chunks are 64 tokens and never span two sequences; an empty sequence
+ * returns final_state = initial_state.  Numerics: bf16 tensor-core operands,
+ * fp32 accumulation and fp32 carried state; chunk-local decays are applied
+ * through 16-token sub-chunk references (burn-gdn2 README, "Numerical
+ * stability"), which stays finite while no key channel decays by more than
+ * about 80 nats inside one 16-token sub-chunk (|g| <= 5 per token is always
+ * inside this range).
+ *
+ * Returns GDN2_OK once all kernels are enqueued.  cu_seqlens is checked on
+ * the device; a bad cu_seqlens makes every kernel a no-op and is reported by
+ * gdn2_device_status.
+ */
+GDN2_API gdn2_status gdn2_chunk_fwd(const void *q, const void *k, const void *v, const void *g,
+                           const void *beta, const void *w, float scale,
+                           const float *initial_state, const void *cu_seqlens, void *out,
+                           float *final_state, const gdn2_dims *dims, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * Same as gdn2_chunk_fwd, and additionally records caller-created CUDA events
+ * (cudaEvent_t passed as void*) on `stream` at the boundaries of the launch
+ * sequence: events[i] just before stage i and events[n_stages] after the
+ * last, where n_stages = gdn2_num_stages(dims) and n_events must be at least
+ * n_stages + 1 (else GDN2_ERR_NULL).  Used to time each kernel on the stream
+ * it runs on.  Stage names: gdn2_stage_name.
+ */
+GDN2_API gdn2_status gdn2_chunk_fwd_staged(const void *q, const void *k, const void *v, const void *g,
+                                           const void *beta, const void *w, float scale,
+                                           const float *initial_state, const void *cu_seqlens,
+                                           void *out, float *final_state, const gdn2_dims *dims,
+                                           void *workspace, size_t workspace_bytes, void *stream,
+                                           void *const *events, int32_t n_events);
+
+/* Number of timed stages of the launch sequence for `dims` (0 if invalid).
+ * Host-only. */
+GDN2_API int32_t gdn2_num_stages(const gdn2_dims *dims);
+
+/* Static name of stage i ("prep", "intra", ...), NULL if out of range.
+ * Host-only. */
+GDN2_API const char *gdn2_stage_name(const gdn2_dims *dims, int32_t i);
+
+/* Number of kernel launches one gdn2_chunk_fwd call makes for `dims`
+ * (0 if invalid).  Host-only. */
+GDN2_API int32_t gdn2_launch_count(const gdn2_dims *dims);
+
+/*
+ * Read the device-side status word that the last gdn2_chunk_fwd on this
+ * workspace wrote (GDN2_OK or GDN2_ERR_CU_SEQLENS) into *status.  This call
+ * SYNCHRONISES `stream`.  Returns GDN2_ERR_CUDA if the copy fails.
+ */
+GDN2_API gdn2_status gdn2_device_status(const void *workspace, void *stream, int32_t *status);
+
+/* Static, human-readable text for a status code.  Host-only. */
+GDN2_API const char *gdn2_status_string(int status);
+
+/* Library ABI version: (major << 16) | minor.  Host-only. */
+GDN2_API int32_t gdn2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN2_H */

@@ -1,0 +1,152 @@
+"""The C-ABI library on the host: it loads, exports every symbol the header
+declares, and rejects bad arguments before touching a device.  No kernel is
+launched here (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from gated_deltanet_prefill_gb300 import build as gbuild
+from gated_deltanet_prefill_gb300 import gdn2
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdn2.load()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "gdn2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"GDN2_API\s+[\w\s\*]+?\b(gdn2_\w+)\s*\(", src)))
+
+
+def test_header_declares_entry_points():
+    fns = header_functions()
+    assert "gdn2_chunk_fwd" in fns and "gdn2_workspace_bytes" in fns
+    assert set(fns) == set(gdn2.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for fn in header_functions():
+        assert hasattr(lib, fn), fn
+
+
+def test_version_and_strings(lib):
+    assert lib.gdn2_version() >> 16 == 1
+    for code in range(12):
+        s = lib.gdn2_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.gdn2_status_string(999).decode() == "unknown status"
+
+
+def _dims(lib, T=256, N=2, H=2, HV=4, K=64, V=64):
+    d = gdn2.Dims()
+    assert lib.gdn2_dims_init(ctypes.byref(d), T, N, H, HV, K, V) == 0
+    return d
+
+
+# Fake, well-separated, 256-byte aligned "device" addresses: the checks are
+# host arithmetic only and never dereference them.
+BASE = 1 << 40
+
+
+def _ptrs(d, ws_bytes):
+    MB = 1 << 26
+    names = ["q", "k", "v", "g", "beta", "w", "h0", "cu", "out", "hT", "ws"]
+    return {n: BASE + i * MB for i, n in enumerate(names)}
+
+
+def _check(lib, d, p, ws_bytes=None, **over):
+    p = {**p, **over}
+    if ws_bytes is None:
+        ws_bytes = lib.gdn2_workspace_bytes(ctypes.byref(d))
+    return lib.gdn2_check_args(p["q"], p["k"], p["v"], p["g"], p["beta"], p["w"], p["h0"], p["cu"],
+                               p["out"], p["hT"], ctypes.byref(d), p["ws"], ws_bytes)
+
+
+def test_workspace_bytes(lib):
+    d = _dims(lib)
+    n = lib.gdn2_workspace_bytes(ctypes.byref(d))
+    assert n > 0
+    d2 = _dims(lib, T=512)
+    assert lib.gdn2_workspace_bytes(ctypes.byref(d2)) > n
+    bad = _dims(lib)
+    bad.K = 96
+    assert lib.gdn2_workspace_bytes(ctypes.byref(bad)) == 0
+
+
+def test_check_args_ok(lib):
+    d = _dims(lib)
+    assert _check(lib, d, _ptrs(d, 0)) == 0
+
+
+def test_check_args_errors(lib):
+    d = _dims(lib)
+    p = _ptrs(d, 0)
+    assert _check(lib, d, p, q=None) == 1                 # ERR_NULL
+    assert _check(lib, d, p, cu=None) == 1
+    assert _check(lib, d, p, ws=None) == 1
+    assert _check(lib, d, p, ws_bytes=100) == 5           # ERR_WORKSPACE
+    assert _check(lib, d, p, q=p["q"] + 8) == 3           # ERR_STRIDE: base not 16B aligned
+    assert _check(lib, d, p, out=p["v"]) == 4             # ERR_ALIAS: out == v
+    assert _check(lib, d, p, hT=p["h0"]) == 4             # final_state == initial_state
+    assert _check(lib, d, p, out=p["hT"]) == 4
+    # optional gates may be NULL
+    assert _check(lib, d, p, g=None, beta=None, w=None, h0=None, hT=None) == 0
+    for field, val, code in (("K", 96, 2), ("HV", 3, 2), ("N", -1, 2), ("dtype_qkv", 1, 8),
+                             ("dtype_g", 0, 8), ("impl", 7, 11)):
+        d2 = _dims(lib)
+        setattr(d2, field, val)
+        assert _check(lib, d2, p, ws_bytes=1 << 30) == code, field
+    d3 = _dims(lib)
+    d3.q_stride[0] = 2 * 64 + 4                           # 264 bytes: not a multiple of 16
+    assert _check(lib, d3, p) == 3
+    d4 = _dims(lib)
+    d4.o_stride[1] = 32                                   # heads of out overlap
+    assert _check(lib, d4, p) == 4
+
+
+def test_chunk_fwd_rejects_before_launch(lib):
+    """gdn2_chunk_fwd returns the argument error without any CUDA call."""
+    d = _dims(lib)
+    p = _ptrs(d, 0)
+    ws = lib.gdn2_workspace_bytes(ctypes.byref(d))
+    st = lib.gdn2_chunk_fwd(None, p["k"], p["v"], p["g"], p["beta"], p["w"], ctypes.c_float(0.0),
+                            p["h0"], p["cu"], p["out"], p["hT"], ctypes.byref(d), p["ws"], ws, None)
+    assert st == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device error")
+def test_chunk_fwd_without_device_fails_loudly(lib):
+    """With valid arguments but no CUDA device the call fails with ERR_ARCH
+    (there is no CPU path)."""
+    d = _dims(lib)
+    p = _ptrs(d, 0)
+    ws = lib.gdn2_workspace_bytes(ctypes.byref(d))
+    st = lib.gdn2_chunk_fwd(p["q"], p["k"], p["v"], p["g"], p["beta"], p["w"], ctypes.c_float(0.0),
+                            p["h0"], p["cu"], p["out"], p["hT"], ctypes.byref(d), p["ws"], ws, None)
+    assert st == 6
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    q = torch.zeros(64, 1, 64, dtype=torch.bfloat16)
+    cu = torch.tensor([0, 64], dtype=torch.int32)
+    with pytest.raises(ValueError):
+        gdn2.chunk_gdn2_fwd(q, q, q, cu_seqlens=cu)
+
+
+def test_product_package_does_not_import_oracle():
+    """The product package never reaches into oracle/ (no CPU fallback)."""
+    pkg = os.path.join(ROOT, "gated_deltanet_prefill_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", src, re.M), f
+                assert "gdn2_oracle" not in src, f

@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA library against the FP64 oracle on the same inputs.
+
+Bar (GDN-2 prefill forward): max|o - o_ref| / max|o_ref| <= 1e-2, and the
+same bound on the final state, per compared set of outputs.  Small cases are
+compared element by element; the full-size workloads on sampled
+(sequence, value head) units that the oracle computes one by one, in the
+launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_prefill_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-2
+IMPLS = ["simt"]
+
+
+def rel_max(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.isfinite(x).all(), "non-finite output"
+    return float(np.abs(x - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def to_dev(d):
+    return {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in d.items()}
+
+
+def run_gpu(gdn2, d, impl, **kw):
+    o, hT = gdn2.chunk_gdn2_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                                initial_state=d["h0"], cu_seqlens=d["cu_seqlens"], impl=impl, **kw)
+    torch.cuda.synchronize()
+    return o, hT
+
+
+def run_oracle(d, **kw):
+    return oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                               initial_state=d["h0"], cu_seqlens=d["cu_seqlens"], **kw)
+
+
+def check_full(gdn2, wl, impl, tol=TOL, **kw):
+    d = inputs.generate(wl)
+    o_ref, h_ref = run_oracle(d, use_qk_l2norm=kw.get("use_qk_l2norm", False))
+    o, hT = run_gpu(gdn2, to_dev(d), impl, **kw)
+    eo = rel_max(o.float().cpu().numpy(), o_ref) if wl.T_tot else 0.0
+    eh = rel_max(hT.cpu().numpy(), h_ref)
+    assert eo <= tol and eh <= tol, "%s/%s: o err %.3e, state err %.3e" % (wl.name, impl, eo, eh)
+    return eo, eh
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_tiny_workload(cuda_lib, impl):
+    check_full(cuda_lib, inputs.workload(1), impl)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("D", [64, 128])
+def test_ragged_varlen_gva(cuda_lib, impl, D):
+    """Partial chunks (1, 63, 65, ...), an empty sequence, several tiles per
+    sequence, grouped value heads and an initial state."""
+    wl = inputs.small("ragged", [1, 63, 64, 65, 0, 200, 130], H=2, HV=4, K=D, V=D, g_max=0.5,
+                      beta_max=2.0, h0_std=0.05, seed=31)
+    check_full(cuda_lib, wl, impl)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_strong_decay(cuda_lib, impl):
+    """g = -U(0,3), beta in [0,2]: the decay-stress regime at small size."""
+    wl = inputs.small("decay", [300, 77], H=2, HV=2, K=128, V=128, g_max=3.0, beta_max=2.0,
+                      h0_std=0.05, seed=32)
+    check_full(cuda_lib, wl, impl)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_missing_gates(cuda_lib, impl):
+    wl = inputs.small("nogates", [129, 40], H=1, HV=2, K=64, V=64, seed=33)
+    d = inputs.generate(wl)
+    d["g"] = d["beta"] = d["w"] = None
+    o_ref, h_ref = run_oracle(d)
+    o, hT = run_gpu(cuda_lib, to_dev(d), impl)
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_l2norm_in_kernel(cuda_lib, impl):
+    wl = inputs.small("l2", [150], H=2, HV=2, K=128, V=128, seed=34)
+    d = inputs.generate(wl)
+    d["q"] = (d["q"].float() * 3.0).to(torch.bfloat16)
+    d["k"] = (d["k"].float() * 0.25).to(torch.bfloat16)
+    o_ref, h_ref = run_oracle(d, use_qk_l2norm=True)
+    o, hT = run_gpu(cuda_lib, to_dev(d), impl, use_qk_l2norm=True)
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_strided_inputs_and_int64_cu(cuda_lib, impl):
+    """Token/head strides other than packed (only the channel dim contiguous)
+    and int64 cu_seqlens."""
+    wl = inputs.small("strided", [100, 37], H=2, HV=2, K=64, V=64, h0_std=0.05, seed=35)
+    d = inputs.generate(wl)
+    o_ref, h_ref = run_oracle(d)
+    dd = to_dev(d)
+    for key in ("q", "k", "v", "beta", "w", "g"):
+        x = dd[key]
+        big = torch.zeros(x.shape[0], x.shape[1], 2 * x.shape[2], dtype=x.dtype, device=x.device)
+        big[..., :x.shape[2]] = x
+        dd[key] = big[..., :x.shape[2]]
+        assert not dd[key].is_contiguous()
+    dd["cu_seqlens"] = dd["cu_seqlens"].long()
+    out_big = torch.zeros(wl.T_tot, wl.HV, 2 * wl.V, dtype=torch.bfloat16, device="cuda")
+    o, hT = run_gpu(cuda_lib, dd, impl, out=out_big[..., :wl.V])
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert float(out_big[..., wl.V:].abs().max()) == 0.0, "wrote outside the strided output"
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_split_sequence_matches_one_pass(cuda_lib, impl):
+    """Prefill in two calls carrying the final state equals one call
+    (FlashGDN-2 quick start: prefill, then continue from the state)."""
+    wl = inputs.small("split", [257], H=2, HV=2, K=128, V=128, h0_std=0.05, seed=36)
+    d = to_dev(inputs.generate(wl))
+    o, hT = run_gpu(cuda_lib, d, impl)
+    t = 100
+    a = {**d, **{x: d[x][:t] for x in ("q", "k", "v", "g", "beta", "w")},
+         "cu_seqlens": torch.tensor([0, t], dtype=torch.int32, device="cuda")}
+    o1, h1 = run_gpu(cuda_lib, a, impl)
+    b = {**d, **{x: d[x][t:] for x in ("q", "k", "v", "g", "beta", "w")}, "h0": h1,
+         "cu_seqlens": torch.tensor([0, 257 - t], dtype=torch.int32, device="cuda")}
+    o2, h2 = run_gpu(cuda_lib, b, impl)
+    assert rel_max(torch.cat([o1, o2]).float().cpu().numpy(), o.float().cpu().numpy()) <= TOL
+    assert rel_max(h2.cpu().numpy(), hT.cpu().numpy()) <= TOL
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_empty_tokens_keep_state(cuda_lib, impl):
+    """T_tot = 0 with N = 2 sequences: final_state = initial_state."""
+    h0 = torch.randn(2, 2, 64, 64, device="cuda")
+    z = torch.zeros(0, 2, 64, dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros(0, 2, 64, device="cuda")
+    cu = torch.tensor([0, 0, 0], dtype=torch.int32, device="cuda")
+    o, hT = cuda_lib.chunk_gdn2_fwd(z, z, z, g, z, z, initial_state=h0, cu_seqlens=cu, impl=impl)
+    torch.cuda.synchronize()
+    assert torch.equal(hT, h0)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_bad_cu_seqlens_reported_on_device(cuda_lib, impl):
+    wl = inputs.small("badcu", [64, 64], H=1, HV=1, K=64, V=64, seed=37)
+    d = to_dev(inputs.generate(wl))
+    d["cu_seqlens"] = torch.tensor([0, 100, 64], dtype=torch.int32, device="cuda")  # decreasing
+    ws = torch.empty(1 << 22, dtype=torch.uint8, device="cuda")
+    run_gpu(cuda_lib, d, impl, workspace=ws)
+    assert cuda_lib.device_status(ws) == 9
+    d["cu_seqlens"] = torch.tensor([0, 64, 128], dtype=torch.int32, device="cuda")
+    run_gpu(cuda_lib, d, impl, workspace=ws)
+    assert cuda_lib.device_status(ws) == 0
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads: run the whole launch, compare sampled units.
+# ---------------------------------------------------------------------------
+def sample_units(wl, k=3, seed=0):
+    rng = np.random.default_rng(seed)
+    lens = np.array(wl.lens)
+    n_long = int(np.argmax(lens))
+    units = {(n_long, wl.HV - 1), (0, 0)}
+    while len(units) < k + 2:
+        units.add((int(rng.integers(wl.N)), int(rng.integers(wl.HV))))
+    return sorted(units)
+
+
+def unit_problem(d, wl, n, hv):
+    """Inputs of one (sequence, value head) unit as a stand-alone problem."""
+    cu = d["cu_seqlens"].tolist()
+    a, b = cu[n], cu[n + 1]
+    h = hv // (wl.HV // wl.H)
+    sl = lambda x, head: None if x is None else x[a:b, head:head + 1].cpu()
+    return dict(q=sl(d["q"], h), k=sl(d["k"], h), v=sl(d["v"], hv), g=sl(d["g"], hv),
+                beta=sl(d["beta"], hv), w=sl(d["w"], hv),
+                h0=None if d["h0"] is None else d["h0"][n:n + 1, hv:hv + 1].cpu(),
+                cu_seqlens=[0, b - a], scale=d["scale"]), (a, b)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("index", [2, 3, 4, 5])
+def test_full_size_sampled(cuda_lib, impl, index):
+    wl = inputs.workload(index)
+    d = inputs.generate(wl, device="cuda")
+    o, hT = run_gpu(cuda_lib, d, impl)
+    from concurrent.futures import ThreadPoolExecutor
+
+    units = sample_units(wl)
+
+    def one(u):
+        n, hv = u
+        pd, (a, b) = unit_problem(d, wl, n, hv)
+        o_ref, h_ref = run_oracle(pd)
+        return u, (a, b), o_ref[:, 0], h_ref[0, 0]
+
+    with ThreadPoolExecutor(4) as ex:
+        res = list(ex.map(one, units))
+    o_cat, r_cat, h_cat, hr_cat = [], [], [], []
+    for (n, hv), (a, b), o_ref, h_ref in res:
+        o_cat.append(o[a:b, hv].float().cpu().numpy()); r_cat.append(o_ref)
+        h_cat.append(hT[n, hv].cpu().numpy()); hr_cat.append(h_ref)
+    eo = rel_max(np.concatenate(o_cat), np.concatenate(r_cat))
+    eh = rel_max(np.stack(h_cat), np.stack(hr_cat))
+    assert eo <= TOL and eh <= TOL, "%s/%s: o err %.3e, state err %.3e" % (wl.name, impl, eo, eh)
