@@ -217,6 +217,13 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     p.Ut = reinterpret_cast<bf16 *>(ws + L.Ut);
     p.hbuf = reinterpret_cast<bf16 *>(ws + L.hbuf);
     p.vnew = reinterpret_cast<bf16 *>(ws + L.vnew);
+    p.q_in = p.q; p.k_in = p.k;
+    p.sq_in_t = p.sq_t; p.sq_in_h = p.sq_h; p.sk_in_t = p.sk_t; p.sk_in_h = p.sk_h;
+    if (p.l2norm) {  // chunk kernels read the normalised packed copies
+        p.q = p.qn; p.k = p.kn;
+        p.sq_t = p.sk_t = static_cast<int64_t>(p.H) * p.K;
+        p.sq_h = p.sk_h = p.K;
+    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaGetLastError();  // clear a stale error so the checks below see only ours

@@ -19,7 +19,12 @@ using bf16 = __nv_bfloat16;
 // Everything a kernel needs, passed by value.  Token-major tensors carry
 // element strides (token, head); the channel stride is 1.
 struct Params {
+    // q, k: what the chunk kernels read.  With the fused L2 norm these point
+    // at the normalised copies in the workspace (packed [T_tot, H, K]) and
+    // q_in / k_in hold the caller's tensors for the norm kernel.
     const bf16 *q, *k, *v, *beta, *w;
+    const bf16 *q_in, *k_in;
+    int64_t sq_in_t, sq_in_h, sk_in_t, sk_in_h;
     const float *g;
     int64_t sq_t, sq_h, sk_t, sk_h, sv_t, sv_h, sg_t, sg_h, sb_t, sb_h, sw_t, sw_h, so_t, so_h;
     bf16 *o;

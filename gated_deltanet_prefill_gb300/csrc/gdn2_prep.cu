@@ -109,7 +109,7 @@ __global__ void l2norm_kernel(Params p) {
     const int64_t t = row / p.H;
     const int h = static_cast<int>(row % p.H);
     for (int which = 0; which < 2; ++which) {
-        const bf16 *src = which ? p.k + t * p.sk_t + h * p.sk_h : p.q + t * p.sq_t + h * p.sq_h;
+        const bf16 *src = which ? p.k_in + t * p.sk_in_t + h * p.sk_in_h : p.q_in + t * p.sq_in_t + h * p.sq_in_h;
         bf16 *dst = (which ? p.kn : p.qn) + row * p.K;
         float x[4];
         float ss = 0.f;

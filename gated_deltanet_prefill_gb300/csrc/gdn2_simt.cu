@@ -30,22 +30,6 @@ __device__ __forceinline__ int sub_end(int r, int len) {  // last row of r's sub
     return min((r / kSub) * kSub + kSub - 1, len - 1);
 }
 
-template <int D>
-struct TokenPtrs {
-    const bf16 *q, *k;
-    int64_t sq_t, sq_h, sk_t, sk_h;
-    __device__ TokenPtrs(const Params &p) {
-        if (p.l2norm) {
-            q = p.qn; k = p.kn;
-            sq_t = sk_t = static_cast<int64_t>(p.H) * D;
-            sq_h = sk_h = D;
-        } else {
-            q = p.q; k = p.k;
-            sq_t = p.sq_t; sq_h = p.sq_h; sk_t = p.sk_t; sk_h = p.sk_h;
-        }
-    }
-};
-
 // ---------------------------------------------------------------------------
 // Intra-chunk: A, T = (I + A)^{-1}, Wt, Ut.  One CTA per (chunk, value head).
 // ---------------------------------------------------------------------------
@@ -67,7 +51,6 @@ __global__ void __launch_bounds__(kIntraThreads) simt_intra_kernel(Params p) {
     const int64_t start = p.chunk_start[c];
     const int len = p.chunk_len[c];
     const int h = hv / p.group;
-    const TokenPtrs<D> tp(p);
 
     for (int i = tid; i < 64 * D; i += kIntraThreads) {
         const int r = i / D, ch = i % D;
@@ -76,7 +59,7 @@ __global__ void __launch_bounds__(kIntraThreads) simt_intra_kernel(Params p) {
         Gs[r * LD + ch] = p.G[(t * p.HV + hv) * D + ch];
         float kv = 0.f, bv = 0.f;
         if (r < len) {
-            kv = __bfloat162float(tp.k[t * tp.sk_t + h * tp.sk_h + ch]);
+            kv = __bfloat162float(p.k[t * p.sk_t + h * p.sk_h + ch]);
             bv = p.has_beta ? __bfloat162float(p.beta[t * p.sb_t + hv * p.sb_h + ch]) : 1.f;
         }
         Ks[r * LD + ch] = kv;
@@ -169,7 +152,6 @@ __global__ void __launch_bounds__(D) simt_state_kernel(Params p) {
     if (p.status[0] != GDN2_OK) return;
     const int n = blockIdx.x, hv = blockIdx.y, v0 = blockIdx.z * VT, c = threadIdx.x;
     const int h = hv / p.group;
-    const TokenPtrs<D> tp(p);
     float S[VT];
     const size_t sbase = ((static_cast<size_t>(n) * p.HV + hv) * D + c) * D + v0;
 #pragma unroll
@@ -208,7 +190,7 @@ __global__ void __launch_bounds__(D) simt_state_kernel(Params p) {
         for (int j = 0; j < VT; ++j) S[j] *= a;
         for (int t = 0; t < len; ++t) {
             const int64_t tok = start + t;
-            const float kd = __bfloat162float(tp.k[tok * tp.sk_t + h * tp.sk_h + c]) *
+            const float kd = __bfloat162float(p.k[tok * p.sk_t + h * p.sk_h + c]) *
                              __expf(GL - p.G[(tok * p.HV + hv) * D + c]);
 #pragma unroll
             for (int j = 0; j < VT; ++j) S[j] += kd * Us[t * (VT + 1) + j];
@@ -243,14 +225,13 @@ __global__ void __launch_bounds__(kOutThreads) simt_output_kernel(Params p) {
     const int64_t start = p.chunk_start[c];
     const int len = p.chunk_len[c];
     const int h = hv / p.group;
-    const TokenPtrs<D> tp(p);
 
     for (int i = tid; i < 64 * D; i += kOutThreads) {
         const int r = i / D, ch = i % D;
         const int64_t t = start + min(r, len - 1);
         Gs[r * LD + ch] = p.G[(t * p.HV + hv) * D + ch];
-        Rs[r * LD + ch] = r < len ? __bfloat162float(tp.k[t * tp.sk_t + h * tp.sk_h + ch]) : 0.f;
-        Qs[r * LD + ch] = r < len ? __bfloat162float(tp.q[t * tp.sq_t + h * tp.sq_h + ch]) : 0.f;
+        Rs[r * LD + ch] = r < len ? __bfloat162float(p.k[t * p.sk_t + h * p.sk_h + ch]) : 0.f;
+        Qs[r * LD + ch] = r < len ? __bfloat162float(p.q[t * p.sq_t + h * p.sq_h + ch]) : 0.f;
     }
     for (int i = tid; i < 64 * 65; i += kOutThreads) Ps[i] = 0.f;
     __syncthreads();
