@@ -201,55 +201,56 @@ class Clocks:
 # ---------------------------------------------------------------------------
 # oracle timing (CPU baseline and reference arm)
 # ---------------------------------------------------------------------------
-def oracle_sample(d, wl, n_tokens, n_units):
-    """The first n_tokens of sequence 0 for value heads 0..n_units-1, as
-    separate stand-alone units on the host."""
-    import torch
-    a = 0
-    b = a + n_tokens
+def unit_batch(d, wl, units, n_tokens=None):
+    """Stand-alone float64 host problem made of whole (sequence, value head)
+    units (or their first n_tokens): unit i becomes packed sequence i with
+    one key head and one value head."""
+    import numpy as np
+    cu = d["cu_seqlens"].tolist()
     group = wl.HV // wl.H
-    cols_v = list(range(n_units))
-    cols_k = [hv // group for hv in cols_v]
-    take = lambda x, cols: None if x is None else x[a:b][:, cols].cpu()
-    # one packed problem: unit i = head i; q/k expanded per value head
-    q = take(d["q"], cols_k); k = take(d["k"], cols_k)
-    v = take(d["v"], cols_v); g = take(d["g"], cols_v)
-    beta = take(d["beta"], cols_v); w = take(d["w"], cols_v)
-    h0 = None if d["h0"] is None else d["h0"][0:1, cols_v].cpu()
-    return dict(q=q, k=k, v=v, g=g, beta=beta, w=w, h0=h0,
-                cu_seqlens=torch.tensor([0, n_tokens]), scale=d["scale"])
+    parts = {k: [] for k in ("q", "k", "v", "g", "beta", "w", "h0")}
+    lens = []
+    for n, hv in units:
+        a = cu[n]
+        b = cu[n + 1] if n_tokens is None else min(cu[n + 1], a + n_tokens)
+        h = hv // group
+        for key, head in (("q", h), ("k", h), ("v", hv), ("g", hv), ("beta", hv), ("w", hv)):
+            parts[key].append(d[key][a:b, head:head + 1].double().cpu().numpy())
+        if d["h0"] is not None:
+            parts["h0"].append(d["h0"][n:n + 1, hv:hv + 1].double().cpu().numpy())
+        lens.append(b - a)
+    out = {k: (np.concatenate(v) if v else None) for k, v in parts.items()}
+    out["cu_seqlens"] = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    out["scale"] = d["scale"]
+    out["tokens"] = int(sum(lens))
+    return out
 
 
-def time_oracle(sample, threads):
+def time_oracle(b, threads):
+    """Wall time of the oracle's C call on a prepared float64 batch."""
     import oracle
     t0 = time.perf_counter()
-    oracle.gdn2_forward(sample["q"], sample["k"], sample["v"], sample["g"], sample["beta"],
-                        sample["w"], scale=sample["scale"], initial_state=sample["h0"],
-                        cu_seqlens=sample["cu_seqlens"], threads=threads)
+    oracle.gdn2_forward(b["q"], b["k"], b["v"], b["g"], b["beta"], b["w"], scale=b["scale"],
+                        initial_state=b["h0"], cu_seqlens=b["cu_seqlens"], threads=threads)
     return time.perf_counter() - t0
 
 
-def size_oracle_sample(d, wl, seconds):
-    """Pick (tokens, units) so the oracle runs about `seconds` on the host."""
-    cores = os.cpu_count() or 1
-    units = max(1, min(wl.HV, cores))
-    probe_tokens = min(wl.lens[0], 256)
-    t = time_oracle(oracle_sample(d, wl, probe_tokens, units), units)
-    per_token = t / probe_tokens
-    n_tok = int(seconds / max(per_token, 1e-9))
-    n_tok = max(64, min(wl.lens[0], (n_tok // 64) * 64))
-    return n_tok, units
-
-
 def cpu_baseline(d, wl, seconds):
-    n_tok, units = size_oracle_sample(d, wl, seconds)
-    s = oracle_sample(d, wl, n_tok, units)
-    dt = time_oracle(s, units)
-    token_heads = n_tok * units
-    return {"value": token_heads / wl.HV / dt, "unit": "tokens/s", "cores": units, "kind": "oracle",
-            "sample": "FP64 oracle, sequence 0 tokens [0,%d) x %d of %d value heads (%d token-heads) "
-                      "in %.1f s on %d threads; tokens/s = token-heads / HV / s"
-                      % (n_tok, units, wl.HV, token_heads, dt, units)}
+    """The oracle, as it stands, on the host cores over a bounded sample:
+    whole (sequence, value head) units in order, one batch of `threads`
+    units at a time, until about `seconds` of oracle time is spent."""
+    threads = max(1, min(os.cpu_count() or 1, wl.N * wl.HV))
+    all_units = [(n, hv) for n in range(wl.N) for hv in range(wl.HV)]
+    total_t, tokens, done = 0.0, 0, 0
+    while done < len(all_units) and total_t < seconds:
+        batch = unit_batch(d, wl, all_units[done:done + threads])
+        total_t += time_oracle(batch, threads)
+        tokens += batch["tokens"]
+        done += min(threads, len(all_units) - done)
+    return {"value": tokens / wl.HV / total_t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": "FP64 oracle on %d of %d whole (sequence, value head) units (%d token-heads), "
+                      "%.1f s on %d threads; tokens/s = token-heads / HV / s"
+                      % (done, len(all_units), tokens, total_t, threads)}
 
 
 # ---------------------------------------------------------------------------
@@ -267,14 +268,18 @@ def run_reference(args):
     wl_s = inputs.Workload(wl.name + "_slice", small_lens, wl.H, wl.HV, wl.K, wl.V, g_max=wl.g_max,
                            beta_max=wl.beta_max, h0_std=wl.h0_std, seed=wl.seed, scale=wl.scale)
     d = inputs.generate(wl_s)
+    threads = max(1, min(os.cpu_count() or 1, wl.HV))
+    units = [(0, hv) for hv in range(threads)]
     per_step = max(2.0, 90.0 / max(1, args.steps + args.warmup))
-    n_tok, units = size_oracle_sample(d, wl_s, per_step)
-    s = oracle_sample(d, wl_s, n_tok, units)
+    probe = time_oracle(unit_batch(d, wl_s, units, 256), threads) / 256
+    n_tok = max(64, min(wl_s.lens[0], int(per_step / max(probe, 1e-9)) // 64 * 64))
+    b = unit_batch(d, wl_s, units, n_tok)
     for _ in range(args.warmup):
-        time_oracle(s, units)
-    times = [time_oracle(s, units) for _ in range(args.steps)]
+        time_oracle(b, threads)
+    times = [time_oracle(b, threads) for _ in range(args.steps)]
     dt = sum(times) / len(times)
-    val = n_tok * units / wl.HV / dt
+    val = n_tok * threads / wl.HV / dt
+    units = threads
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

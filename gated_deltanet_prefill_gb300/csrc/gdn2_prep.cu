@@ -19,7 +19,7 @@ constexpr int kMapThreads = 1024;
 
 // One CTA: validate cu_seqlens, scan the per-sequence chunk counts, fill the
 // per-chunk table.  Invalid cu_seqlens -> status word set, zero chunks.
-__global__ void __launch_bounds__(kMapThreads) chunk_map_kernel(Params p) {
+__global__ void __launch_bounds__(kMapThreads) gdn2_chunk_map_kernel(Params p) {
     __shared__ int s_bad;
     __shared__ int s_scan[kMapThreads];
     __shared__ int s_total;
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kMapThreads) chunk_map_kernel(Params p) {
 
 // Chunk-local inclusive cumsum of g, one CTA per (chunk, value head), one
 // thread per key channel.  Absent g -> G = 0.
-__global__ void cumsum_kernel(Params p) {
+__global__ void gdn2_cumsum_kernel(Params p) {
     const int c = blockIdx.x, hv = blockIdx.y, ch = threadIdx.x;
     const int seq = p.chunk_seq[c];
     if (seq < 0) return;
@@ -102,7 +102,7 @@ __global__ void cumsum_kernel(Params p) {
 }
 
 // Row L2 norm of q and k, one warp per (token, head) row, fp32 math, bf16 out.
-__global__ void l2norm_kernel(Params p) {
+__global__ void gdn2_l2norm_kernel(Params p) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     if (row >= p.T_tot * p.H) return;
@@ -127,7 +127,7 @@ __global__ void l2norm_kernel(Params p) {
 }  // namespace
 
 cudaError_t launch_chunk_map(const Params &p, cudaStream_t s) {
-    chunk_map_kernel<<<1, kMapThreads, 0, s>>>(p);
+    gdn2_chunk_map_kernel<<<1, kMapThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
@@ -135,9 +135,9 @@ cudaError_t launch_prep(const Params &p, cudaStream_t s) {
     if (p.l2norm && p.T_tot > 0) {
         const int64_t rows = p.T_tot * p.H;
         const int per_block = 8;
-        l2norm_kernel<<<static_cast<unsigned>((rows + per_block - 1) / per_block), 32 * per_block, 0, s>>>(p);
+        gdn2_l2norm_kernel<<<static_cast<unsigned>((rows + per_block - 1) / per_block), 32 * per_block, 0, s>>>(p);
     }
-    if (p.NCmax > 0) cumsum_kernel<<<dim3(p.NCmax, p.HV), p.K, 0, s>>>(p);
+    if (p.NCmax > 0) gdn2_cumsum_kernel<<<dim3(p.NCmax, p.HV), p.K, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -34,7 +34,7 @@ __device__ __forceinline__ int sub_end(int r, int len) {  // last row of r's sub
 // Intra-chunk: A, T = (I + A)^{-1}, Wt, Ut.  One CTA per (chunk, value head).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kIntraThreads) simt_intra_kernel(Params p) {
+__global__ void __launch_bounds__(kIntraThreads) gdn2_simt_intra_kernel(Params p) {
     constexpr int LD = D + 1;
     extern __shared__ float sm[];
     float *Gs = sm;               // [64][LD] G
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kIntraThreads) simt_intra_kernel(Params p) {
 // Writes the state entering each chunk (bf16), u_t (bf16), final state (fp32).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(D) simt_state_kernel(Params p) {
+__global__ void __launch_bounds__(D) gdn2_simt_state_kernel(Params p) {
     constexpr int VT = 32;
     constexpr int LD = D + 1;
     extern __shared__ float sm[];
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(D) simt_state_kernel(Params p) {
 // Output: O = scale [ (q e^G) S_chunk + P U ].  One CTA per (chunk, value head).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(kOutThreads) simt_output_kernel(Params p) {
+__global__ void __launch_bounds__(kOutThreads) gdn2_simt_output_kernel(Params p) {
     constexpr int LD = D + 1;
     extern __shared__ float sm[];
     float *Gs = sm;               // [64][LD]   } reused together as Hs [D][LD]
@@ -288,24 +288,24 @@ __global__ void __launch_bounds__(kOutThreads) simt_output_kernel(Params p) {
 template <int D>
 cudaError_t launch_intra_d(const Params &p, cudaStream_t s) {
     const size_t smem = (5 * 64 * (D + 1) + 2 * 64 * 65) * sizeof(float);
-    cudaFuncSetAttribute(simt_intra_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (p.NCmax > 0) simt_intra_kernel<D><<<dim3(p.NCmax, p.HV), kIntraThreads, smem, s>>>(p);
+    cudaFuncSetAttribute(gdn2_simt_intra_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (p.NCmax > 0) gdn2_simt_intra_kernel<D><<<dim3(p.NCmax, p.HV), kIntraThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_state_d(const Params &p, cudaStream_t s) {
     const size_t smem = (D * 33 + 64 * (D + 1) + 64 * 33) * sizeof(float);
-    cudaFuncSetAttribute(simt_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (p.N > 0) simt_state_kernel<D><<<dim3(p.N, p.HV, D / 32), D, smem, s>>>(p);
+    cudaFuncSetAttribute(gdn2_simt_state_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (p.N > 0) gdn2_simt_state_kernel<D><<<dim3(p.N, p.HV, D / 32), D, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_output_d(const Params &p, cudaStream_t s) {
     const size_t smem = (5 * 64 * (D + 1) + 64 * 65) * sizeof(float);
-    cudaFuncSetAttribute(simt_output_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (p.NCmax > 0) simt_output_kernel<D><<<dim3(p.NCmax, p.HV), kOutThreads, smem, s>>>(p);
+    cudaFuncSetAttribute(gdn2_simt_output_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (p.NCmax > 0) gdn2_simt_output_kernel<D><<<dim3(p.NCmax, p.HV), kOutThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
