@@ -84,6 +84,13 @@ def stage_bytes(wl, impl, has_h0, write_state=True, l2norm=False):
     vh = T * HV * V
     hb = NC * HV * K * V * 2       # bf16 chunk states
     out = {}
+    if impl == "tc":
+        rec = (73728 + 512 + 1023) // 1024 * 1024 if K == 128 else (40960 + 256 + 1023) // 1024 * 1024
+        rec_read = (rec - 1024 + 4 * K) if K == 128 else (rec - 1024 + 4 * K)
+        out["chunk_map"] = 0
+        out["intra"] = 2 * qk1 + vh * 2 * 2 + kh * 4 + kh * 2 + NC * HV * rec
+        out["state_output"] = NC * HV * rec_read + vh * 2 + (st if has_h0 else 0) + (st if write_state else 0)
+        return out
     out["prep"] = kh * 4 * 2 + (4 * qk1 if l2norm else 0)
     out["intra"] = qk1 + kh * 4 + kh * 2 + vh * 2 * 2 + kh * 2 + vh * 2
     out["state"] = kh * 2 + vh * 2 + qk1 + kh * 4 + hb + vh * 2 + (st if has_h0 else 0) + (

@@ -53,6 +53,7 @@ bool strides_ok(const void *base, const int64_t *st, size_t esize, int heads, in
 
 WsLayout workspace_layout(const gdn2_dims &d) {
     WsLayout L;
+    memset(&L, 0, sizeof(L));
     const size_t T = static_cast<size_t>(d.T_tot), NC = static_cast<size_t>(nc_max(d));
     size_t off = 0;
     auto take = [&](size_t bytes) { const size_t o = off; off += align_up(bytes); return o; };
@@ -61,13 +62,18 @@ WsLayout workspace_layout(const gdn2_dims &d) {
     L.chunk_len = take(NC * 4);
     L.chunk_start = take(NC * 8);
     L.seq_first = take((static_cast<size_t>(d.N) + 1) * 4);
-    L.G = take(T * d.HV * d.K * 4);
-    L.qn = take(d.use_qk_l2norm ? T * d.H * d.K * 2 : 0);
-    L.kn = take(d.use_qk_l2norm ? T * d.H * d.K * 2 : 0);
-    L.Wt = take(T * d.HV * d.K * 2);
-    L.Ut = take(T * d.HV * d.V * 2);
-    L.hbuf = take(NC * d.HV * d.K * d.V * 2);
-    L.vnew = take(T * d.HV * d.V * 2);
+    if (d.impl == GDN2_IMPL_SIMT) {
+        L.G = take(T * d.HV * d.K * 4);
+        L.qn = take(d.use_qk_l2norm ? T * d.H * d.K * 2 : 0);
+        L.kn = take(d.use_qk_l2norm ? T * d.H * d.K * 2 : 0);
+        L.Wt = take(T * d.HV * d.K * 2);
+        L.Ut = take(T * d.HV * d.V * 2);
+        L.hbuf = take(NC * d.HV * d.K * d.V * 2);
+        L.vnew = take(T * d.HV * d.V * 2);
+    } else {
+        off = (off + 1023) & ~static_cast<size_t>(1023);  // records are 1 KB aligned
+        L.rec = take(NC * d.HV * tc_record_bytes(d.K));
+    }
     L.total = off;
     return L;
 }
@@ -94,6 +100,7 @@ const char *gdn2_status_string(int status) {
         case GDN2_ERR_CU_SEQLENS: return "cu_seqlens invalid on the device (cu[0] != 0, decreasing, or cu[N] != T_tot)";
         case GDN2_ERR_CUDA: return "CUDA runtime error";
         case GDN2_ERR_IMPL: return "unknown implementation selector";
+        case GDN2_ERR_TIMEOUT: return "a tensor-core kernel timed out waiting on its own pipeline (outputs invalid)";
         default: return "unknown status";
     }
 }
@@ -163,6 +170,8 @@ namespace {
 
 const char *const kSimtStages[] = {"prep", "intra", "state", "output"};
 constexpr int kNumSimtStages = 4;
+const char *const kTcStages[] = {"chunk_map", "intra", "state_output"};
+constexpr int kNumTcStages = 3;
 
 gdn2_status run(const void *q, const void *k, const void *v, const void *g, const void *beta, const void *w,
                 float scale, const float *initial_state, const void *cu_seqlens, void *out, float *final_state,
@@ -180,7 +189,6 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
         return GDN2_ERR_ARCH;
     }
     if (major != 10 || minor != 3) return GDN2_ERR_ARCH;
-    if (d->impl == GDN2_IMPL_TC) return GDN2_ERR_IMPL;  // tensor-core path not built yet
 
     const WsLayout L = workspace_layout(*d);
     char *ws = static_cast<char *>(workspace);
@@ -217,9 +225,11 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     p.Ut = reinterpret_cast<bf16 *>(ws + L.Ut);
     p.hbuf = reinterpret_cast<bf16 *>(ws + L.hbuf);
     p.vnew = reinterpret_cast<bf16 *>(ws + L.vnew);
+    p.rec = reinterpret_cast<uint8_t *>(ws + L.rec);
+    p.vtile = d->K;
     p.q_in = p.q; p.k_in = p.k;
     p.sq_in_t = p.sq_t; p.sq_in_h = p.sq_h; p.sk_in_t = p.sk_t; p.sk_in_h = p.sk_h;
-    if (p.l2norm) {  // chunk kernels read the normalised packed copies
+    if (p.l2norm && d->impl == GDN2_IMPL_SIMT) {  // SIMT kernels read the normalised packed copies
         p.q = p.qn; p.k = p.kn;
         p.sq_t = p.sk_t = static_cast<int64_t>(p.H) * p.K;
         p.sq_h = p.sk_h = p.K;
@@ -234,14 +244,22 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     };
     mark();
     if (launch_chunk_map(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
-    if (p.N > 0 && launch_prep(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
-    mark();
-    if (p.N > 0 && launch_simt_intra(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
-    mark();
-    if (p.N > 0 && launch_simt_state(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
-    mark();
-    if (p.N > 0 && launch_simt_output(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
-    mark();
+    if (d->impl == GDN2_IMPL_TC) {
+        mark();
+        if (p.N > 0 && launch_tc_intra(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+        mark();
+        if (p.N > 0 && launch_tc_state(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+        mark();
+    } else {
+        if (p.N > 0 && launch_prep(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+        mark();
+        if (p.N > 0 && launch_simt_intra(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+        mark();
+        if (p.N > 0 && launch_simt_state(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+        mark();
+        if (p.N > 0 && launch_simt_output(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+        mark();
+    }
     if (events && cudaGetLastError() != cudaSuccess) return GDN2_ERR_CUDA;
     return GDN2_OK;
 }
@@ -250,18 +268,19 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
 
 int32_t gdn2_num_stages(const gdn2_dims *d) {
     if (!d || !shape_ok(*d)) return 0;
-    return kNumSimtStages;
+    return d->impl == GDN2_IMPL_SIMT ? kNumSimtStages : kNumTcStages;
 }
 
 const char *gdn2_stage_name(const gdn2_dims *d, int32_t i) {
     if (i < 0 || i >= gdn2_num_stages(d)) return nullptr;
-    return kSimtStages[i];
+    return d->impl == GDN2_IMPL_SIMT ? kSimtStages[i] : kTcStages[i];
 }
 
 int32_t gdn2_launch_count(const gdn2_dims *d) {
     if (!d || !shape_ok(*d)) return 0;
     if (d->N == 0) return 1;
     const int64_t ncmax = nc_max(*d);
+    if (d->impl != GDN2_IMPL_SIMT) return 1 + (ncmax > 0 ? 1 : 0) + 1;  // map, intra, state
     int n = 1;                                          // chunk map
     n += (d->use_qk_l2norm && d->T_tot > 0) ? 1 : 0;    // q/k L2 norm
     n += ncmax > 0 ? 1 : 0;                             // cumsum
@@ -291,13 +310,13 @@ gdn2_status gdn2_chunk_fwd_staged(const void *q, const void *k, const void *v, c
 gdn2_status gdn2_device_status(const void *workspace, void *stream, int32_t *status) {
     if (!workspace || !status) return GDN2_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int32_t host = 0;  // the status word sits at offset 0 of the workspace
-    if (cudaMemcpyAsync(&host, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+    int32_t host[3] = {0, 0, 0};  // the status words sit at offset 0 of the workspace
+    if (cudaMemcpyAsync(host, workspace, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return GDN2_ERR_CUDA;
     }
-    *status = host;
+    *status = host[0] != GDN2_OK ? host[0] : host[2];
     return GDN2_OK;
 }
 

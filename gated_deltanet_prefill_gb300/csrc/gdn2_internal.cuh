@@ -38,7 +38,7 @@ struct Params {
     int has_g, has_beta, has_w, l2norm;
     int NCmax;                  // upper bound on the chunk count: T_tot/64 + N
     // ---- workspace ----
-    int *status;                // [0] status word, [1] chunk count NC
+    int *status;                // [0] cu_seqlens status, [1] chunk count NC, [2] wait timeout
     int *chunk_seq;             // [NCmax]  sequence of chunk c, -1 past NC
     int *chunk_len;             // [NCmax]  tokens in chunk c (1..64)
     int64_t *chunk_start;       // [NCmax]  first token of chunk c
@@ -48,11 +48,13 @@ struct Params {
     bf16 *Wt, *Ut;              // [T_tot, HV, K], [T_tot, HV, V]  WY pseudo-keys / values
     bf16 *hbuf;                 // [NCmax, HV, K, V] state entering each chunk (bf16)
     bf16 *vnew;                 // [T_tot, HV, V]  u_t (v_new) per token
+    uint8_t *rec;               // [NCmax, HV] records of the tensor-core path
+    int vtile;                  // V columns per state CTA (tensor-core path)
 };
 
 // Workspace layout (byte offsets), a function of the problem only.
 struct WsLayout {
-    size_t status, chunk_seq, chunk_len, chunk_start, seq_first, G, qn, kn, Wt, Ut, hbuf, vnew;
+    size_t status, chunk_seq, chunk_len, chunk_start, seq_first, G, qn, kn, Wt, Ut, hbuf, vnew, rec;
     size_t total;
 };
 
@@ -69,5 +71,8 @@ cudaError_t launch_prep(const Params &p, cudaStream_t s);
 cudaError_t launch_simt_intra(const Params &p, cudaStream_t s);
 cudaError_t launch_simt_state(const Params &p, cudaStream_t s);
 cudaError_t launch_simt_output(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_intra(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_state(const Params &p, cudaStream_t s);
+size_t tc_record_bytes(int D);
 
 }  // namespace gdn2

@@ -24,7 +24,10 @@ __global__ void __launch_bounds__(kMapThreads) gdn2_chunk_map_kernel(Params p) {
     __shared__ int s_scan[kMapThreads];
     __shared__ int s_total;
     const int tid = threadIdx.x;
-    if (tid == 0) s_bad = 0;
+    if (tid == 0) {
+        s_bad = 0;
+        p.status[2] = GDN2_OK;
+    }
     __syncthreads();
     for (int n = tid; n < p.N; n += kMapThreads)
         if (cu_at(p, n + 1) < cu_at(p, n)) s_bad = 1;

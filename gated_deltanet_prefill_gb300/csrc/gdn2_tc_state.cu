@@ -1,0 +1,349 @@
+// Tensor-core state-passing kernel with the output fused in.
+//
+// One CTA per (sequence, value head, V tile of VT columns) walks the
+// sequence's chunks in order (the inter-chunk recurrence is sequential; V
+// columns of S evolve independently, so V tiles are exact).  The state S
+// (D x VT fp32) stays in Tensor Memory for the whole sequence.  Per chunk,
+// with the intra kernel's record (gdn2_record.cuh):
+//   MMA1  D1 = [Qe ; Wt] x S_bf16          (M=128, N=VT, K=D)
+//   epi   U  = Ut - (Wt S)  -> bf16 smem   (rows 64-127 of D1)
+//   MMA2  D1[0:64] += P x U                (M=128, K=64; rows 64-127 dead)
+//   MMA3  S  += Kd^T x U                   (M=128, K=64), S pre-scaled by eGL
+//   epi   o = scale * D1[0:64] -> bf16 global
+// which is the FlashRT page's WY chain (chunk_h then output_o) fused into one
+// pass, with burn-gdn2's "in-loop output phase".
+//
+// Warp roles (12 warps): 0 bulk-copy producer, 1 MMA issuer (and TMEM owner),
+// 4-7 state epilogue (S -> bf16 operand, S *= eGL), 8-9 output epilogue,
+// 10-11 U epilogue.  Every wait is time-bounded; a timeout sets the device
+// status word and the CTA unwinds.
+#include "gdn2_internal.cuh"
+#include "gdn2_record.cuh"
+#include "gdn2_tc.cuh"
+
+namespace gdn2 {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kStateThreads = 384;
+
+template <int D, int VT, int NSTAGE>
+struct StateCfg {
+    static constexpr uint32_t sP = 0;
+    static constexpr uint32_t sA1 = 8192;
+    static constexpr uint32_t sKdT = sA1 + (D / 64) * 16384;
+    static constexpr uint32_t sZero = sKdT + (D / 64) * 8192;        // 8 KB zeros when D == 64
+    static constexpr uint32_t sUt = sZero + (D == 64 ? 8192 : 0);
+    static constexpr uint32_t sEGL = sUt + (VT / 64) * 8192;
+    static constexpr uint32_t kStage = (sEGL + D * 4 + 1023) / 1024 * 1024;
+    static constexpr uint32_t oS = NSTAGE * kStage;                   // S bf16, MN-major B
+    static constexpr uint32_t oU = oS + (VT / 64) * D * 128;          // U bf16, MN-major B
+    static constexpr uint32_t kSmem = oU + (VT / 64) * 8192 + 1024;   // + alignment slack
+    static constexpr uint32_t kLoadBytes = Rec<D>::mma_prefix + (VT / 64) * 8192 + D * 4;
+    static constexpr uint32_t kTmemCols = 3 * VT <= 256 ? 256 : 512;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void set_timeout(const Params &p) {
+    atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t x) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x));
+}
+
+template <int D, int VT, int NSTAGE>
+__global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params p) {
+    using C = StateCfg<D, VT, NSTAGE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ uint64_t full_bar[NSTAGE], empty_bar[NSTAGE];
+    __shared__ uint64_t s_ready, u_ready, s_full, drain;
+    __shared__ uint64_t d1_full[2], o_full[2], d1_free[2];
+    __shared__ uint32_t tmem_slot;
+
+    if (p.status[0] != GDN2_OK) return;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int n = blockIdx.x, hv = blockIdx.y, v0 = blockIdx.z * VT;
+    const int first = p.seq_first[n], nck = p.seq_first[n + 1] - first;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        mbar_init(&s_ready, 128);
+        mbar_init(&u_ready, 64);
+        mbar_init(&s_full, 1);
+        mbar_init(&drain, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&d1_full[b], 1);
+            mbar_init(&o_full[b], 1);
+            mbar_init(&d1_free[b], 64);
+        }
+        fence_mbar_init();
+    }
+    if (D == 64) {  // zero rows that pad the 64-channel Kd^T operand to M = 128
+        for (int s = 0; s < NSTAGE; ++s)
+            for (int i = threadIdx.x; i < 8192 / 16; i += kStateThreads)
+                reinterpret_cast<uint4 *>(sm + s * C::kStage + C::sZero)[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS = tmem_slot;
+    const uint32_t tD1[2] = {tmem_slot + VT, tmem_slot + 2 * VT};
+    const uint32_t sS = smem_u32(sm + C::oS), sU = smem_u32(sm + C::oU);
+
+    if (warp == 0) {
+        // ------------------------------------------------ bulk-copy producer
+        if (lane == 0) {
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < nck && ok; ++i) {
+                const int s = i % NSTAGE;
+                if (i >= NSTAGE && !mbar_wait(&empty_bar[s], ((i / NSTAGE) - 1) & 1)) {
+                    set_timeout(p);
+                    ok = false;
+                    break;
+                }
+                const uint8_t *rec = p.rec + (static_cast<size_t>(first + i) * p.HV + hv) * Rec<D>::bytes;
+                uint8_t *st = sm + s * C::kStage;
+                mbar_arrive_expect_tx(&full_bar[s], C::kLoadBytes);
+                bulk_g2s(st + C::sP, rec + Rec<D>::P, Rec<D>::mma_prefix, &full_bar[s]);
+                bulk_g2s(st + C::sUt, rec + Rec<D>::Ut + (v0 / 64) * 8192, (VT / 64) * 8192, &full_bar[s]);
+                bulk_g2s(st + C::sEGL, rec + Rec<D>::eGL, D * 4, &full_bar[s]);
+                ++issued;
+            }
+            if (!ok) {  // let every copy in flight land before the CTA exits
+                for (int i = issued - NSTAGE > 0 ? issued - NSTAGE : 0; i < issued; ++i)
+                    mbar_wait(&full_bar[i % NSTAGE], (i / NSTAGE) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id1 = idesc_bf16(128, VT, false, true);
+            constexpr uint32_t id3 = idesc_bf16(128, VT, true, true);
+            for (int i = 0; i < nck; ++i) {
+                const int s = i % NSTAGE, b = i & 1;
+                if (!mbar_wait(&full_bar[s], (i / NSTAGE) & 1) || !mbar_wait(&s_ready, i & 1) ||
+                    (i >= 2 && !mbar_wait(&d1_free[b], ((i >> 1) - 1) & 1))) {
+                    set_timeout(p);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = smem_u32(sm + s * C::kStage);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_bf16(tD1[b], desc_kmajor(st + C::sA1, 128, kk), desc_mnmajor(sS, D, kk), id1, kk > 0);
+                mma_commit(&d1_full[b]);
+                if (!mbar_wait(&u_ready, i & 1)) {
+                    set_timeout(p);
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tD1[b], desc_kmajor(st + C::sP, 128, kk), desc_mnmajor(sU, 64, kk), id1, 1);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tS, desc_mnmajor(st + C::sKdT, 64, kk), desc_mnmajor(sU, 64, kk), id3, 1);
+                mma_commit(&o_full[b]);
+                mma_commit(&s_full);
+                mma_commit(&empty_bar[s]);
+            }
+            mma_commit(&drain);
+            if (!mbar_wait(&drain, 0)) set_timeout(p);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------- state epilogue (S rows = key channels)
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const bool active = row < D;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        if (active) {
+            const float *h0 = p.h0 ? p.h0 + ((static_cast<size_t>(n) * p.HV + hv) * D + row) * D + v0 : nullptr;
+#pragma unroll 1
+            for (int j = 0; j < VT / 32; ++j) {
+                uint32_t r[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    float4 x = h0 ? *reinterpret_cast<const float4 *>(h0 + 32 * j + e) : make_float4(0, 0, 0, 0);
+                    r[e] = __float_as_uint(x.x); r[e + 1] = __float_as_uint(x.y);
+                    r[e + 2] = __float_as_uint(x.z); r[e + 3] = __float_as_uint(x.w);
+                }
+                tmem_st32(tS + lane_base + 32 * j, r);
+            }
+            tmem_st_wait();
+        }
+        bool ok = true;
+        for (int i = 0; i < nck; ++i) {
+            const int s = i % NSTAGE;
+            if ((i > 0 && !warp_wait(&s_full, (i - 1) & 1)) || !warp_wait(&full_bar[s], (i / NSTAGE) & 1)) {
+                set_timeout(p);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (active) {
+                const float egl = reinterpret_cast<const float *>(sm + s * C::kStage + C::sEGL)[row];
+#pragma unroll 1
+                for (int j = 0; j < VT / 32; ++j) {
+                    uint32_t r[32];
+                    tmem_ld32(tS + lane_base + 32 * j, r);
+                    tmem_ld_wait();
+                    uint8_t *dst = sm + C::oS + ((32 * j) / 64) * D * 128;
+                    const int c0 = ((32 * j) % 64) / 8;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(r[8 * cc + 0]), __uint_as_float(r[8 * cc + 1]));
+                        v.y = pack_bf16(__uint_as_float(r[8 * cc + 2]), __uint_as_float(r[8 * cc + 3]));
+                        v.z = pack_bf16(__uint_as_float(r[8 * cc + 4]), __uint_as_float(r[8 * cc + 5]));
+                        v.w = pack_bf16(__uint_as_float(r[8 * cc + 6]), __uint_as_float(r[8 * cc + 7]));
+                        *reinterpret_cast<uint4 *>(dst + swz(row, c0 + cc)) = v;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * egl);
+                    tmem_st32(tS + lane_base + 32 * j, r);
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(&s_ready);
+        }
+        if (ok && nck > 0 && !warp_wait(&s_full, (nck - 1) & 1)) {
+            set_timeout(p);
+            ok = false;
+        }
+        tc_fence_after();
+        if (ok && active && p.hT) {
+            float *hT = p.hT + ((static_cast<size_t>(n) * p.HV + hv) * D + row) * D + v0;
+#pragma unroll 1
+            for (int j = 0; j < VT / 32; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tS + lane_base + 32 * j, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(hT + 32 * j + e) =
+                        make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                    __uint_as_float(r[e + 3]));
+            }
+        }
+    } else if (warp == 8 || warp == 9) {
+        // ----------------------------------------- output epilogue (tokens 0-63)
+        const int q = warp & 3;  // 0 or 1
+        const int t = 32 * q + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        for (int i = 0; i < nck; ++i) {
+            const int b = i & 1;
+            if (!warp_wait(&o_full[b], (i >> 1) & 1)) {
+                set_timeout(p);
+                break;
+            }
+            tc_fence_after();
+            const int ck = first + i;
+            const int64_t tok = p.chunk_start[ck] + t;
+            const bool valid = t < p.chunk_len[ck];
+            bf16 *orow = p.o + tok * p.so_t + static_cast<int64_t>(hv) * p.so_h + v0;
+#pragma unroll 1
+            for (int j = 0; j < VT / 32; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tD1[b] + lane_base + 32 * j, r);
+                tmem_ld_wait();
+                if (valid) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint4 v;
+                        v.x = pack_bf16(__uint_as_float(r[8 * cc + 0]) * p.scale, __uint_as_float(r[8 * cc + 1]) * p.scale);
+                        v.y = pack_bf16(__uint_as_float(r[8 * cc + 2]) * p.scale, __uint_as_float(r[8 * cc + 3]) * p.scale);
+                        v.z = pack_bf16(__uint_as_float(r[8 * cc + 4]) * p.scale, __uint_as_float(r[8 * cc + 5]) * p.scale);
+                        v.w = pack_bf16(__uint_as_float(r[8 * cc + 6]) * p.scale, __uint_as_float(r[8 * cc + 7]) * p.scale);
+                        reinterpret_cast<uint4 *>(orow + 32 * j)[cc] = v;
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&d1_free[b]);
+        }
+    } else if (warp == 10 || warp == 11) {
+        // ----------------------------------- U epilogue (D1 rows 64-127 = Wt S)
+        const int q = warp & 3;  // 2 or 3
+        const int t = 32 * (q - 2) + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        for (int i = 0; i < nck; ++i) {
+            const int s = i % NSTAGE, b = i & 1;
+            if (!warp_wait(&d1_full[b], (i >> 1) & 1) || !warp_wait(&full_bar[s], (i / NSTAGE) & 1)) {
+                set_timeout(p);
+                break;
+            }
+            tc_fence_after();
+            const uint8_t *ut = sm + s * C::kStage + C::sUt;
+#pragma unroll 1
+            for (int j = 0; j < VT / 32; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tD1[b] + lane_base + 32 * j, r);
+                tmem_ld_wait();
+                const int blk = (32 * j) / 64, c0 = ((32 * j) % 64) / 8;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(ut + blk * 8192 + swz(t, c0 + cc));
+                    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+                    uint32_t ow[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 a = unpack_bf16(uw[e]);
+                        ow[e] = pack_bf16(a.x - __uint_as_float(r[8 * cc + 2 * e]),
+                                          a.y - __uint_as_float(r[8 * cc + 2 * e + 1]));
+                    }
+                    *reinterpret_cast<uint4 *>(sm + C::oU + blk * 8192 + swz(t, c0 + cc)) =
+                        make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                }
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(&u_ready);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tS, C::kTmemCols);
+    }
+}
+
+template <int D, int VT, int NSTAGE>
+cudaError_t launch_state(const Params &p, cudaStream_t s) {
+    using C = StateCfg<D, VT, NSTAGE>;
+    auto kern = gdn2_tc_state_kernel<D, VT, NSTAGE>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    if (p.N > 0) kern<<<dim3(p.N, p.HV, D / VT), kStateThreads, C::kSmem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_state(const Params &p, cudaStream_t s) {
+    if (p.K == 64) return launch_state<64, 64, 3>(p, s);
+    if (p.vtile == 64) return launch_state<128, 64, 3>(p, s);
+    return launch_state<128, 128, 2>(p, s);
+}
+
+}  // namespace gdn2

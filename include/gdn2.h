@@ -58,7 +58,9 @@ typedef enum gdn2_status {
     GDN2_ERR_CU_SEQLENS = 9,  /* device-side: cu_seqlens[0] != 0, decreasing, or      */
                               /* cu_seqlens[N] != T_tot (see gdn2_device_status)      */
     GDN2_ERR_CUDA = 10,       /* another CUDA runtime error                           */
-    GDN2_ERR_IMPL = 11        /* unknown implementation selector                      */
+    GDN2_ERR_IMPL = 11,       /* unknown implementation selector                      */
+    GDN2_ERR_TIMEOUT = 12     /* device-side: a kernel gave up waiting on one of its  */
+                              /* own pipeline barriers (see gdn2_device_status)       */
 } gdn2_status;
 
 typedef enum gdn2_dtype {
@@ -191,9 +193,11 @@ GDN2_API const char *gdn2_stage_name(const gdn2_dims *dims, int32_t i);
 GDN2_API int32_t gdn2_launch_count(const gdn2_dims *dims);
 
 /*
- * Read the device-side status word that the last gdn2_chunk_fwd on this
- * workspace wrote (GDN2_OK or GDN2_ERR_CU_SEQLENS) into *status.  This call
- * SYNCHRONISES `stream`.  Returns GDN2_ERR_CUDA if the copy fails.
+ * Read the device-side status that the last gdn2_chunk_fwd on this workspace
+ * wrote into *status: GDN2_OK, GDN2_ERR_CU_SEQLENS, or GDN2_ERR_TIMEOUT (a
+ * tensor-core kernel waited more than 2 s on one of its own barriers and
+ * unwound; its outputs are then invalid).  This call SYNCHRONISES `stream`.
+ * Returns GDN2_ERR_CUDA if the copy fails.
  */
 GDN2_API gdn2_status gdn2_device_status(const void *workspace, void *stream, int32_t *status);
 

@@ -15,7 +15,7 @@ from gated_deltanet_prefill_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-2
-IMPLS = ["simt"]
+IMPLS = ["simt", "tc"]
 
 
 def rel_max(x, ref):
