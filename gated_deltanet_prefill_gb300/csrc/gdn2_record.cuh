@@ -17,7 +17,9 @@
 //   KdT  Kd as an MN-major A   D/64 blocks of [64 s][128 B] = 8 KB
 //   Ut   [64 t][D]             D/64 blocks of [64 t][128 B], swizzled
 //   eGL  D fp32
-// Rows of tokens past the chunk's length are zero (eGL is always defined).
+// Qe, Wt, P, KdT and Ut are fp16 (10-bit mantissa; conversions saturate at
+// +-65504).  Rows of tokens past the chunk's length are zero (eGL is always
+// defined).
 #pragma once
 
 #include <stdint.h>

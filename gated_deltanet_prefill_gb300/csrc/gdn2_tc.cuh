@@ -12,6 +12,8 @@
 //    columns, each [K rows][128 B]; an MMA step of 16 K advances 2048 bytes.
 #pragma once
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace gdn2 {
@@ -173,14 +175,21 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, uint32_t krows, 
     return sdesc(base + kk * 2048u, krows * 128u, 1024u);
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
+// Instruction descriptor, kind::f16, fp32 D; A and B both bf16 or both fp16.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool a_mn, bool b_mn, bool bf16) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+    return idesc_f16kind(M, N, a_mn, b_mn, true);
+}
+__host__ __device__ constexpr uint32_t idesc_fp16(int M, int N, bool a_mn, bool b_mn) {
+    return idesc_f16kind(M, N, a_mn, b_mn, false);
 }
 
-// D[tmem] (+)= A[smem] x B[smem]; issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+// D[tmem] (+)= A[smem] x B[smem], kind::f16 (bf16 or fp16 operands per the
+// instruction descriptor); issued by one thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
     asm volatile(
         "{\n.reg .pred p;\n"
@@ -201,6 +210,38 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 // 128B-swizzled block whose rows are 128 bytes.
 __host__ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
     return (row >> 3) * 1024u + (row & 7u) * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// ----------------------------------------------------------- conversions
+// fp16 intermediates saturate at +-65504 instead of overflowing to inf.
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 v = __floats2half2_rn(fminf(fmaxf(a, -65504.f), 65504.f), fminf(fmaxf(b, -65504.f), 65504.f));
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+__device__ __forceinline__ float2 unpack_h2(uint32_t x) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&x));
+}
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+__device__ __forceinline__ float2 unpack_bf2(uint32_t x) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x));
+}
+__device__ __forceinline__ uint4 pack8_h(const float (&f)[8]) {
+    return make_uint4(pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
+}
+__device__ __forceinline__ uint4 pack8_bf(const float (&f)[8]) {
+    return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));
+}
+__device__ __forceinline__ void unpack8_bf(const uint4 &u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 x = unpack_bf2(w[e]);
+        f[2 * e] = x.x;
+        f[2 * e + 1] = x.y;
+    }
 }
 
 }  // namespace tc

@@ -4,9 +4,9 @@
 // two CTAs per SM.
 //
 // Steps (FlashRT gated-delta-attention page: norm/cumsum, kkt, solve_tril,
-// recompute_wu; here fused into one kernel, GDN-2 channel-wise gates):
-//  1. load k, q (key head), v, w, beta, g (value head); optional q/k L2 norm;
-//     G = chunk-local inclusive cumsum of g.
+// recompute_wu; fused into one kernel here, with GDN-2's channel-wise gates):
+//  1. load g, k, q (key head), v, w, beta (value head); optional q/k L2 norm;
+//     G = chunk-local inclusive cumsum of g (two-part scan in shared memory).
 //  2. decay factors through 16-token sub-chunk references (burn-gdn2 README,
 //     "Numerical stability"): with B_I the row before sub-chunk I and E_J the
 //     last row of sub-chunk J,
@@ -14,13 +14,16 @@
 //        eR_s = e^{G_{E_J} - G_s} <= 1, m_{I,J} = e^{G_{B_I} - G_{E_J}}
 //     (m <= 1 for J < I; m = e^{+decay of sub-chunk I} for J = I).  Every m is
 //     a product of the per-sub-chunk decays ge_J = e^{G_{E_J} - G_{E_{J-1}}}.
-//  3. tcgen05: for each row block I, [beta k F ; q F] (M=128) x R_I^T where
-//     R_I = k eR m_{I,.} (N = 16(I+1)): rows of block I give A (strict lower)
-//     and P (lower incl. diagonal).
-//  4. T = (I + A)^{-1} by blocked forward substitution in fp32 (16x16
-//     diagonal blocks, then off-diagonal blocks level by level).
-//  5. tcgen05: [Wt | Ut] = T x [beta k e^G | w v]  (M=128, N=2D, K=64).
-//  6. write Qe, Kd^T, P, Wt, Ut, eGL as shared-memory images.
+//  3. tcgen05 (bf16): for each row block I, [beta k F ; q F] (M=128) x R_I^T
+//     with R_I = k eR m_{I,.} (N = 16(I+1)); rows of block I give A (strictly
+//     lower) and P (lower incl. diagonal).
+//  4. T = (I + A)^{-1} by blocked forward substitution in fp32.
+//  5. tcgen05 (fp16): [Wt | Ut] = T x [beta k e^G | w v]  (M=128, N=2D, K=64).
+//  6. write Qe, Kd^T, P, Wt, Ut (fp16) and eGL (fp32) as shared-memory images.
+//
+// Thread (t = tid / 4, seg = tid % 4) owns token row t and the 8-channel
+// chunks seg, seg + 4, seg + 8, ...: the four segments of a row fall in
+// different shared-memory banks for every per-channel table read.
 #include "gdn2_internal.cuh"
 #include "gdn2_record.cuh"
 #include "gdn2_tc.cuh"
@@ -32,58 +35,52 @@ namespace {
 using namespace tc;
 
 constexpr int kIntraThreads = 256;
+constexpr int kLD = 68;  // row stride (floats) of the fp32 solver matrices
 
 template <int D>
 struct IntraCfg {
-    // region X: A_left image (M=128, K=D) then the four R_I images
+    // region X: A_left image (bf16, M=128, K=D) then the four R_I images (bf16)
     static constexpr uint32_t oAL = 0;
     static constexpr uint32_t kAL = (D / 64) * 16384;
     __host__ __device__ static constexpr uint32_t rows_R(int I) { return 16u * (I + 1); }
-    __host__ __device__ static constexpr uint32_t oR(int I) {  // cumulative (D/64) * rows * 128 bytes
+    __host__ __device__ static constexpr uint32_t oR(int I) {
         return kAL + (D / 64) * 128u * 16u * (I * (I + 1) / 2);
     }
     static constexpr uint32_t kOperands = kAL + (D / 64) * 128u * 160u;
-    static constexpr uint32_t kX = kOperands > 45056u ? kOperands : 45056u;
-    // reused after the A/P MMA: solver buffers and the T image (last 8 KB of X)
-    static constexpr uint32_t oAf = 0;                      // [64][65] fp32
-    static constexpr uint32_t oTf = 16640;                  // [64][65] fp32
-    static constexpr uint32_t oY = 33280;                   // 3 x [16][16] fp32
-    static constexpr uint32_t oTimg = kX - 8192;            // [64 t][64 s] K-major bf16
-    // B operand [beta k e^G | w v], MN-major, N = 2D, K = 64; holds G before
+    static constexpr uint32_t kX = kOperands > 46080u ? kOperands : 46080u;
+    // reused after the A/P MMA: fp32 solver matrices and the fp16 T image
+    static constexpr uint32_t oAf = 0;                         // [64][kLD]
+    static constexpr uint32_t oTf = 64 * kLD * 4;              // [64][kLD]
+    static constexpr uint32_t oY = 2 * 64 * kLD * 4;           // 3 x [16][16]
+    static constexpr uint32_t oTimg = kX - 8192;               // [64 t][64 s] K-major fp16
+    // [beta k e^G | w v] fp16 MN-major B (N = 2D, K = 64); G scratch before
     static constexpr uint32_t oBWU = kX;
     static constexpr uint32_t kBWU = (2 * D / 64) * 8192;
-    // per-channel tables: gE[4][D], ge[4][D], inv_ge[4][D]
+    // per-channel tables gE[4][D], ge[4][D], ige[4][D]; scan totals [parts][D]
     static constexpr uint32_t oTab = oBWU + kBWU;
-    static constexpr uint32_t kSmem = oTab + 3 * 4 * D * 4 + 1024;
+    static constexpr uint32_t oTot = oTab + 3 * 4 * D * 4;
+    static constexpr uint32_t kSmem = oTot + (kIntraThreads / D) * D * 4 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 256;
     static_assert(oTimg >= oY + 3 * 1024, "solver buffers overlap the T image");
     static_assert(kBWU >= 64 * D * 4, "G scratch must fit in the B operand area");
-    static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
+    // two CTAs per SM: 2 x (dynamic + 64 B static + 1 KB reserved) <= 228 KB
+    static_assert(2 * (kSmem + 64 + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[e]));
-        f[2 * e] = x.x;
-        f[2 * e + 1] = x.y;
-    }
-}
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-    return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]), pack2(f[6], f[7]));
-}
 __device__ __forceinline__ uint4 ldg16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+
+// G scratch [64][D] fp32 with float4 chunks XOR-swizzled by (t & 7)
+template <int D>
+__device__ __forceinline__ int gidx(int t, int c) {
+    return t * D + ((((c >> 2) ^ (t & 7))) << 2) + (c & 3);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params p) {
     using C = IntraCfg<D>;
-    constexpr int SEG = D / 4;       // channels per thread (row t, segment seg)
-    constexpr int NH = SEG / 16;     // halves of 16 channels
+    constexpr int NJ = D / 32;         // 8-channel chunks per thread
+    constexpr int PARTS = kIntraThreads / D;
+    constexpr int ROWS = 64 / PARTS;   // rows per scan part
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ uint64_t bar_mma;
@@ -96,11 +93,17 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     const int64_t start = p.chunk_start[c];
     const int len = p.chunk_len[c];
     const int h = hv / p.group;
-    const int t = tid / 4, seg = tid % 4;   // row and channel segment owned in steps 1-2
-    const int cb = seg * SEG;               // first channel of the segment
+    const int t = tid / 4, seg = tid % 4;
+    const int I = t / 16;
     const bool live = t < len;
     const int64_t tok = start + (live ? t : 0);
     uint8_t *rec = p.rec + (static_cast<size_t>(c) * p.HV + hv) * Rec<D>::bytes;
+    const bf16 *kp = p.k + tok * p.sk_t + static_cast<int64_t>(h) * p.sk_h;
+    const bf16 *qp = p.q + tok * p.sq_t + static_cast<int64_t>(h) * p.sq_h;
+    const bf16 *bp = p.beta + tok * p.sb_t + static_cast<int64_t>(hv) * p.sb_h;
+    const bf16 *vp = p.v + tok * p.sv_t + static_cast<int64_t>(hv) * p.sv_h;
+    const bf16 *wp = p.w + tok * p.sw_t + static_cast<int64_t>(hv) * p.sw_h;
+    const float *gp = p.g + tok * p.sg_t + static_cast<int64_t>(hv) * p.sg_h;
 
     if (tid == 0) {
         mbar_init(&bar_mma, 1);
@@ -111,29 +114,38 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         tmem_relinquish();
     }
 
-    // ---- 1. g -> shared scratch, cumsum over the chunk's tokens -------------
-    float *Gs = reinterpret_cast<float *>(sm + C::oBWU);  // [64][D] fp32
-    {
-        const float *gp = p.g + tok * p.sg_t + static_cast<int64_t>(hv) * p.sg_h + cb;
+    // ---- 1. loads, cumsum ------------------------------------------------------
+    const uint4 z4 = make_uint4(0, 0, 0, 0);
+    float4 graw[2 * NJ];
 #pragma unroll
-        for (int e = 0; e < SEG; e += 4) {
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (live && p.has_g) x = __ldg(reinterpret_cast<const float4 *>(gp + e));
-            *reinterpret_cast<float4 *>(Gs + t * D + cb + e) = x;
+    for (int j = 0; j < NJ; ++j) {
+        const int cb = 8 * (seg + 4 * j);
+        graw[2 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        graw[2 * j + 1] = graw[2 * j];
+        if (live && p.has_g) {
+            graw[2 * j] = __ldg(reinterpret_cast<const float4 *>(gp + cb));
+            graw[2 * j + 1] = __ldg(reinterpret_cast<const float4 *>(gp + cb + 4));
         }
     }
-    // q/k L2 norm factors (fp32, per row) when requested
+    // chunk-0 operands, prefetched; later chunks are fetched one ahead
+    uint4 nk = z4, nq = z4, nb = z4, nv = z4, nw = z4;
+    if (live) {
+        const int cb = 8 * seg;
+        nk = ldg16(kp + cb);
+        nq = ldg16(qp + cb);
+        nv = ldg16(vp + cb);
+        if (p.has_beta) nb = ldg16(bp + cb);
+        if (p.has_w) nw = ldg16(wp + cb);
+    }
     float kscale = 1.f, qscale = 1.f;
     if (p.l2norm) {
         float sk = 0.f, sq = 0.f;
         if (live) {
-            const bf16 *kp = p.k + tok * p.sk_t + static_cast<int64_t>(h) * p.sk_h + cb;
-            const bf16 *qp = p.q + tok * p.sq_t + static_cast<int64_t>(h) * p.sq_h + cb;
 #pragma unroll
-            for (int e = 0; e < SEG; e += 8) {
+            for (int j = 0; j < NJ; ++j) {
                 float a[8], b[8];
-                unpack8(ldg16(kp + e), a);
-                unpack8(ldg16(qp + e), b);
+                unpack8_bf(ldg16(kp + 8 * (seg + 4 * j)), a);
+                unpack8_bf(ldg16(qp + 8 * (seg + 4 * j)), b);
 #pragma unroll
                 for (int x = 0; x < 8; ++x) {
                     sk += a[x] * a[x];
@@ -148,127 +160,143 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         kscale = 1.f / fmaxf(sqrtf(sk), 1e-12f);
         qscale = 1.f / fmaxf(sqrtf(sq), 1e-12f);
     }
+    float *Gs = reinterpret_cast<float *>(sm + C::oBWU);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        const int cb = 8 * (seg + 4 * j);
+        *reinterpret_cast<float4 *>(Gs + gidx<D>(t, cb)) = graw[2 * j];
+        *reinterpret_cast<float4 *>(Gs + gidx<D>(t, cb + 4)) = graw[2 * j + 1];
+    }
     __syncthreads();
-    if (tid < D) {
+    float *tot = reinterpret_cast<float *>(sm + C::oTot);  // [PARTS][D]
+    {
+        const int ch = tid % D, part = tid / D;
         float acc = 0.f;
 #pragma unroll 8
-        for (int r = 0; r < 64; ++r) {
-            acc += Gs[r * D + tid];
-            Gs[r * D + tid] = acc;
+        for (int r = part * ROWS; r < (part + 1) * ROWS; ++r) {
+            acc += Gs[gidx<D>(r, ch)];
+            Gs[gidx<D>(r, ch)] = acc;
+        }
+        tot[part * D + ch] = acc;
+        __syncthreads();
+        float off = 0.f;
+        for (int pp = 0; pp < part; ++pp) off += tot[pp * D + ch];
+        if (part > 0) {
+#pragma unroll 8
+            for (int r = part * ROWS; r < (part + 1) * ROWS; ++r) Gs[gidx<D>(r, ch)] += off;
         }
     }
     __syncthreads();
-    float *gE = reinterpret_cast<float *>(sm + C::oTab);      // [4][D]  G at E_J
-    float *ge = gE + 4 * D;                                   // [4][D]  e^{G_{E_J} - G_{E_{J-1}}}
-    float *ige = ge + 4 * D;                                  // [4][D]  1 / ge
+    float *gE = reinterpret_cast<float *>(sm + C::oTab);  // G at E_J
+    float *ge = gE + 4 * D;                               // e^{G_{E_J} - G_{E_{J-1}}}
+    float *ige = ge + 4 * D;                              // 1 / ge
     if (tid < D) {
-        float prev = 0.f, egl = 1.f;
+        float prev = 0.f;
 #pragma unroll
         for (int J = 0; J < 4; ++J) {
-            const int e = min(16 * J + 15, len - 1);
-            const float gv = Gs[e * D + tid];
+            const float gv = Gs[gidx<D>(min(16 * J + 15, len - 1), tid)];
             gE[J * D + tid] = gv;
             ge[J * D + tid] = __expf(gv - prev);
             ige[J * D + tid] = __expf(prev - gv);
-            egl *= __expf(gv - prev);
             prev = gv;
         }
         reinterpret_cast<float *>(rec + Rec<D>::eGL)[tid] = __expf(prev);
-        (void)egl;
     }
-    float Gr[SEG];
+    float Gr[8 * NJ];
 #pragma unroll
-    for (int e = 0; e < SEG; e += 4) {
-        const float4 x = *reinterpret_cast<const float4 *>(Gs + t * D + cb + e);
-        Gr[e] = x.x; Gr[e + 1] = x.y; Gr[e + 2] = x.z; Gr[e + 3] = x.w;
+    for (int j = 0; j < NJ; ++j) {
+        const int cb = 8 * (seg + 4 * j);
+        const float4 a = *reinterpret_cast<const float4 *>(Gs + gidx<D>(t, cb));
+        const float4 b = *reinterpret_cast<const float4 *>(Gs + gidx<D>(t, cb + 4));
+        Gr[8 * j + 0] = a.x; Gr[8 * j + 1] = a.y; Gr[8 * j + 2] = a.z; Gr[8 * j + 3] = a.w;
+        Gr[8 * j + 4] = b.x; Gr[8 * j + 5] = b.y; Gr[8 * j + 6] = b.z; Gr[8 * j + 7] = b.w;
     }
-    __syncthreads();  // G scratch is dead from here on; tables are visible
+    __syncthreads();  // G scratch is dead from here on; the tables are visible
 
-    // ---- 2. operand images --------------------------------------------------
-    {
-        const int I = t / 16;
-        const bf16 *kp = p.k + tok * p.sk_t + static_cast<int64_t>(h) * p.sk_h;
-        const bf16 *qp = p.q + tok * p.sq_t + static_cast<int64_t>(h) * p.sq_h;
-        const bf16 *bp = p.beta + tok * p.sb_t + static_cast<int64_t>(hv) * p.sb_h;
-        const bf16 *vp = p.v + tok * p.sv_t + static_cast<int64_t>(hv) * p.sv_h;
-        const bf16 *wp = p.w + tok * p.sw_t + static_cast<int64_t>(hv) * p.sw_h;
+    // ---- 2. operand images -------------------------------------------------------
 #pragma unroll
-        for (int hf = 0; hf < NH; ++hf) {
-            const int c0 = cb + 16 * hf;   // 16 channels: two 8-element chunks
+    for (int j = 0; j < NJ; ++j) {
+        const int cb = 8 * (seg + 4 * j);
+        float kk[8], qq[8], bb[8], vv[8], ww[8];
+        unpack8_bf(nk, kk);
+        unpack8_bf(nq, qq);
+        unpack8_bf(nv, vv);
+        unpack8_bf(nb, bb);
+        unpack8_bf(nw, ww);
+        if (!p.has_beta && live) {
 #pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const int cc = c0 + 8 * ch;
-                float kk[8], qq[8], bb[8], vv[8], ww[8];
-                if (live) {
-                    unpack8(ldg16(kp + cc), kk);
-                    unpack8(ldg16(qp + cc), qq);
-                    unpack8(ldg16(vp + cc), vv);
-                    if (p.has_beta) unpack8(ldg16(bp + cc), bb);
-                    else {
-#pragma unroll
-                        for (int x = 0; x < 8; ++x) bb[x] = 1.f;
-                    }
-                    if (p.has_w) unpack8(ldg16(wp + cc), ww);
-                    else {
-#pragma unroll
-                        for (int x = 0; x < 8; ++x) ww[x] = 1.f;
-                    }
-                } else {
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) kk[x] = qq[x] = vv[x] = bb[x] = ww[x] = 0.f;
-                }
-                float Lk[8], Lq[8], kr[8], X1[8], X2[8], Qe[8], Kd[8];
-#pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const int ci = cc + x;
-                    const float gt = Gr[16 * hf + 8 * ch + x];
-                    const float gB = I > 0 ? gE[(I - 1) * D + ci] : 0.f;
-                    const float F = __expf(gt - gB);
-                    const float eR = __expf(gE[I * D + ci] - gt);
-                    const float kx = kk[x] * kscale;
-                    float eGB = 1.f, eLE = 1.f;
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        if (m < I) eGB *= ge[m * D + ci];
-                        if (m > I) eLE *= ge[m * D + ci];
-                    }
-                    Lk[x] = bb[x] * kx * F;
-                    Lq[x] = qq[x] * qscale * F;
-                    kr[x] = kx * eR;
-                    X1[x] = Lk[x] * eGB;
-                    Qe[x] = Lq[x] * eGB;
-                    Kd[x] = kr[x] * eLE;
-                    X2[x] = ww[x] * vv[x];
-                }
-                const int kb = cc / 64, chunk = (cc % 64) / 8;
-                // A_left rows t (beta k F) and 64 + t (q F)
-                *reinterpret_cast<uint4 *>(sm + C::oAL + kb * 16384 + swz(t, chunk)) = pack8(Lk);
-                *reinterpret_cast<uint4 *>(sm + C::oAL + kb * 16384 + swz(64 + t, chunk)) = pack8(Lq);
-                // R_{I'} for I' >= I: k eR m_{I',I}
-#pragma unroll
-                for (int Ip = 0; Ip < 4; ++Ip) {
-                    if (Ip < I) continue;
-                    float r8[8];
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) {
-                        const int ci = cc + x;
-                        float m = 1.f;
-                        if (Ip == I) m = ige[I * D + ci];
-                        else
-                            for (int mm = I + 1; mm < Ip; ++mm) m *= ge[mm * D + ci];
-                        r8[x] = kr[x] * m;
-                    }
-                    *reinterpret_cast<uint4 *>(sm + C::oR(Ip) + kb * (C::rows_R(Ip) * 128u) + swz(t, chunk)) =
-                        pack8(r8);
-                }
-                // B operand [X1 | X2], MN-major: n = cc (X1), n = D + cc (X2)
-                *reinterpret_cast<uint4 *>(sm + C::oBWU + (cc / 64) * 8192 + swz(t, chunk)) = pack8(X1);
-                *reinterpret_cast<uint4 *>(sm + C::oBWU + ((D + cc) / 64) * 8192 + swz(t, chunk)) = pack8(X2);
-                // record: Qe (A1 rows 0-63) and Kd^T (MN-major A)
-                *reinterpret_cast<uint4 *>(rec + Rec<D>::A1 + kb * 16384 + swz(t, chunk)) = pack8(Qe);
-                *reinterpret_cast<uint4 *>(rec + Rec<D>::KdT + kb * 8192 + swz(t, chunk)) = pack8(Kd);
-            }
+            for (int x = 0; x < 8; ++x) bb[x] = 1.f;
         }
+        if (!p.has_w && live) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x) ww[x] = 1.f;
+        }
+        if (j + 1 < NJ && live) {  // fetch the next chunk while this one is processed
+            const int cn = 8 * (seg + 4 * (j + 1));
+            nk = ldg16(kp + cn);
+            nq = ldg16(qp + cn);
+            nv = ldg16(vp + cn);
+            if (p.has_beta) nb = ldg16(bp + cn);
+            if (p.has_w) nw = ldg16(wp + cn);
+        }
+        // outputs packed two channels per 32-bit word as they are produced
+        uint32_t wLk[4], wLq[4], wkr[4], wX1[4], wX2[4], wQe[4], wKd[4], wr0[4], wr2[4], wr3[4];
+#pragma unroll
+        for (int x2 = 0; x2 < 4; ++x2) {
+            float lk[2], lq[2], kr[2], x1[2], xv[2], qe[2], kd[2], r0[2], r2[2], r3[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int x = 2 * x2 + e;
+                const int ci = cb + x;
+                const float g0 = ge[ci], g1 = ge[D + ci], g2 = ge[2 * D + ci], g3 = ge[3 * D + ci];
+                const float gB = I > 0 ? gE[(I - 1) * D + ci] : 0.f;
+                const float gt = Gr[8 * j + x];
+                const float F = __expf(gt - gB);
+                const float eR = __expf(gE[I * D + ci] - gt);
+                // e^{G_{B_I}} and e^{G_L - G_{E_I}} as products of sub-chunk decays
+                const float eGB = I == 0 ? 1.f : (I == 1 ? g0 : (I == 2 ? g0 * g1 : g0 * g1 * g2));
+                const float eLE = I == 3 ? 1.f : (I == 2 ? g3 : (I == 1 ? g2 * g3 : g1 * g2 * g3));
+                const float kx = kk[x] * kscale;
+                lk[e] = bb[x] * kx * F;
+                lq[e] = qq[x] * qscale * F;
+                kr[e] = kx * eR;
+                x1[e] = lk[e] * eGB;
+                qe[e] = lq[e] * eGB;
+                kd[e] = kr[e] * eLE;
+                xv[e] = ww[x] * vv[x];
+                r0[e] = kr[e] * ige[I * D + ci];      // row of R_I:     m = e^{G_{B_I} - G_{E_I}}
+                r2[e] = kr[e] * (I == 0 ? g1 : g2);   // row of R_{I+2}: m = ge_{I+1}
+                r3[e] = kr[e] * g1 * g2;              // row of R_3 when I = 0: m = ge_1 ge_2
+            }
+            wLk[x2] = pack_bf2(lk[0], lk[1]);
+            wLq[x2] = pack_bf2(lq[0], lq[1]);
+            wkr[x2] = pack_bf2(kr[0], kr[1]);
+            wr0[x2] = pack_bf2(r0[0], r0[1]);
+            wr2[x2] = pack_bf2(r2[0], r2[1]);
+            wr3[x2] = pack_bf2(r3[0], r3[1]);
+            wX1[x2] = pack_h2(x1[0], x1[1]);
+            wX2[x2] = pack_h2(xv[0], xv[1]);
+            wQe[x2] = pack_h2(qe[0], qe[1]);
+            wKd[x2] = pack_h2(kd[0], kd[1]);
+        }
+        auto u4 = [](const uint32_t (&w)[4]) { return make_uint4(w[0], w[1], w[2], w[3]); };
+        const int kb = cb / 64, chunk = (cb % 64) / 8;
+        *reinterpret_cast<uint4 *>(sm + C::oAL + kb * 16384 + swz(t, chunk)) = u4(wLk);
+        *reinterpret_cast<uint4 *>(sm + C::oAL + kb * 16384 + swz(64 + t, chunk)) = u4(wLq);
+        // rows of R_{I'} for I' >= I (R_{I+1} takes m = 1)
+        *reinterpret_cast<uint4 *>(sm + C::oR(I) + kb * (C::rows_R(I) * 128u) + swz(t, chunk)) = u4(wr0);
+        if (I + 1 < 4)
+            *reinterpret_cast<uint4 *>(sm + C::oR(I + 1) + kb * (C::rows_R(I + 1) * 128u) + swz(t, chunk)) =
+                u4(wkr);
+        if (I + 2 < 4)
+            *reinterpret_cast<uint4 *>(sm + C::oR(I + 2) + kb * (C::rows_R(I + 2) * 128u) + swz(t, chunk)) =
+                u4(wr2);
+        if (I == 0)
+            *reinterpret_cast<uint4 *>(sm + C::oR(3) + kb * (C::rows_R(3) * 128u) + swz(t, chunk)) = u4(wr3);
+        *reinterpret_cast<uint4 *>(sm + C::oBWU + (cb / 64) * 8192 + swz(t, chunk)) = u4(wX1);
+        *reinterpret_cast<uint4 *>(sm + C::oBWU + ((D + cb) / 64) * 8192 + swz(t, chunk)) = u4(wX2);
+        *reinterpret_cast<uint4 *>(rec + Rec<D>::A1 + kb * 16384 + swz(t, chunk)) = u4(wQe);
+        *reinterpret_cast<uint4 *>(rec + Rec<D>::KdT + kb * 8192 + swz(t, chunk)) = u4(wKd);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -276,18 +304,18 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     tc_fence_after();
     const uint32_t tm = tmem_slot;
 
-    // ---- 3. A and P on the tensor cores ---------------------------------------
+    // ---- 3. A and P on the tensor cores (bf16) --------------------------------
     if (tid == 0) {
         const uint32_t al = smem_u32(sm + C::oAL);
         uint32_t col = 0;
 #pragma unroll
-        for (int I = 0; I < 4; ++I) {
-            const uint32_t N = C::rows_R(I);
+        for (int Ib = 0; Ib < 4; ++Ib) {
+            const uint32_t N = C::rows_R(Ib);
             const uint32_t id = idesc_bf16(128, N, false, false);
-            const uint32_t rb = smem_u32(sm + C::oR(I));
+            const uint32_t rb = smem_u32(sm + C::oR(Ib));
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                mma_bf16(tm + col, desc_kmajor(al, 128, kk), desc_kmajor(rb, N, kk), id, kk > 0);
+                mma_f16(tm + col, desc_kmajor(al, 128, kk), desc_kmajor(rb, N, kk), id, kk > 0);
             col += N;
         }
         mma_commit(&bar_mma);
@@ -297,18 +325,18 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
 
     float *Af = reinterpret_cast<float *>(sm + C::oAf);
     if (warp < 4) {
-        // TMEM row r: r < 64 -> A row t = r, r >= 64 -> P row t = r - 64.  The
-        // 32 rows of a warp span row blocks Ilo and Ilo + 1; the warp loads the
-        // union of their column groups at warp-uniform addresses (tcgen05.ld is
-        // warp-collective) and each lane keeps the groups of its own block.
+        // TMEM row r: r < 64 -> A row r, r >= 64 -> P row r - 64.  A warp's 32
+        // rows span row blocks Ilo and Ilo + 1; the warp loads the union of their
+        // column groups at warp-uniform addresses (tcgen05.ld is warp-collective)
+        // and each lane keeps the groups of its own block.
         const int r = 32 * warp + lane;
         const int tt = r & 63;
-        const int I = tt / 16;
+        const int Ir = tt / 16;
         const int Ilo = 2 * (warp & 1);
         const uint32_t cbeg = 16u * (Ilo * (Ilo + 1) / 2);
         const uint32_t cend = 16u * ((Ilo + 2) * (Ilo + 3) / 2);
-        const uint32_t mycol0 = 16u * (I * (I + 1) / 2);
-        const uint32_t mycols = 16u * (I + 1);
+        const uint32_t mycol0 = 16u * (Ir * (Ir + 1) / 2);
+        const uint32_t mycols = 16u * (Ir + 1);
         __syncwarp();
 #pragma unroll 1
         for (uint32_t cg = cbeg; cg < cend; cg += 16) {
@@ -321,7 +349,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
 #pragma unroll
                     for (int x = 0; x < 16; ++x) {
                         const int s = s0 + x;
-                        Af[tt * 65 + s] = s < tt ? __uint_as_float(v[x]) : 0.f;
+                        Af[tt * kLD + s] = s < tt ? __uint_as_float(v[x]) : 0.f;
                     }
                 } else {
 #pragma unroll
@@ -332,85 +360,105 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
                             const int s = s0 + 8 * half + x;
                             f[x] = s <= tt ? __uint_as_float(v[8 * half + x]) : 0.f;
                         }
-                        *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, s0 / 8 + half)) = pack8(f);
+                        *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, s0 / 8 + half)) = pack8_h(f);
                     }
                 }
             }
         }
         if (r >= 64) {  // P columns past this row's block are zero
-            for (int chunk = 2 * (I + 1); chunk < 8; ++chunk)
+            for (int chunk = 2 * (Ir + 1); chunk < 8; ++chunk)
                 *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, chunk)) = make_uint4(0, 0, 0, 0);
         }
     }
     tc_fence_before();
     __syncthreads();
 
-    // ---- 4. T = (I + A)^{-1}, blocked forward substitution -----------------
+    // ---- 4. T = (I + A)^{-1}, blocked forward substitution (fp32) ---------------
     float *Tf = reinterpret_cast<float *>(sm + C::oTf);
     float *Yb = reinterpret_cast<float *>(sm + C::oY);
     if (tid < 64) {  // diagonal 16x16 blocks, one thread per (block, column)
-        const int I = tid / 16, j = tid % 16, o = 16 * I;
+        const int Ib = tid / 16, j = tid % 16, o = 16 * Ib;
         float x[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             float acc = (i == j) ? 1.f : 0.f;
 #pragma unroll
-            for (int m = 0; m < i; ++m) acc -= Af[(o + i) * 65 + o + m] * x[m];
+            for (int m = 0; m < i; ++m) acc -= Af[(o + i) * kLD + o + m] * x[m];
             x[i] = (i < j) ? 0.f : acc;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) Tf[(o + i) * 65 + o + j] = x[i];
+        for (int i = 0; i < 16; ++i) Tf[(o + i) * kLD + o + j] = x[i];
     }
     __syncthreads();
+    // off-diagonal blocks (I, J) = (J + d, J), level d = 1..3: warp J computes
+    // one block, a 2 x 4 register tile per lane
 #pragma unroll 1
     for (int d = 1; d < 4; ++d) {
-        const int nb = 4 - d;  // blocks (I, J) = (J + d, J), J = 0..nb-1
-        for (int e = tid; e < nb * 256; e += kIntraThreads) {
-            const int J = e / 256, i = (e % 256) / 16, j = e % 16;
-            const int I = J + d;
-            float acc = 0.f;  // Y = sum_{m=J}^{I-1} A_{I m} T_{m J}, row i, col j
-            for (int m = 16 * J; m < 16 * I; ++m) acc += Af[(16 * I + i) * 65 + m] * Tf[m * 65 + 16 * J + j];
-            Yb[e] = acc;
+        const int J = warp, Ib = J + d;
+        const int i0 = 2 * (lane / 4), j0 = 4 * (lane % 4);
+        if (Ib < 4) {
+            float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const float *a0 = Af + (16 * Ib + i0) * kLD;
+            const float *a1 = a0 + kLD;
+#pragma unroll 4
+            for (int m = 16 * J; m < 16 * Ib; ++m) {
+                const float4 tv = *reinterpret_cast<const float4 *>(Tf + m * kLD + 16 * J + j0);
+                const float x0 = a0[m], x1 = a1[m];
+                y[0][0] += x0 * tv.x; y[0][1] += x0 * tv.y; y[0][2] += x0 * tv.z; y[0][3] += x0 * tv.w;
+                y[1][0] += x1 * tv.x; y[1][1] += x1 * tv.y; y[1][2] += x1 * tv.z; y[1][3] += x1 * tv.w;
+            }
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+                *reinterpret_cast<float4 *>(Yb + J * 256 + (i0 + a) * 16 + j0) =
+                    make_float4(y[a][0], y[a][1], y[a][2], y[a][3]);
         }
         __syncthreads();
-        for (int e = tid; e < nb * 256; e += kIntraThreads) {
-            const int J = e / 256, i = (e % 256) / 16, j = e % 16;
-            const int I = J + d;
-            float acc = 0.f;  // T_{IJ} = -T_{II} Y
+        if (Ib < 4) {
+            float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const float *t0 = Tf + (16 * Ib + i0) * kLD + 16 * Ib;
+            const float *t1 = t0 + kLD;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc -= Tf[(16 * I + i) * 65 + 16 * I + m] * Yb[J * 256 + m * 16 + j];
-            Tf[(16 * I + i) * 65 + 16 * J + j] = acc;
+            for (int m = 0; m < 16; ++m) {
+                const float4 yv = *reinterpret_cast<const float4 *>(Yb + J * 256 + m * 16 + j0);
+                const float x0 = t0[m], x1 = t1[m];
+                y[0][0] -= x0 * yv.x; y[0][1] -= x0 * yv.y; y[0][2] -= x0 * yv.z; y[0][3] -= x0 * yv.w;
+                y[1][0] -= x1 * yv.x; y[1][1] -= x1 * yv.y; y[1][2] -= x1 * yv.z; y[1][3] -= x1 * yv.w;
+            }
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+                *reinterpret_cast<float4 *>(Tf + (16 * Ib + i0 + a) * kLD + 16 * J + j0) =
+                    make_float4(y[a][0], y[a][1], y[a][2], y[a][3]);
         }
         __syncthreads();
     }
-    // T -> bf16 K-major image [64 t][64 s]; zeros above the diagonal
+    // T -> fp16 K-major image [64 t][64 s]; zeros above the diagonal
     for (int e = tid; e < 64 * 8; e += kIntraThreads) {
         const int tt = e / 8, chunk = e % 8;
         float f[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) {
             const int s = 8 * chunk + x;
-            f[x] = s <= tt ? Tf[tt * 65 + s] : 0.f;
+            f[x] = s <= tt ? Tf[tt * kLD + s] : 0.f;
         }
-        *reinterpret_cast<uint4 *>(sm + C::oTimg + swz(tt, chunk)) = pack8(f);
+        *reinterpret_cast<uint4 *>(sm + C::oTimg + swz(tt, chunk)) = pack8_h(f);
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // ---- 5. [Wt | Ut] = T x [X1 | X2] ------------------------------------------
+    // ---- 5. [Wt | Ut] = T x [X1 | X2] (fp16) -----------------------------------
     if (tid == 0) {
-        constexpr uint32_t id = idesc_bf16(128, 2 * D, false, true);
+        constexpr uint32_t id = idesc_fp16(128, 2 * D, false, true);
         const uint32_t ti = smem_u32(sm + C::oTimg), bw = smem_u32(sm + C::oBWU);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_bf16(tm, desc_kmajor(ti, 128, kk), desc_mnmajor(bw, 64, kk), id, kk > 0);
+        for (int kk = 0; kk < 4; ++kk) mma_f16(tm, desc_kmajor(ti, 128, kk), desc_mnmajor(bw, 64, kk), id, kk > 0);
         mma_commit(&bar_mma);
     }
     if (!mbar_wait(&bar_mma, 1)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
     tc_fence_after();
 
-    // ---- 6. Wt -> A1 rows 64-127, Ut -> Ut image ------------------------------
+    // ---- 6. Wt -> A1 rows 64-127, Ut -> Ut image (fp16) -------------------------
     if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
         __syncwarp();
         const int q = warp & 3;
@@ -425,10 +473,10 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
             const int n0 = 32 * j, kb = n0 / 64, c0 = (n0 % 64) / 8;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                const uint4 o = make_uint4(pack2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
-                                           pack2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
-                                           pack2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
-                                           pack2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
+                const uint4 o = make_uint4(pack_h2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
+                                           pack_h2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
+                                           pack_h2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
+                                           pack_h2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
                 uint8_t *dst = is_u ? rec + Rec<D>::Ut + kb * 8192 + swz(tt, c0 + cc)
                                     : rec + Rec<D>::A1 + kb * 16384 + swz(64 + tt, c0 + cc);
                 *reinterpret_cast<uint4 *>(dst) = o;

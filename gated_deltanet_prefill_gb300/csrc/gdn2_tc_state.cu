@@ -5,8 +5,8 @@
 // columns of S evolve independently, so V tiles are exact).  The state S
 // (D x VT fp32) stays in Tensor Memory for the whole sequence.  Per chunk,
 // with the intra kernel's record (gdn2_record.cuh):
-//   MMA1  D1 = [Qe ; Wt] x S_bf16          (M=128, N=VT, K=D)
-//   epi   U  = Ut - (Wt S)  -> bf16 smem   (rows 64-127 of D1)
+//   MMA1  D1 = [Qe ; Wt] x S_fp16          (M=128, N=VT, K=D)
+//   epi   U  = Ut - (Wt S)  -> fp16 smem   (rows 64-127 of D1)
 //   MMA2  D1[0:64] += P x U                (M=128, K=64; rows 64-127 dead)
 //   MMA3  S  += Kd^T x U                   (M=128, K=64), S pre-scaled by eGL
 //   epi   o = scale * D1[0:64] -> bf16 global
@@ -14,9 +14,10 @@
 // pass, with burn-gdn2's "in-loop output phase".
 //
 // Warp roles (12 warps): 0 bulk-copy producer, 1 MMA issuer (and TMEM owner),
-// 4-7 state epilogue (S -> bf16 operand, S *= eGL), 8-9 output epilogue,
+// 4-7 state epilogue (S -> fp16 operand, S *= eGL), 8-9 output epilogue,
 // 10-11 U epilogue.  Every wait is time-bounded; a timeout sets the device
-// status word and the CTA unwinds.
+// status word and the CTA unwinds.  Operands are fp16 (10-bit mantissa,
+// saturating at +-65504); accumulation and the carried state are fp32.
 #include "gdn2_internal.cuh"
 #include "gdn2_record.cuh"
 #include "gdn2_tc.cuh"
@@ -38,8 +39,8 @@ struct StateCfg {
     static constexpr uint32_t sUt = sZero + (D == 64 ? 8192 : 0);
     static constexpr uint32_t sEGL = sUt + (VT / 64) * 8192;
     static constexpr uint32_t kStage = (sEGL + D * 4 + 1023) / 1024 * 1024;
-    static constexpr uint32_t oS = NSTAGE * kStage;                   // S bf16, MN-major B
-    static constexpr uint32_t oU = oS + (VT / 64) * D * 128;          // U bf16, MN-major B
+    static constexpr uint32_t oS = NSTAGE * kStage;                   // S fp16, MN-major B
+    static constexpr uint32_t oU = oS + (VT / 64) * D * 128;          // U fp16, MN-major B
     static constexpr uint32_t kSmem = oU + (VT / 64) * 8192 + 1024;   // + alignment slack
     static constexpr uint32_t kLoadBytes = Rec<D>::mma_prefix + (VT / 64) * 8192 + D * 4;
     static constexpr uint32_t kTmemCols = 3 * VT <= 256 ? 256 : 512;
@@ -48,14 +49,6 @@ struct StateCfg {
 
 __device__ __forceinline__ void set_timeout(const Params &p) {
     atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-__device__ __forceinline__ float2 unpack_bf16(uint32_t x) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x));
 }
 
 template <int D, int VT, int NSTAGE>
@@ -134,8 +127,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t id1 = idesc_bf16(128, VT, false, true);
-            constexpr uint32_t id3 = idesc_bf16(128, VT, true, true);
+            constexpr uint32_t id1 = idesc_fp16(128, VT, false, true);
+            constexpr uint32_t id3 = idesc_fp16(128, VT, true, true);
             for (int i = 0; i < nck; ++i) {
                 const int s = i % NSTAGE, b = i & 1;
                 if (!mbar_wait(&full_bar[s], (i / NSTAGE) & 1) || !mbar_wait(&s_ready, i & 1) ||
@@ -147,7 +140,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                 const uint32_t st = smem_u32(sm + s * C::kStage);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_bf16(tD1[b], desc_kmajor(st + C::sA1, 128, kk), desc_mnmajor(sS, D, kk), id1, kk > 0);
+                    mma_f16(tD1[b], desc_kmajor(st + C::sA1, 128, kk), desc_mnmajor(sS, D, kk), id1, kk > 0);
                 mma_commit(&d1_full[b]);
                 if (!mbar_wait(&u_ready, i & 1)) {
                     set_timeout(p);
@@ -156,10 +149,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tD1[b], desc_kmajor(st + C::sP, 128, kk), desc_mnmajor(sU, 64, kk), id1, 1);
+                    mma_f16(tD1[b], desc_kmajor(st + C::sP, 128, kk), desc_mnmajor(sU, 64, kk), id1, 1);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tS, desc_mnmajor(st + C::sKdT, 64, kk), desc_mnmajor(sU, 64, kk), id3, 1);
+                    mma_f16(tS, desc_mnmajor(st + C::sKdT, 64, kk), desc_mnmajor(sU, 64, kk), id3, 1);
                 mma_commit(&o_full[b]);
                 mma_commit(&s_full);
                 mma_commit(&empty_bar[s]);
@@ -209,10 +202,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         uint4 v;
-                        v.x = pack_bf16(__uint_as_float(r[8 * cc + 0]), __uint_as_float(r[8 * cc + 1]));
-                        v.y = pack_bf16(__uint_as_float(r[8 * cc + 2]), __uint_as_float(r[8 * cc + 3]));
-                        v.z = pack_bf16(__uint_as_float(r[8 * cc + 4]), __uint_as_float(r[8 * cc + 5]));
-                        v.w = pack_bf16(__uint_as_float(r[8 * cc + 6]), __uint_as_float(r[8 * cc + 7]));
+                        v.x = pack_h2(__uint_as_float(r[8 * cc + 0]), __uint_as_float(r[8 * cc + 1]));
+                        v.y = pack_h2(__uint_as_float(r[8 * cc + 2]), __uint_as_float(r[8 * cc + 3]));
+                        v.z = pack_h2(__uint_as_float(r[8 * cc + 4]), __uint_as_float(r[8 * cc + 5]));
+                        v.w = pack_h2(__uint_as_float(r[8 * cc + 6]), __uint_as_float(r[8 * cc + 7]));
                         *reinterpret_cast<uint4 *>(dst + swz(row, c0 + cc)) = v;
                     }
 #pragma unroll
@@ -269,10 +262,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         uint4 v;
-                        v.x = pack_bf16(__uint_as_float(r[8 * cc + 0]) * p.scale, __uint_as_float(r[8 * cc + 1]) * p.scale);
-                        v.y = pack_bf16(__uint_as_float(r[8 * cc + 2]) * p.scale, __uint_as_float(r[8 * cc + 3]) * p.scale);
-                        v.z = pack_bf16(__uint_as_float(r[8 * cc + 4]) * p.scale, __uint_as_float(r[8 * cc + 5]) * p.scale);
-                        v.w = pack_bf16(__uint_as_float(r[8 * cc + 6]) * p.scale, __uint_as_float(r[8 * cc + 7]) * p.scale);
+                        v.x = pack_bf2(__uint_as_float(r[8 * cc + 0]) * p.scale, __uint_as_float(r[8 * cc + 1]) * p.scale);
+                        v.y = pack_bf2(__uint_as_float(r[8 * cc + 2]) * p.scale, __uint_as_float(r[8 * cc + 3]) * p.scale);
+                        v.z = pack_bf2(__uint_as_float(r[8 * cc + 4]) * p.scale, __uint_as_float(r[8 * cc + 5]) * p.scale);
+                        v.w = pack_bf2(__uint_as_float(r[8 * cc + 6]) * p.scale, __uint_as_float(r[8 * cc + 7]) * p.scale);
                         reinterpret_cast<uint4 *>(orow + 32 * j)[cc] = v;
                     }
                 }
@@ -306,9 +299,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                     uint32_t ow[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 a = unpack_bf16(uw[e]);
-                        ow[e] = pack_bf16(a.x - __uint_as_float(r[8 * cc + 2 * e]),
-                                          a.y - __uint_as_float(r[8 * cc + 2 * e + 1]));
+                        const float2 a = unpack_h2(uw[e]);
+                        ow[e] = pack_h2(a.x - __uint_as_float(r[8 * cc + 2 * e]),
+                                        a.y - __uint_as_float(r[8 * cc + 2 * e + 1]));
                     }
                     *reinterpret_cast<uint4 *>(sm + C::oU + blk * 8192 + swz(t, c0 + cc)) =
                         make_uint4(ow[0], ow[1], ow[2], ow[3]);
