@@ -305,11 +305,10 @@ def run_ours(args):
     import torch
     import torch.distributed as dist
     from gated_deltanet_prefill_gb300 import build as gbuild
+    from gated_deltanet_prefill_gb300 import dist as gdist
     from gated_deltanet_prefill_gb300 import gdn2, inputs
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local = gdist.rank_world()
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
@@ -320,7 +319,7 @@ def run_ours(args):
     gdn2.load()
 
     wl = inputs.workload(args.workload)
-    wl_r = inputs.with_seed(wl, wl.seed + 1000 * rank)  # each rank: its own batch
+    wl_r = inputs.with_seed(wl, gdist.rank_seed(wl.seed, rank))  # each rank: its own batch
     d = inputs.generate(wl_r, device="cuda")
     T, HV, V = wl.T_tot, wl.HV, wl.V
     out = torch.empty((T, HV, V), dtype=torch.bfloat16, device="cuda")
@@ -358,11 +357,7 @@ def run_ours(args):
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms = start.elapsed_time(end) / K
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = gdist.max_over_ranks(start.elapsed_time(end) / K, device="cuda")
     stage_ms = {n: sum(ev[i].elapsed_time(ev[i + 1]) for ev in stage_evs) / K for i, n in enumerate(names)}
 
     # roofline of the dominant kernel
@@ -397,12 +392,8 @@ def run_ours(args):
             runner()
         ee.record(stream)
         torch.cuda.synchronize()
-        ems = es.elapsed_time(ee) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([ems], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * T / (ems * 1e-3), "unit": "tokens/s",
+        ems = gdist.max_over_ranks(es.elapsed_time(ee) / args.e2e_steps, device="cuda")
+        e2e = {"value": gdist.aggregate_throughput(T, world, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
                "ms_per_step": ems, "steps": args.e2e_steps}
         del runner, host
@@ -412,7 +403,8 @@ def run_ours(args):
         cpu = cpu_baseline(d, wl, args.cpu_seconds)
 
     if rank == 0:
-        line = {"metric": METRIC, "value": world * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        line = {"metric": METRIC, "value": gdist.aggregate_throughput(T, world, ms), "unit": "tokens/s",
+                "n_gpus": world,
                 "steps": K, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if args.kernels == "tc" else "f32", "data": "synthetic",

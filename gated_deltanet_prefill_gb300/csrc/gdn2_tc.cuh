@@ -212,6 +212,15 @@ __host__ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
     return (row >> 3) * 1024u + (row & 7u) * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// 2^x on the special-function unit (PTX ex2.approx, flush-to-zero): used on
+// log2(e)-prescaled decay exponents, which are <= 0 except for the documented
+// sub-chunk factor.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ----------------------------------------------------------- conversions
 // fp16 intermediates saturate at +-65504 instead of overflowing to inf.
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {

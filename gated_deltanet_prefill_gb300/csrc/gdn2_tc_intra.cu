@@ -14,9 +14,10 @@
 //        eR_s = e^{G_{E_J} - G_s} <= 1, m_{I,J} = e^{G_{B_I} - G_{E_J}}
 //     (m <= 1 for J < I; m = e^{+decay of sub-chunk I} for J = I).  Every m is
 //     a product of the per-sub-chunk decays ge_J = e^{G_{E_J} - G_{E_{J-1}}}.
-//  3. tcgen05 (bf16): for each row block I, [beta k F ; q F] (M=128) x R_I^T
-//     with R_I = k eR m_{I,.} (N = 16(I+1)); rows of block I give A (strictly
-//     lower) and P (lower incl. diagonal).
+//  3. tcgen05 (bf16): [beta k F ; q F] (M=128) x [R_0; R_1; R_2; R_3]^T, one
+//     N = 160 product, where R_I = k eR m_{I,.} holds the 16(I+1) tokens of row
+//     blocks <= I; the rows of block I against R_I give A (strictly lower) and
+//     P (lower incl. diagonal).
 //  4. T = (I + A)^{-1} by blocked forward substitution in fp32.
 //  5. tcgen05 (fp16): [Wt | Ut] = T x [beta k e^G | w v]  (M=128, N=2D, K=64).
 //  6. write Qe, Kd^T, P, Wt, Ut (fp16) and eGL (fp32) as shared-memory images.
@@ -39,14 +40,14 @@ constexpr int kLD = 68;  // row stride (floats) of the fp32 solver matrices
 
 template <int D>
 struct IntraCfg {
-    // region X: A_left image (bf16, M=128, K=D) then the four R_I images (bf16)
+    // region X: A_left image (bf16, M=128, K=D), then the right operands R_0..R_3
+    // stacked as one K-major tile of 160 rows (R_I at row 16 I (I + 1) / 2)
     static constexpr uint32_t oAL = 0;
     static constexpr uint32_t kAL = (D / 64) * 16384;
-    __host__ __device__ static constexpr uint32_t rows_R(int I) { return 16u * (I + 1); }
-    __host__ __device__ static constexpr uint32_t oR(int I) {
-        return kAL + (D / 64) * 128u * 16u * (I * (I + 1) / 2);
-    }
-    static constexpr uint32_t kOperands = kAL + (D / 64) * 128u * 160u;
+    static constexpr uint32_t oR = kAL;
+    static constexpr uint32_t kRrows = 160;
+    __host__ __device__ static constexpr uint32_t row_R(int I) { return 16u * (I * (I + 1) / 2); }
+    static constexpr uint32_t kOperands = kAL + (D / 64) * 128u * kRrows;
     static constexpr uint32_t kX = kOperands > 46080u ? kOperands : 46080u;
     // reused after the A/P MMA: fp32 solver matrices and the fp16 T image
     static constexpr uint32_t oAf = 0;                         // [64][kLD]
@@ -56,15 +57,19 @@ struct IntraCfg {
     // [beta k e^G | w v] fp16 MN-major B (N = 2D, K = 64); G scratch before
     static constexpr uint32_t oBWU = kX;
     static constexpr uint32_t kBWU = (2 * D / 64) * 8192;
-    // per-channel tables gE[4][D], ge[4][D], ige[4][D]; scan totals [parts][D]
+    // per-channel tables (log2-scaled G): gE[4][D] = G'_{E_J}, tGB[4][D] =
+    // e^{G_{B_I}}, tI[4][D] = e^{G_{B_I} - G_{E_I}}, t2[2][D] = e^{G_{E_{I+1}} -
+    // G_{E_I}}; the scan totals use the same area before the tables exist
     static constexpr uint32_t oTab = oBWU + kBWU;
-    static constexpr uint32_t oTot = oTab + 3 * 4 * D * 4;
-    static constexpr uint32_t kSmem = oTot + (kIntraThreads / D) * D * 4 + 1024;  // + alignment slack
+    static constexpr uint32_t kTab = 14 * D * 4;
+    static constexpr uint32_t oBar = oTab + kTab;               // mbarrier + TMEM slot
+    static constexpr uint32_t kSmem = oBar + 16 + 1024;         // + alignment slack
     static constexpr uint32_t kTmemCols = 256;
     static_assert(oTimg >= oY + 3 * 1024, "solver buffers overlap the T image");
     static_assert(kBWU >= 64 * D * 4, "G scratch must fit in the B operand area");
-    // two CTAs per SM: 2 x (dynamic + 64 B static + 1 KB reserved) <= 228 KB
-    static_assert(2 * (kSmem + 64 + 1024) <= 228 * 1024, "two CTAs per SM");
+    static_assert(kTab >= (kIntraThreads / D) * D * 4, "scan totals must fit in the table area");
+    // two CTAs per SM: 2 x (dynamic + 1 KB reserved) <= 228 KB
+    static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
 __device__ __forceinline__ uint4 ldg16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
@@ -83,8 +88,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     constexpr int ROWS = 64 / PARTS;   // rows per scan part
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t bar_mma;
-    __shared__ uint32_t tmem_slot;
+    uint64_t &bar_mma = *reinterpret_cast<uint64_t *>(sm + C::oBar);
+    uint32_t &tmem_slot = *reinterpret_cast<uint32_t *>(sm + C::oBar + 8);
 
     const int c = blockIdx.x, hv = blockIdx.y;
     const int seq = p.chunk_seq[c];
@@ -160,47 +165,70 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         kscale = 1.f / fmaxf(sqrtf(sk), 1e-12f);
         qscale = 1.f / fmaxf(sqrtf(sq), 1e-12f);
     }
+    // G' = G log2(e): every decay factor below is an exact power of two of a
+    // difference of G' values
+    constexpr float kLog2e = 1.4426950408889634f;
     float *Gs = reinterpret_cast<float *>(sm + C::oBWU);
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         const int cb = 8 * (seg + 4 * j);
-        *reinterpret_cast<float4 *>(Gs + gidx<D>(t, cb)) = graw[2 * j];
-        *reinterpret_cast<float4 *>(Gs + gidx<D>(t, cb + 4)) = graw[2 * j + 1];
+        float4 a = graw[2 * j], b = graw[2 * j + 1];
+        a.x *= kLog2e; a.y *= kLog2e; a.z *= kLog2e; a.w *= kLog2e;
+        b.x *= kLog2e; b.y *= kLog2e; b.z *= kLog2e; b.w *= kLog2e;
+        *reinterpret_cast<float4 *>(Gs + gidx<D>(t, cb)) = a;
+        *reinterpret_cast<float4 *>(Gs + gidx<D>(t, cb + 4)) = b;
     }
     __syncthreads();
-    float *tot = reinterpret_cast<float *>(sm + C::oTot);  // [PARTS][D]
+    float *tot = reinterpret_cast<float *>(sm + C::oTab);  // [PARTS][D], before the tables
     {
+        // rows come in groups of 8, so the (t & 7) swizzle of each row in a
+        // group is a compile-time constant
         const int ch = tid % D, part = tid / D;
+        const int c4 = ch >> 2, c3 = ch & 3;
+        float *base = Gs + part * ROWS * D + c3;
         float acc = 0.f;
-#pragma unroll 8
-        for (int r = part * ROWS; r < (part + 1) * ROWS; ++r) {
-            acc += Gs[gidx<D>(r, ch)];
-            Gs[gidx<D>(r, ch)] = acc;
+#pragma unroll 1
+        for (int r8 = 0; r8 < ROWS; r8 += 8) {
+            float *b8 = base + r8 * D;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                float *a = b8 + k * D + ((c4 ^ k) << 2);
+                acc += *a;
+                *a = acc;
+            }
         }
         tot[part * D + ch] = acc;
         __syncthreads();
         float off = 0.f;
         for (int pp = 0; pp < part; ++pp) off += tot[pp * D + ch];
         if (part > 0) {
-#pragma unroll 8
-            for (int r = part * ROWS; r < (part + 1) * ROWS; ++r) Gs[gidx<D>(r, ch)] += off;
+#pragma unroll 1
+            for (int r8 = 0; r8 < ROWS; r8 += 8) {
+                float *b8 = base + r8 * D;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) b8[k * D + ((c4 ^ k) << 2)] += off;
+            }
         }
     }
     __syncthreads();
-    float *gE = reinterpret_cast<float *>(sm + C::oTab);  // G at E_J
-    float *ge = gE + 4 * D;                               // e^{G_{E_J} - G_{E_{J-1}}}
-    float *ige = ge + 4 * D;                              // 1 / ge
+    float *gE = reinterpret_cast<float *>(sm + C::oTab);  // G' at E_J
+    float *tGB = gE + 4 * D;                              // e^{G_{B_I}}
+    float *tI = tGB + 4 * D;                              // e^{G_{B_I} - G_{E_I}}
+    float *t2 = tI + 4 * D;                               // e^{G_{E_{I+1}} - G_{E_I}}, I = 0, 1
     if (tid < D) {
-        float prev = 0.f;
+        float e[4];
+#pragma unroll
+        for (int J = 0; J < 4; ++J) e[J] = Gs[gidx<D>(min(16 * J + 15, len - 1), tid)];
 #pragma unroll
         for (int J = 0; J < 4; ++J) {
-            const float gv = Gs[gidx<D>(min(16 * J + 15, len - 1), tid)];
-            gE[J * D + tid] = gv;
-            ge[J * D + tid] = __expf(gv - prev);
-            ige[J * D + tid] = __expf(prev - gv);
-            prev = gv;
+            const float b = J > 0 ? e[J - 1] : 0.f;
+            gE[J * D + tid] = e[J];
+            tGB[J * D + tid] = ex2(b);
+            tI[J * D + tid] = ex2(b - e[J]);
         }
-        reinterpret_cast<float *>(rec + Rec<D>::eGL)[tid] = __expf(prev);
+        t2[tid] = ex2(e[1] - e[0]);
+        t2[D + tid] = ex2(e[2] - e[1]);
+        reinterpret_cast<float *>(rec + Rec<D>::eGL)[tid] = ex2(e[3]);
     }
     float Gr[8 * NJ];
 #pragma unroll
@@ -248,25 +276,24 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
             for (int e = 0; e < 2; ++e) {
                 const int x = 2 * x2 + e;
                 const int ci = cb + x;
-                const float g0 = ge[ci], g1 = ge[D + ci], g2 = ge[2 * D + ci], g3 = ge[3 * D + ci];
                 const float gB = I > 0 ? gE[(I - 1) * D + ci] : 0.f;
                 const float gt = Gr[8 * j + x];
-                const float F = __expf(gt - gB);
-                const float eR = __expf(gE[I * D + ci] - gt);
-                // e^{G_{B_I}} and e^{G_L - G_{E_I}} as products of sub-chunk decays
-                const float eGB = I == 0 ? 1.f : (I == 1 ? g0 : (I == 2 ? g0 * g1 : g0 * g1 * g2));
-                const float eLE = I == 3 ? 1.f : (I == 2 ? g3 : (I == 1 ? g2 * g3 : g1 * g2 * g3));
+                const float F = ex2(gt - gB);                         // e^{G_t - G_{B_I}}
+                const float eR = ex2(gE[I * D + ci] - gt);            // e^{G_{E_I} - G_t}
+                const float eL = ex2(gE[3 * D + ci] - gt);            // e^{G_L - G_t}
+                const float eGB = tGB[I * D + ci];                    // e^{G_{B_I}}
                 const float kx = kk[x] * kscale;
                 lk[e] = bb[x] * kx * F;
                 lq[e] = qq[x] * qscale * F;
                 kr[e] = kx * eR;
                 x1[e] = lk[e] * eGB;
                 qe[e] = lq[e] * eGB;
-                kd[e] = kr[e] * eLE;
+                kd[e] = kx * eL;
                 xv[e] = ww[x] * vv[x];
-                r0[e] = kr[e] * ige[I * D + ci];      // row of R_I:     m = e^{G_{B_I} - G_{E_I}}
-                r2[e] = kr[e] * (I == 0 ? g1 : g2);   // row of R_{I+2}: m = ge_{I+1}
-                r3[e] = kr[e] * g1 * g2;              // row of R_3 when I = 0: m = ge_1 ge_2
+                r0[e] = kr[e] * tI[I * D + ci];                       // row of R_I
+                const float f2 = t2[(I & 1) * D + ci];                // e^{G_{E_{I+1}} - G_{E_I}}
+                r2[e] = kr[e] * f2;                                   // row of R_{I+2}, I <= 1
+                r3[e] = r2[e] * t2[D + ci];                           // row of R_3, I = 0
             }
             wLk[x2] = pack_bf2(lk[0], lk[1]);
             wLq[x2] = pack_bf2(lq[0], lq[1]);
@@ -283,16 +310,12 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         const int kb = cb / 64, chunk = (cb % 64) / 8;
         *reinterpret_cast<uint4 *>(sm + C::oAL + kb * 16384 + swz(t, chunk)) = u4(wLk);
         *reinterpret_cast<uint4 *>(sm + C::oAL + kb * 16384 + swz(64 + t, chunk)) = u4(wLq);
-        // rows of R_{I'} for I' >= I (R_{I+1} takes m = 1)
-        *reinterpret_cast<uint4 *>(sm + C::oR(I) + kb * (C::rows_R(I) * 128u) + swz(t, chunk)) = u4(wr0);
-        if (I + 1 < 4)
-            *reinterpret_cast<uint4 *>(sm + C::oR(I + 1) + kb * (C::rows_R(I + 1) * 128u) + swz(t, chunk)) =
-                u4(wkr);
-        if (I + 2 < 4)
-            *reinterpret_cast<uint4 *>(sm + C::oR(I + 2) + kb * (C::rows_R(I + 2) * 128u) + swz(t, chunk)) =
-                u4(wr2);
-        if (I == 0)
-            *reinterpret_cast<uint4 *>(sm + C::oR(3) + kb * (C::rows_R(3) * 128u) + swz(t, chunk)) = u4(wr3);
+        // rows of R_{I'} for I' >= I (R_{I+1} takes m = 1) in the stacked 160-row tile
+        uint8_t *rt = sm + C::oR + kb * (C::kRrows * 128u);
+        *reinterpret_cast<uint4 *>(rt + swz(C::row_R(I) + t, chunk)) = u4(wr0);
+        if (I + 1 < 4) *reinterpret_cast<uint4 *>(rt + swz(C::row_R(I + 1) + t, chunk)) = u4(wkr);
+        if (I + 2 < 4) *reinterpret_cast<uint4 *>(rt + swz(C::row_R(I + 2) + t, chunk)) = u4(wr2);
+        if (I == 0) *reinterpret_cast<uint4 *>(rt + swz(C::row_R(3) + t, chunk)) = u4(wr3);
         *reinterpret_cast<uint4 *>(sm + C::oBWU + (cb / 64) * 8192 + swz(t, chunk)) = u4(wX1);
         *reinterpret_cast<uint4 *>(sm + C::oBWU + ((D + cb) / 64) * 8192 + swz(t, chunk)) = u4(wX2);
         *reinterpret_cast<uint4 *>(rec + Rec<D>::A1 + kb * 16384 + swz(t, chunk)) = u4(wQe);
@@ -305,43 +328,38 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     const uint32_t tm = tmem_slot;
 
     // ---- 3. A and P on the tensor cores (bf16) --------------------------------
-    if (tid == 0) {
-        const uint32_t al = smem_u32(sm + C::oAL);
-        uint32_t col = 0;
+    if (tid == 0) {  // one N = 160 chain: columns 16 I (I + 1) / 2 .. hold R_I
+        const uint32_t al = smem_u32(sm + C::oAL), rb = smem_u32(sm + C::oR);
+        constexpr uint32_t id = idesc_bf16(128, C::kRrows, false, false);
 #pragma unroll
-        for (int Ib = 0; Ib < 4; ++Ib) {
-            const uint32_t N = C::rows_R(Ib);
-            const uint32_t id = idesc_bf16(128, N, false, false);
-            const uint32_t rb = smem_u32(sm + C::oR(Ib));
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                mma_f16(tm + col, desc_kmajor(al, 128, kk), desc_kmajor(rb, N, kk), id, kk > 0);
-            col += N;
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+            mma_f16(tm, desc_kmajor(al, 128, kk), desc_kmajor(rb, C::kRrows, kk), id, kk > 0);
         mma_commit(&bar_mma);
     }
     if (!mbar_wait(&bar_mma, 0)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
     tc_fence_after();
 
     float *Af = reinterpret_cast<float *>(sm + C::oAf);
-    if (warp < 4) {
+    {
         // TMEM row r: r < 64 -> A row r, r >= 64 -> P row r - 64.  A warp's 32
         // rows span row blocks Ilo and Ilo + 1; the warp loads the union of their
-        // column groups at warp-uniform addresses (tcgen05.ld is warp-collective)
-        // and each lane keeps the groups of its own block.
-        const int r = 32 * warp + lane;
+        // 16-column groups at warp-uniform addresses (tcgen05.ld is
+        // warp-collective) and each lane keeps the groups of its own block.
+        // Warps w and w + 4 share lane quarter w % 4 and take alternate groups.
+        const int wq = warp & 3;
+        const int r = 32 * wq + lane;
         const int tt = r & 63;
         const int Ir = tt / 16;
-        const int Ilo = 2 * (warp & 1);
-        const uint32_t cbeg = 16u * (Ilo * (Ilo + 1) / 2);
+        const int Ilo = 2 * (wq & 1);
+        const uint32_t cbeg = 16u * (Ilo * (Ilo + 1) / 2) + 16u * (warp >> 2);
         const uint32_t cend = 16u * ((Ilo + 2) * (Ilo + 3) / 2);
         const uint32_t mycol0 = 16u * (Ir * (Ir + 1) / 2);
         const uint32_t mycols = 16u * (Ir + 1);
         __syncwarp();
 #pragma unroll 1
-        for (uint32_t cg = cbeg; cg < cend; cg += 16) {
+        for (uint32_t cg = cbeg; cg < cend; cg += 32) {
             uint32_t v[16];
-            tmem_ld16(tm + (static_cast<uint32_t>(32 * warp) << 16) + cg, v);
+            tmem_ld16(tm + (static_cast<uint32_t>(32 * wq) << 16) + cg, v);
             tmem_ld_wait();
             if (cg >= mycol0 && cg < mycol0 + mycols) {
                 const int s0 = static_cast<int>(cg - mycol0);
@@ -365,7 +383,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
                 }
             }
         }
-        if (r >= 64) {  // P columns past this row's block are zero
+        if (r >= 64 && warp < 4) {  // P columns past this row's block are zero
             for (int chunk = 2 * (Ir + 1); chunk < 8; ++chunk)
                 *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, chunk)) = make_uint4(0, 0, 0, 0);
         }
@@ -466,20 +484,25 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         const bool is_u = warp >= 4;
         const uint32_t cbase = is_u ? D : 0;
 #pragma unroll 1
-        for (int j = 0; j < D / 32; ++j) {
-            uint32_t v[32];
-            tmem_ld32(tm + (static_cast<uint32_t>(32 * q) << 16) + cbase + 32 * j, v);
+        for (int j2 = 0; j2 < D / 32; j2 += 2) {  // two 32-column groups per TMEM round trip
+            uint32_t v[2][32];
+            tmem_ld32(tm + (static_cast<uint32_t>(32 * q) << 16) + cbase + 32 * j2, v[0]);
+            tmem_ld32(tm + (static_cast<uint32_t>(32 * q) << 16) + cbase + 32 * (j2 + 1), v[1]);
             tmem_ld_wait();
-            const int n0 = 32 * j, kb = n0 / 64, c0 = (n0 % 64) / 8;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const uint4 o = make_uint4(pack_h2(__uint_as_float(v[8 * cc]), __uint_as_float(v[8 * cc + 1])),
-                                           pack_h2(__uint_as_float(v[8 * cc + 2]), __uint_as_float(v[8 * cc + 3])),
-                                           pack_h2(__uint_as_float(v[8 * cc + 4]), __uint_as_float(v[8 * cc + 5])),
-                                           pack_h2(__uint_as_float(v[8 * cc + 6]), __uint_as_float(v[8 * cc + 7])));
-                uint8_t *dst = is_u ? rec + Rec<D>::Ut + kb * 8192 + swz(tt, c0 + cc)
-                                    : rec + Rec<D>::A1 + kb * 16384 + swz(64 + tt, c0 + cc);
-                *reinterpret_cast<uint4 *>(dst) = o;
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int n0 = 32 * (j2 + h2), kb = n0 / 64, c0 = (n0 % 64) / 8;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint32_t *w = v[h2] + 8 * cc;
+                    const uint4 o = make_uint4(pack_h2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                               pack_h2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                               pack_h2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                                               pack_h2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+                    uint8_t *dst = is_u ? rec + Rec<D>::Ut + kb * 8192 + swz(tt, c0 + cc)
+                                        : rec + Rec<D>::A1 + kb * 16384 + swz(64 + tt, c0 + cc);
+                    *reinterpret_cast<uint4 *>(dst) = o;
+                }
             }
         }
     }

@@ -13,9 +13,10 @@
 // which is the FlashRT page's WY chain (chunk_h then output_o) fused into one
 // pass, with burn-gdn2's "in-loop output phase".
 //
-// Warp roles (12 warps): 0 bulk-copy producer, 1 MMA issuer (and TMEM owner),
-// 4-7 state epilogue (S -> fp16 operand, S *= eGL), 8-9 output epilogue,
-// 10-11 U epilogue.  Every wait is time-bounded; a timeout sets the device
+// Warp roles (16 warps): 0 bulk-copy producer, 1 MMA issuer (and TMEM owner),
+// 4-11 state epilogue (S -> fp16 operand, S *= eGL; two warps per TMEM lane
+// quarter, each half of the columns), 2-3 and 14-15 U epilogue (the Wt S rows
+// live in lane quarters 2 and 3), 12-13 output epilogue.  Every wait is time-bounded; a timeout sets the device
 // status word and the CTA unwinds.  Operands are fp16 (10-bit mantissa,
 // saturating at +-65504); accumulation and the carried state are fp32.
 #include "gdn2_internal.cuh"
@@ -28,7 +29,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStateThreads = 384;
+constexpr int kStateThreads = 512;
 
 template <int D, int VT, int NSTAGE>
 struct StateCfg {
@@ -71,8 +72,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
-        mbar_init(&s_ready, 128);
-        mbar_init(&u_ready, 64);
+        mbar_init(&s_ready, 256);
+        mbar_init(&u_ready, 128);
         mbar_init(&s_full, 1);
         mbar_init(&drain, 1);
         for (int b = 0; b < 2; ++b) {
@@ -160,16 +161,17 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             mma_commit(&drain);
             if (!mbar_wait(&drain, 0)) set_timeout(p);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------- state epilogue (S rows = key channels)
         const int q = warp & 3;
         const int row = 32 * q + lane;
         const bool active = row < D;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const int j0 = warp < 8 ? 0 : VT / 64, j1 = warp < 8 ? VT / 64 : VT / 32;  // 32-column groups
         if (active) {
             const float *h0 = p.h0 ? p.h0 + ((static_cast<size_t>(n) * p.HV + hv) * D + row) * D + v0 : nullptr;
 #pragma unroll 1
-            for (int j = 0; j < VT / 32; ++j) {
+            for (int j = j0; j < j1; ++j) {
                 uint32_t r[32];
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             if (active) {
                 const float egl = reinterpret_cast<const float *>(sm + s * C::kStage + C::sEGL)[row];
 #pragma unroll 1
-                for (int j = 0; j < VT / 32; ++j) {
+                for (int j = j0; j < j1; ++j) {
                     uint32_t r[32];
                     tmem_ld32(tS + lane_base + 32 * j, r);
                     tmem_ld_wait();
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
         if (ok && active && p.hT) {
             float *hT = p.hT + ((static_cast<size_t>(n) * p.HV + hv) * D + row) * D + v0;
 #pragma unroll 1
-            for (int j = 0; j < VT / 32; ++j) {
+            for (int j = j0; j < j1; ++j) {
                 uint32_t r[32];
                 tmem_ld32(tS + lane_base + 32 * j, r);
                 tmem_ld_wait();
@@ -237,11 +239,13 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                                     __uint_as_float(r[e + 3]));
             }
         }
-    } else if (warp == 8 || warp == 9) {
+    } else if (warp == 12 || warp == 13) {
         // ----------------------------------------- output epilogue (tokens 0-63)
         const int q = warp & 3;  // 0 or 1
         const int t = 32 * q + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        // chunk i of sequence n covers tokens [cu[n] + 64 i, min(cu[n] + 64 i + 64, cu[n + 1]))
+        const int64_t seq_start = cu_at(p, n), seq_end = cu_at(p, n + 1);
         for (int i = 0; i < nck; ++i) {
             const int b = i & 1;
             if (!warp_wait(&o_full[b], (i >> 1) & 1)) {
@@ -249,9 +253,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                 break;
             }
             tc_fence_after();
-            const int ck = first + i;
-            const int64_t tok = p.chunk_start[ck] + t;
-            const bool valid = t < p.chunk_len[ck];
+            const int64_t tok = seq_start + static_cast<int64_t>(i) * kChunk + t;
+            const bool valid = tok < seq_end;
             bf16 *orow = p.o + tok * p.so_t + static_cast<int64_t>(hv) * p.so_h + v0;
 #pragma unroll 1
             for (int j = 0; j < VT / 32; ++j) {
@@ -273,11 +276,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             tc_fence_before();
             mbar_arrive(&d1_free[b]);
         }
-    } else if (warp == 10 || warp == 11) {
+    } else if (warp == 2 || warp == 3 || warp == 14 || warp == 15) {
         // ----------------------------------- U epilogue (D1 rows 64-127 = Wt S)
         const int q = warp & 3;  // 2 or 3
         const int t = 32 * (q - 2) + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const int j0 = warp < 4 ? 0 : VT / 64, j1 = warp < 4 ? VT / 64 : VT / 32;  // 32-column groups
         for (int i = 0; i < nck; ++i) {
             const int s = i % NSTAGE, b = i & 1;
             if (!warp_wait(&d1_full[b], (i >> 1) & 1) || !warp_wait(&full_bar[s], (i / NSTAGE) & 1)) {
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             tc_fence_after();
             const uint8_t *ut = sm + s * C::kStage + C::sUt;
 #pragma unroll 1
-            for (int j = 0; j < VT / 32; ++j) {
+            for (int j = j0; j < j1; ++j) {
                 uint32_t r[32];
                 tmem_ld32(tD1[b] + lane_base + 32 * j, r);
                 tmem_ld_wait();
