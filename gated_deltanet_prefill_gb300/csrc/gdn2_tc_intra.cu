@@ -1,7 +1,8 @@
 // Tensor-core intra-chunk kernel: everything of a 64-token chunk that does
 // not depend on the incoming state, written as the record the state kernel
-// consumes (gdn2_record.cuh).  One CTA per (chunk, value head), 256 threads,
-// two CTAs per SM.
+// consumes (gdn2_record.cuh).  Persistent: two CTAs of 256 threads per SM walk
+// the (chunk, value head) items; each CTA loads its next item's inputs while
+// the current one is in its solve and epilogues.
 //
 // Steps (FlashRT gated-delta-attention page: norm/cumsum, kkt, solve_tril,
 // recompute_wu; fused into one kernel here, with GDN-2's channel-wise gates):
@@ -91,24 +92,10 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     uint64_t &bar_mma = *reinterpret_cast<uint64_t *>(sm + C::oBar);
     uint32_t &tmem_slot = *reinterpret_cast<uint32_t *>(sm + C::oBar + 8);
 
-    const int c = blockIdx.x, hv = blockIdx.y;
-    const int seq = p.chunk_seq[c];
-    if (seq < 0) return;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int64_t start = p.chunk_start[c];
-    const int len = p.chunk_len[c];
-    const int h = hv / p.group;
     const int t = tid / 4, seg = tid % 4;
     const int I = t / 16;
-    const bool live = t < len;
-    const int64_t tok = start + (live ? t : 0);
-    uint8_t *rec = p.rec + (static_cast<size_t>(c) * p.HV + hv) * Rec<D>::bytes;
-    const bf16 *kp = p.k + tok * p.sk_t + static_cast<int64_t>(h) * p.sk_h;
-    const bf16 *qp = p.q + tok * p.sq_t + static_cast<int64_t>(h) * p.sq_h;
-    const bf16 *bp = p.beta + tok * p.sb_t + static_cast<int64_t>(hv) * p.sb_h;
-    const bf16 *vp = p.v + tok * p.sv_t + static_cast<int64_t>(hv) * p.sv_h;
-    const bf16 *wp = p.w + tok * p.sw_t + static_cast<int64_t>(hv) * p.sw_h;
-    const float *gp = p.g + tok * p.sg_t + static_cast<int64_t>(hv) * p.sg_h;
+    const int total = p.status[0] == GDN2_OK ? p.status[1] * p.HV : 0;  // (chunk, value head) items
 
     if (tid == 0) {
         mbar_init(&bar_mma, 1);
@@ -119,22 +106,53 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         tmem_relinquish();
     }
 
-    // ---- 1. loads, cumsum ------------------------------------------------------
+    // Per-item inputs.  The CTA walks items it = blockIdx.x, + gridDim.x, ...;
+    // the next item's g is loaded while the current item is in its solve and
+    // epilogues; its first operand chunk is loaded at the start of its cumsum.
+    int c = 0, hv = 0, len = 1, h = 0;
+    bool live = false;
+    const bf16 *kp = nullptr, *qp = nullptr, *bp = nullptr, *vp = nullptr, *wp = nullptr;
     const uint4 z4 = make_uint4(0, 0, 0, 0);
     float4 graw[2 * NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        const int cb = 8 * (seg + 4 * j);
-        graw[2 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        graw[2 * j + 1] = graw[2 * j];
-        if (live && p.has_g) {
-            graw[2 * j] = __ldg(reinterpret_cast<const float4 *>(gp + cb));
-            graw[2 * j + 1] = __ldg(reinterpret_cast<const float4 *>(gp + cb + 4));
-        }
-    }
-    // chunk-0 operands, prefetched; later chunks are fetched one ahead
     uint4 nk = z4, nq = z4, nb = z4, nv = z4, nw = z4;
-    if (live) {
+    auto fetch = [&](int it) {
+        c = it / p.HV;
+        hv = it - c * p.HV;
+        const int64_t start = p.chunk_start[c];
+        len = p.chunk_len[c];
+        h = hv / p.group;
+        live = t < len;
+        const int64_t tok = start + (live ? t : 0);
+        kp = p.k + tok * p.sk_t + static_cast<int64_t>(h) * p.sk_h;
+        qp = p.q + tok * p.sq_t + static_cast<int64_t>(h) * p.sq_h;
+        bp = p.beta + tok * p.sb_t + static_cast<int64_t>(hv) * p.sb_h;
+        vp = p.v + tok * p.sv_t + static_cast<int64_t>(hv) * p.sv_h;
+        wp = p.w + tok * p.sw_t + static_cast<int64_t>(hv) * p.sw_h;
+        const float *gp = p.g + tok * p.sg_t + static_cast<int64_t>(hv) * p.sg_h;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int cb = 8 * (seg + 4 * j);
+            graw[2 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            graw[2 * j + 1] = graw[2 * j];
+            if (live && p.has_g) {
+                graw[2 * j] = __ldg(reinterpret_cast<const float4 *>(gp + cb));
+                graw[2 * j + 1] = __ldg(reinterpret_cast<const float4 *>(gp + cb + 4));
+            }
+        }
+    };
+    if (static_cast<int>(blockIdx.x) < total) fetch(blockIdx.x);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_slot;
+
+#pragma unroll 1
+    for (int it = blockIdx.x; it < total; it += gridDim.x) {
+    uint8_t *rec = p.rec + (static_cast<size_t>(c) * p.HV + hv) * Rec<D>::bytes;
+
+    // ---- 1. cumsum (g was loaded by fetch) -----------------------------------------
+    nk = nq = nb = nv = nw = z4;
+    if (live) {  // first operand chunk; later chunks are fetched one ahead
         const int cb = 8 * seg;
         nk = ldg16(kp + cb);
         nq = ldg16(qp + cb);
@@ -325,7 +343,6 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tm = tmem_slot;
 
     // ---- 3. A and P on the tensor cores (bf16) --------------------------------
     if (tid == 0) {  // one N = 160 chain: columns 16 I (I + 1) / 2 .. hold R_I
@@ -388,6 +405,10 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
                 *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, chunk)) = make_uint4(0, 0, 0, 0);
         }
     }
+    // the operand registers are free: start the next item's loads (the last
+    // item re-reads its own inputs, so the prefetch registers are always
+    // redefined here and are dead in the first half of the loop body)
+    fetch(it + static_cast<int>(gridDim.x) < total ? it + static_cast<int>(gridDim.x) : it);
     tc_fence_before();
     __syncthreads();
 
@@ -484,28 +505,28 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         const bool is_u = warp >= 4;
         const uint32_t cbase = is_u ? D : 0;
 #pragma unroll 1
-        for (int j2 = 0; j2 < D / 32; j2 += 2) {  // two 32-column groups per TMEM round trip
-            uint32_t v[2][32];
-            tmem_ld32(tm + (static_cast<uint32_t>(32 * q) << 16) + cbase + 32 * j2, v[0]);
-            tmem_ld32(tm + (static_cast<uint32_t>(32 * q) << 16) + cbase + 32 * (j2 + 1), v[1]);
+        for (int j = 0; j < D / 32; ++j) {
+            uint32_t v[32];
+            tmem_ld32(tm + (static_cast<uint32_t>(32 * q) << 16) + cbase + 32 * j, v);
             tmem_ld_wait();
+            const int n0 = 32 * j, kb = n0 / 64, c0 = (n0 % 64) / 8;
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int n0 = 32 * (j2 + h2), kb = n0 / 64, c0 = (n0 % 64) / 8;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const uint32_t *w = v[h2] + 8 * cc;
-                    const uint4 o = make_uint4(pack_h2(__uint_as_float(w[0]), __uint_as_float(w[1])),
-                                               pack_h2(__uint_as_float(w[2]), __uint_as_float(w[3])),
-                                               pack_h2(__uint_as_float(w[4]), __uint_as_float(w[5])),
-                                               pack_h2(__uint_as_float(w[6]), __uint_as_float(w[7])));
-                    uint8_t *dst = is_u ? rec + Rec<D>::Ut + kb * 8192 + swz(tt, c0 + cc)
-                                        : rec + Rec<D>::A1 + kb * 16384 + swz(64 + tt, c0 + cc);
-                    *reinterpret_cast<uint4 *>(dst) = o;
-                }
+            for (int cc = 0; cc < 4; ++cc) {
+                const uint32_t *w = v + 8 * cc;
+                const uint4 o = make_uint4(pack_h2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                           pack_h2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                           pack_h2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                                           pack_h2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+                uint8_t *dst = is_u ? rec + Rec<D>::Ut + kb * 8192 + swz(tt, c0 + cc)
+                                    : rec + Rec<D>::A1 + kb * 16384 + swz(64 + tt, c0 + cc);
+                *reinterpret_cast<uint4 *>(dst) = o;
             }
         }
     }
+    tc_fence_before();
+    __syncthreads();  // the item's shared memory and TMEM are free for the next one
+    tc_fence_after();
+    }  // items
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -521,7 +542,13 @@ cudaError_t launch_intra(const Params &p, cudaStream_t s) {
     auto kern = gdn2_tc_intra_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    if (p.NCmax > 0) kern<<<dim3(p.NCmax, p.HV), kIntraThreads, C::kSmem, s>>>(p);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaGetLastError();
+    const long long items = static_cast<long long>(p.NCmax) * p.HV;  // upper bound; the kernel reads NC
+    const int grid = static_cast<int>(items < 2ll * sms ? items : 2ll * sms);
+    if (grid > 0) kern<<<grid, kIntraThreads, C::kSmem, s>>>(p);
     return cudaGetLastError();
 }
 
