@@ -101,6 +101,7 @@ const char *gdn2_status_string(int status) {
         case GDN2_ERR_CUDA: return "CUDA runtime error";
         case GDN2_ERR_IMPL: return "unknown implementation selector";
         case GDN2_ERR_TIMEOUT: return "a tensor-core kernel timed out waiting on its own pipeline (outputs invalid)";
+        case GDN2_ERR_NOALLOC_LIMIT: return "problem needs more scratch than the allocation-free entry point holds (GDN2_NOALLOC_SCRATCH_BYTES)";
         default: return "unknown status";
     }
 }

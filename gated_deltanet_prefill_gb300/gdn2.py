@@ -19,13 +19,15 @@ from . import build as _build
 GDN2_OK = 0
 STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_STRIDE", 4: "ERR_ALIAS",
                 5: "ERR_WORKSPACE", 6: "ERR_ARCH", 7: "ERR_LAUNCH", 8: "ERR_DTYPE",
-                9: "ERR_CU_SEQLENS", 10: "ERR_CUDA", 11: "ERR_IMPL", 12: "ERR_TIMEOUT"}
+                9: "ERR_CU_SEQLENS", 10: "ERR_CUDA", 11: "ERR_IMPL", 12: "ERR_TIMEOUT",
+                13: "ERR_NOALLOC_LIMIT"}
+NOALLOC_SCRATCH_BYTES = 64 << 20
 IMPL = {"tc": 0, "simt": 1}
 DTYPE_BF16, DTYPE_F32 = 0, 2
 
 EXPORTS = ("gdn2_workspace_bytes", "gdn2_dims_init", "gdn2_check_args", "gdn2_chunk_fwd",
            "gdn2_chunk_fwd_staged", "gdn2_num_stages", "gdn2_stage_name", "gdn2_launch_count",
-           "gdn2_device_status", "gdn2_status_string", "gdn2_version")
+           "gdn2_device_status", "gdn2_chunk_fwd_noalloc", "gdn2_status_string", "gdn2_version")
 
 
 class Gdn2Error(RuntimeError):
@@ -83,6 +85,9 @@ def load(path: Optional[str] = None):
     lib.gdn2_stage_name.restype = ctypes.c_char_p
     lib.gdn2_launch_count.argtypes = [ctypes.POINTER(Dims)]
     lib.gdn2_launch_count.restype = i32
+    lib.gdn2_chunk_fwd_noalloc.argtypes = [vp] * 6 + [ctypes.c_float, vp, vp, vp, vp,
+                                                      ctypes.POINTER(Dims), vp]
+    lib.gdn2_chunk_fwd_noalloc.restype = ctypes.c_int
     lib.gdn2_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.gdn2_device_status.restype = ctypes.c_int
     lib.gdn2_status_string.argtypes = [ctypes.c_int]
@@ -178,6 +183,33 @@ def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state
         st = lib.gdn2_chunk_fwd_staged(*args, arr, len(stage_events))
     if st != GDN2_OK:
         raise Gdn2Error(st, "gdn2_chunk_fwd")
+    return out, final_state
+
+
+def chunk_gdn2_fwd_noalloc(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=None,
+                           cu_seqlens=None, output_final_state=True, use_qk_l2norm=False, out=None,
+                           final_state=None, impl="tc", stream=None):
+    """The forward through ``gdn2_chunk_fwd_noalloc``: no workspace argument;
+    the library's fixed device scratch (NOALLOC_SCRATCH_BYTES) is used, so
+    calls must not overlap on the GPU.  Outputs are allocated here only when
+    the caller does not pass them."""
+    lib = load()
+    T, H, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((T, HV, V), dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, HV, K, V), dtype=torch.float32, device=q.device)
+    dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, impl)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    st = lib.gdn2_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(w),
+                                    ctypes.c_float(0.0 if scale is None else float(scale)),
+                                    _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                    ctypes.byref(dims), stream)
+    if st != GDN2_OK:
+        raise Gdn2Error(st, "gdn2_chunk_fwd_noalloc")
     return out, final_state
 
 

@@ -59,8 +59,10 @@ typedef enum gdn2_status {
                               /* cu_seqlens[N] != T_tot (see gdn2_device_status)      */
     GDN2_ERR_CUDA = 10,       /* another CUDA runtime error                           */
     GDN2_ERR_IMPL = 11,       /* unknown implementation selector                      */
-    GDN2_ERR_TIMEOUT = 12     /* device-side: a kernel gave up waiting on one of its  */
+    GDN2_ERR_TIMEOUT = 12,    /* device-side: a kernel gave up waiting on one of its  */
                               /* own pipeline barriers (see gdn2_device_status)       */
+    GDN2_ERR_NOALLOC_LIMIT = 13 /* the problem needs more scratch than                */
+                              /* gdn2_chunk_fwd_noalloc holds                         */
 } gdn2_status;
 
 typedef enum gdn2_dtype {
@@ -200,6 +202,45 @@ GDN2_API int32_t gdn2_launch_count(const gdn2_dims *dims);
  * Returns GDN2_ERR_CUDA if the copy fails.
  */
 GDN2_API gdn2_status gdn2_device_status(const void *workspace, void *stream, int32_t *status);
+
+/*
+ * Size of the device scratch array behind gdn2_chunk_fwd_noalloc: 64 MiB,
+ * enough for any problem with gdn2_workspace_bytes(dims) <= this value (for
+ * example T_tot = 2048 tokens on 16 value heads of size 128, or the 256-token,
+ * 2-head, size-64 case with room to spare).
+ */
+#define GDN2_NOALLOC_SCRATCH_BYTES 67108864u
+
+/*
+ * gdn2_chunk_fwd without a workspace argument, for callers that cannot
+ * allocate device memory: code that runs where allocation is not allowed or
+ * not available (a framework hook or plugin with no access to an allocator,
+ * a runtime that forbids cudaMalloc after start-up) but still passes its own
+ * inputs and outputs.  The paper has no counterpart; this is a packaging of
+ * the same computation.
+ *
+ * The workspace is a fixed array of GDN2_NOALLOC_SCRATCH_BYTES inside this
+ * library (a __device__ variable, so every GPU that loads the library holds
+ * it until the process exits).  This call allocates nothing and calls no
+ * allocating routine.  Its first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  Later calls reuse the address.
+ *
+ * All calls share the one array and it keeps the last call's contents; every
+ * call rewrites what it reads (the status words, chunk map and chunk records
+ * are written before use), so nothing needs clearing between calls.  Calls
+ * that overlap on the GPU (different streams, or different host threads
+ * without ordering) race on the array and must not be issued.
+ *
+ * Arguments and results are those of gdn2_chunk_fwd.  Returns
+ * GDN2_ERR_NOALLOC_LIMIT, before touching the device, when
+ * gdn2_workspace_bytes(dims) exceeds GDN2_NOALLOC_SCRATCH_BYTES;
+ * GDN2_ERR_CUDA if the device address cannot be looked up.
+ */
+GDN2_API gdn2_status gdn2_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *g,
+                                            const void *beta, const void *w, float scale,
+                                            const float *initial_state, const void *cu_seqlens, void *out,
+                                            float *final_state, const gdn2_dims *dims, void *stream);
 
 /* Static, human-readable text for a status code.  Host-only. */
 GDN2_API const char *gdn2_status_string(int status);
