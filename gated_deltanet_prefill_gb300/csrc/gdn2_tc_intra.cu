@@ -19,7 +19,9 @@
 //     N = 160 product, where R_I = k eR m_{I,.} holds the 16(I+1) tokens of row
 //     blocks <= I; the rows of block I against R_I give A (strictly lower) and
 //     P (lower incl. diagonal).
-//  4. T = (I + A)^{-1} by blocked forward substitution in fp32.
+//  4. T = (I + A)^{-1} in fp32: 16 x 16 diagonal inverses by forward
+//     substitution, 16 -> 32 merges, one 32 -> 64 merge (block inverse of a
+//     lower triangular matrix, [[Ta, 0], [Aba, Tb]]^{-1} -> -Tb Aba Ta).
 //  5. tcgen05 (fp16): [Wt | Ut] = T x [beta k e^G | w v]  (M=128, N=2D, K=64).
 //  6. write Qe, Kd^T, P, Wt, Ut (fp16) and eGL (fp32) as shared-memory images.
 //
@@ -49,11 +51,11 @@ struct IntraCfg {
     static constexpr uint32_t kRrows = 160;
     __host__ __device__ static constexpr uint32_t row_R(int I) { return 16u * (I * (I + 1) / 2); }
     static constexpr uint32_t kOperands = kAL + (D / 64) * 128u * kRrows;
-    static constexpr uint32_t kX = kOperands > 46080u ? kOperands : 46080u;
+    static constexpr uint32_t kX = kOperands > 47104u ? kOperands : 47104u;
     // reused after the A/P MMA: fp32 solver matrices and the fp16 T image
     static constexpr uint32_t oAf = 0;                         // [64][kLD]
     static constexpr uint32_t oTf = 64 * kLD * 4;              // [64][kLD]
-    static constexpr uint32_t oY = 2 * 64 * kLD * 4;           // 3 x [16][16]
+    static constexpr uint32_t oY = 2 * 64 * kLD * 4;           // merge scratch, [32][32]
     static constexpr uint32_t oTimg = kX - 8192;               // [64 t][64 s] K-major fp16
     // [beta k e^G | w v] fp16 MN-major B (N = 2D, K = 64); G scratch before
     static constexpr uint32_t oBWU = kX;
@@ -66,7 +68,7 @@ struct IntraCfg {
     static constexpr uint32_t oBar = oTab + kTab;               // mbarrier + TMEM slot
     static constexpr uint32_t kSmem = oBar + 16 + 1024;         // + alignment slack
     static constexpr uint32_t kTmemCols = 256;
-    static_assert(oTimg >= oY + 3 * 1024, "solver buffers overlap the T image");
+    static_assert(oTimg >= oY + 4096, "solver buffers overlap the T image");
     static_assert(kBWU >= 64 * D * 4, "G scratch must fit in the B operand area");
     static_assert(kTab >= (kIntraThreads / D) * D * 4, "scan totals must fit in the table area");
     // two CTAs per SM: 2 x (dynamic + 1 KB reserved) <= 228 KB
@@ -382,9 +384,13 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
                 const int s0 = static_cast<int>(cg - mycol0);
                 if (r < 64) {
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const int s = s0 + x;
-                        Af[tt * kLD + s] = s < tt ? __uint_as_float(v[x]) : 0.f;
+                    for (int x4 = 0; x4 < 4; ++x4) {
+                        float4 f;
+                        f.x = s0 + 4 * x4 + 0 < tt ? __uint_as_float(v[4 * x4 + 0]) : 0.f;
+                        f.y = s0 + 4 * x4 + 1 < tt ? __uint_as_float(v[4 * x4 + 1]) : 0.f;
+                        f.z = s0 + 4 * x4 + 2 < tt ? __uint_as_float(v[4 * x4 + 2]) : 0.f;
+                        f.w = s0 + 4 * x4 + 3 < tt ? __uint_as_float(v[4 * x4 + 3]) : 0.f;
+                        *reinterpret_cast<float4 *>(Af + tt * kLD + s0 + 4 * x4) = f;
                     }
                 } else {
 #pragma unroll
@@ -429,47 +435,60 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         for (int i = 0; i < 16; ++i) Tf[(o + i) * kLD + o + j] = x[i];
     }
     __syncthreads();
-    // off-diagonal blocks (I, J) = (J + d, J), level d = 1..3: warp J computes
-    // one block, a 2 x 4 register tile per lane
-#pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
-        const int J = warp, Ib = J + d;
-        const int i0 = 2 * (lane / 4), j0 = 4 * (lane % 4);
-        if (Ib < 4) {
-            float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            const float *a0 = Af + (16 * Ib + i0) * kLD;
-            const float *a1 = a0 + kLD;
-#pragma unroll 4
-            for (int m = 16 * J; m < 16 * Ib; ++m) {
-                const float4 tv = *reinterpret_cast<const float4 *>(Tf + m * kLD + 16 * J + j0);
-                const float x0 = a0[m], x1 = a1[m];
-                y[0][0] += x0 * tv.x; y[0][1] += x0 * tv.y; y[0][2] += x0 * tv.z; y[0][3] += x0 * tv.w;
-                y[1][0] += x1 * tv.x; y[1][1] += x1 * tv.y; y[1][2] += x1 * tv.z; y[1][3] += x1 * tv.w;
-            }
+    // 16 -> 32 merges: T_{I+1,I} = -T_{I+1,I+1} (A_{I+1,I} T_{I,I}), I = 0 and 2,
+    // a 1 x 2 tile per thread
+    {
+        const int b = tid / 128, e = tid % 128, Ib = 2 * b;
+        const int i = e / 8, j0 = 2 * (e % 8);
+        const int r0 = 16 * (Ib + 1), c0 = 16 * Ib;
+        float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-            for (int a = 0; a < 2; ++a)
-                *reinterpret_cast<float4 *>(Yb + J * 256 + (i0 + a) * 16 + j0) =
-                    make_float4(y[a][0], y[a][1], y[a][2], y[a][3]);
+        for (int m = 0; m < 16; ++m) {
+            const float a = Af[(r0 + i) * kLD + c0 + m];
+            const float2 tv = *reinterpret_cast<const float2 *>(Tf + (c0 + m) * kLD + c0 + j0);
+            y0 += a * tv.x;
+            y1 += a * tv.y;
         }
+        *reinterpret_cast<float2 *>(Yb + b * 256 + i * 16 + j0) = make_float2(y0, y1);
         __syncthreads();
-        if (Ib < 4) {
-            float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            const float *t0 = Tf + (16 * Ib + i0) * kLD + 16 * Ib;
-            const float *t1 = t0 + kLD;
+        float z0 = 0.f, z1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const float4 yv = *reinterpret_cast<const float4 *>(Yb + J * 256 + m * 16 + j0);
-                const float x0 = t0[m], x1 = t1[m];
-                y[0][0] -= x0 * yv.x; y[0][1] -= x0 * yv.y; y[0][2] -= x0 * yv.z; y[0][3] -= x0 * yv.w;
-                y[1][0] -= x1 * yv.x; y[1][1] -= x1 * yv.y; y[1][2] -= x1 * yv.z; y[1][3] -= x1 * yv.w;
-            }
-#pragma unroll
-            for (int a = 0; a < 2; ++a)
-                *reinterpret_cast<float4 *>(Tf + (16 * Ib + i0 + a) * kLD + 16 * J + j0) =
-                    make_float4(y[a][0], y[a][1], y[a][2], y[a][3]);
+        for (int m = 0; m < 16; ++m) {
+            const float tv = Tf[(r0 + i) * kLD + r0 + m];
+            const float2 yv = *reinterpret_cast<const float2 *>(Yb + b * 256 + m * 16 + j0);
+            z0 -= tv * yv.x;
+            z1 -= tv * yv.y;
         }
-        __syncthreads();
+        *reinterpret_cast<float2 *>(Tf + (r0 + i) * kLD + c0 + j0) = make_float2(z0, z1);
     }
+    __syncthreads();
+    // 32 -> 64 merge on the 32 x 32 halves a (rows/cols 0-31) and b (32-63):
+    // X = A_ba T_a, then T_ba = -T_b X; a 2 x 2 tile per thread.  T_a and T_b
+    // are block lower triangular, so the sums skip their zero upper blocks.
+    {
+        const int i0 = 2 * (tid / 16), j0 = 2 * (tid % 16);
+        float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
+#pragma unroll 4
+        for (int m = j0 & ~15; m < 32; ++m) {
+            const float a0 = Af[(32 + i0) * kLD + m], a1 = Af[(33 + i0) * kLD + m];
+            const float2 tv = *reinterpret_cast<const float2 *>(Tf + m * kLD + j0);
+            x00 += a0 * tv.x; x01 += a0 * tv.y; x10 += a1 * tv.x; x11 += a1 * tv.y;
+        }
+        *reinterpret_cast<float2 *>(Yb + i0 * 32 + j0) = make_float2(x00, x01);
+        *reinterpret_cast<float2 *>(Yb + (i0 + 1) * 32 + j0) = make_float2(x10, x11);
+        __syncthreads();
+        float z00 = 0.f, z01 = 0.f, z10 = 0.f, z11 = 0.f;
+        const int mend = (i0 & ~15) + 16;
+#pragma unroll 4
+        for (int m = 0; m < mend; ++m) {
+            const float t0 = Tf[(32 + i0) * kLD + 32 + m], t1 = Tf[(33 + i0) * kLD + 32 + m];
+            const float2 xv = *reinterpret_cast<const float2 *>(Yb + m * 32 + j0);
+            z00 -= t0 * xv.x; z01 -= t0 * xv.y; z10 -= t1 * xv.x; z11 -= t1 * xv.y;
+        }
+        *reinterpret_cast<float2 *>(Tf + (32 + i0) * kLD + j0) = make_float2(z00, z01);
+        *reinterpret_cast<float2 *>(Tf + (33 + i0) * kLD + j0) = make_float2(z10, z11);
+    }
+    __syncthreads();
     // T -> fp16 K-major image [64 t][64 s]; zeros above the diagonal
     for (int e = tid; e < 64 * 8; e += kIntraThreads) {
         const int tt = e / 8, chunk = e % 8;
