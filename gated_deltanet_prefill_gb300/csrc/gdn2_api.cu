@@ -227,7 +227,16 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     p.hbuf = reinterpret_cast<bf16 *>(ws + L.hbuf);
     p.vnew = reinterpret_cast<bf16 *>(ws + L.vnew);
     p.rec = reinterpret_cast<uint8_t *>(ws + L.rec);
+    // State-kernel V tile: V columns of S evolve independently, so splitting V
+    // is exact.  Two 64-column tiles per (sequence, head) when the untiled
+    // grid would leave more than half of the SMs idle.
     p.vtile = d->K;
+    if (d->K == 128) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            2ll * d->N * d->HV <= sms)
+            p.vtile = 64;
+    }
     p.q_in = p.q; p.k_in = p.k;
     p.sq_in_t = p.sq_t; p.sq_in_h = p.sq_h; p.sk_in_t = p.sk_t; p.sk_in_h = p.sk_h;
     if (p.l2norm && d->impl == GDN2_IMPL_SIMT) {  // SIMT kernels read the normalised packed copies

@@ -85,6 +85,16 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Per-thread 16-byte global -> shared copy (L2 only); src_bytes = 0 writes
+// zeros without reading src.  Completion: cp_async_wait_all by the issuing
+// thread, then a block barrier before other threads read the data.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Make generic-proxy shared-memory writes visible to the async proxy
 // (tcgen05.mma operand reads, bulk copies).
 __device__ __forceinline__ void fence_proxy_async() {
@@ -224,8 +234,9 @@ __device__ __forceinline__ float ex2(float x) {
 // ----------------------------------------------------------- conversions
 // fp16 intermediates saturate at +-65504 instead of overflowing to inf.
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
-    const __half2 v = __floats2half2_rn(fminf(fmaxf(a, -65504.f), 65504.f), fminf(fmaxf(b, -65504.f), 65504.f));
-    return *reinterpret_cast<const uint32_t *>(&v);
+    uint32_t r;  // a -> low half; out-of-range finite values saturate to +-65504
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
 }
 __device__ __forceinline__ float2 unpack_h2(uint32_t x) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&x));

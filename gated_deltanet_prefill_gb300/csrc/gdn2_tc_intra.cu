@@ -52,12 +52,18 @@ struct IntraCfg {
     __host__ __device__ static constexpr uint32_t row_R(int I) { return 16u * (I * (I + 1) / 2); }
     static constexpr uint32_t kOperands = kAL + (D / 64) * 128u * kRrows;
     static constexpr uint32_t kX = kOperands > 47104u ? kOperands : 47104u;
+    // before the operand images: the G scratch [64][D] fp32 (plain rows), which
+    // receives the item's g (bulk copies) while the previous item is in its
+    // W/U product
+    static constexpr uint32_t oG = 0;
     // reused after the A/P MMA: fp32 solver matrices and the fp16 T image
     static constexpr uint32_t oAf = 0;                         // [64][kLD]
     static constexpr uint32_t oTf = 64 * kLD * 4;              // [64][kLD]
     static constexpr uint32_t oY = 2 * 64 * kLD * 4;           // merge scratch, [32][32]
     static constexpr uint32_t oTimg = kX - 8192;               // [64 t][64 s] K-major fp16
-    // [beta k e^G | w v] fp16 MN-major B (N = 2D, K = 64); G scratch before
+    // [beta k e^G | w v] fp16 MN-major B (N = 2D, K = 64).  Before the item's
+    // operand images it holds the item's raw v and w rows (bf16, [64][D] each),
+    // copied in while the previous item is in its W/U epilogue.
     static constexpr uint32_t oBWU = kX;
     static constexpr uint32_t kBWU = (2 * D / 64) * 8192;
     // per-channel tables (log2-scaled G): gE[4][D] = G'_{E_J}, tGB[4][D] =
@@ -65,23 +71,19 @@ struct IntraCfg {
     // G_{E_I}}; the scan totals use the same area before the tables exist
     static constexpr uint32_t oTab = oBWU + kBWU;
     static constexpr uint32_t kTab = 14 * D * 4;
-    static constexpr uint32_t oBar = oTab + kTab;               // mbarrier + TMEM slot
-    static constexpr uint32_t kSmem = oBar + 16 + 1024;         // + alignment slack
+    // mbarriers (MMA, g copies, v/w copies) and the TMEM slot
+    static constexpr uint32_t oBar = oTab + kTab;
+    static constexpr uint32_t kSmem = oBar + 32 + 1024;         // + alignment slack
     static constexpr uint32_t kTmemCols = 256;
     static_assert(oTimg >= oY + 4096, "solver buffers overlap the T image");
-    static_assert(kBWU >= 64 * D * 4, "G scratch must fit in the B operand area");
+    static_assert(oG + 64 * D * 4 <= oTimg, "G scratch must not overlap the T image");
+    static_assert(kBWU >= 2 * 64 * D * 2, "raw v and w must fit in the B operand area");
     static_assert(kTab >= (kIntraThreads / D) * D * 4, "scan totals must fit in the table area");
     // two CTAs per SM: 2 x (dynamic + 1 KB reserved) <= 228 KB
     static_assert(2 * (kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
 __device__ __forceinline__ uint4 ldg16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
-
-// G scratch [64][D] fp32 with float4 chunks XOR-swizzled by (t & 7)
-template <int D>
-__device__ __forceinline__ int gidx(int t, int c) {
-    return t * D + ((((c >> 2) ^ (t & 7))) << 2) + (c & 3);
-}
 
 template <int D>
 __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params p) {
@@ -93,6 +95,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t &bar_mma = *reinterpret_cast<uint64_t *>(sm + C::oBar);
     uint32_t &tmem_slot = *reinterpret_cast<uint32_t *>(sm + C::oBar + 8);
+    uint64_t &bar_g = *reinterpret_cast<uint64_t *>(sm + C::oBar + 16);
+    uint64_t &bar_vw = *reinterpret_cast<uint64_t *>(sm + C::oBar + 24);
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int t = tid / 4, seg = tid % 4;
@@ -101,6 +105,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
 
     if (tid == 0) {
         mbar_init(&bar_mma, 1);
+        mbar_init(&bar_g, 1);
+        mbar_init(&bar_vw, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -108,41 +114,64 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         tmem_relinquish();
     }
 
-    // Per-item inputs.  The CTA walks items it = blockIdx.x, + gridDim.x, ...;
-    // the next item's g is loaded while the current item is in its solve and
-    // epilogues; its first operand chunk is loaded at the start of its cumsum.
+    // Per-item inputs.  The CTA walks items it = blockIdx.x, + gridDim.x, ...
+    // The next item's chunk metadata is loaded after the A/P epilogue.  Its g
+    // rows are bulk-copied into the G scratch once the T image is written
+    // (warp 7), its v and w rows into the B operand area once the W/U product
+    // has read it (warp 2); both land during the W/U product and epilogue.
+    // k, q and beta are read by every thread during the operand images.
     int c = 0, hv = 0, len = 1, h = 0;
+    int nc = 0, nhv = 0, nlen = 1;
+    int64_t nstart = 0;
     bool live = false;
-    const bf16 *kp = nullptr, *qp = nullptr, *bp = nullptr, *vp = nullptr, *wp = nullptr;
+    const bf16 *kp = nullptr, *qp = nullptr, *bp = nullptr;
     const uint4 z4 = make_uint4(0, 0, 0, 0);
-    float4 graw[2 * NJ];
-    uint4 nk = z4, nq = z4, nb = z4, nv = z4, nw = z4;
-    auto fetch = [&](int it) {
-        c = it / p.HV;
-        hv = it - c * p.HV;
-        const int64_t start = p.chunk_start[c];
-        len = p.chunk_len[c];
+    uint4 nk = z4, nq = z4, nb = z4;
+    auto meta = [&](int it) {
+        nc = it / p.HV;
+        nhv = it - nc * p.HV;
+        nstart = p.chunk_start[nc];
+        nlen = p.chunk_len[nc];
+    };
+    float *Gs = reinterpret_cast<float *>(sm + C::oG);
+    uint8_t *raw_v = sm + C::oBWU;
+    uint8_t *raw_w = sm + C::oBWU + 64 * D * 2;
+    auto stage_g = [&]() {  // warp 7
+        const uint32_t rows = p.has_g ? static_cast<uint32_t>(nlen) : 0u;
+        if (lane == 0) mbar_arrive_expect_tx(&bar_g, rows * D * 4);
+        __syncwarp();
+        for (uint32_t r = lane; r < rows; r += 32)
+            bulk_g2s(Gs + r * D, p.g + (nstart + r) * p.sg_t + static_cast<int64_t>(nhv) * p.sg_h, D * 4, &bar_g);
+    };
+    auto stage_vw = [&]() {  // warp 2
+        const uint32_t rows = static_cast<uint32_t>(nlen);
+        if (lane == 0) mbar_arrive_expect_tx(&bar_vw, rows * D * 2 * (p.has_w ? 2u : 1u));
+        __syncwarp();
+        for (uint32_t r = lane; r < rows; r += 32) {
+            const int64_t tok = nstart + r;
+            bulk_g2s(raw_v + r * D * 2, p.v + tok * p.sv_t + static_cast<int64_t>(nhv) * p.sv_h, D * 2, &bar_vw);
+            if (p.has_w)
+                bulk_g2s(raw_w + r * D * 2, p.w + tok * p.sw_t + static_cast<int64_t>(nhv) * p.sw_h, D * 2, &bar_vw);
+        }
+    };
+    auto adopt = [&]() {  // the staged item becomes the current one
+        c = nc;
+        hv = nhv;
+        len = nlen;
         h = hv / p.group;
         live = t < len;
-        const int64_t tok = start + (live ? t : 0);
+        const int64_t tok = nstart + (live ? t : 0);
         kp = p.k + tok * p.sk_t + static_cast<int64_t>(h) * p.sk_h;
         qp = p.q + tok * p.sq_t + static_cast<int64_t>(h) * p.sq_h;
         bp = p.beta + tok * p.sb_t + static_cast<int64_t>(hv) * p.sb_h;
-        vp = p.v + tok * p.sv_t + static_cast<int64_t>(hv) * p.sv_h;
-        wp = p.w + tok * p.sw_t + static_cast<int64_t>(hv) * p.sw_h;
-        const float *gp = p.g + tok * p.sg_t + static_cast<int64_t>(hv) * p.sg_h;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            const int cb = 8 * (seg + 4 * j);
-            graw[2 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            graw[2 * j + 1] = graw[2 * j];
-            if (live && p.has_g) {
-                graw[2 * j] = __ldg(reinterpret_cast<const float4 *>(gp + cb));
-                graw[2 * j + 1] = __ldg(reinterpret_cast<const float4 *>(gp + cb + 4));
-            }
-        }
     };
-    if (static_cast<int>(blockIdx.x) < total) fetch(blockIdx.x);
+    if (static_cast<int>(blockIdx.x) < total) meta(blockIdx.x);
+    __syncthreads();  // barriers initialised
+    if (static_cast<int>(blockIdx.x) < total) {
+        if (warp == 7) stage_g();
+        if (warp == 2) stage_vw();
+    }
+    uint32_t phase = 0;  // parity of the staging barriers for the current item
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -150,17 +179,20 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
 
 #pragma unroll 1
     for (int it = blockIdx.x; it < total; it += gridDim.x) {
+    adopt();
     uint8_t *rec = p.rec + (static_cast<size_t>(c) * p.HV + hv) * Rec<D>::bytes;
 
-    // ---- 1. cumsum (g was loaded by fetch) -----------------------------------------
-    nk = nq = nb = nv = nw = z4;
-    if (live) {  // first operand chunk; later chunks are fetched one ahead
+    // ---- 1. cumsum (g is in the G scratch) ----------------------------------------
+    nk = nq = nb = z4;
+    uint4 mk = z4, mq = z4, mb = z4;
+    if (live) {  // first two operand chunks; later chunks are fetched two ahead
         const int cb = 8 * seg;
         nk = ldg16(kp + cb);
         nq = ldg16(qp + cb);
-        nv = ldg16(vp + cb);
         if (p.has_beta) nb = ldg16(bp + cb);
-        if (p.has_w) nw = ldg16(wp + cb);
+        mk = ldg16(kp + cb + 32);
+        mq = ldg16(qp + cb + 32);
+        if (p.has_beta) mb = ldg16(bp + cb + 32);
     }
     float kscale = 1.f, qscale = 1.f;
     if (p.l2norm) {
@@ -186,35 +218,37 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         qscale = 1.f / fmaxf(sqrtf(sq), 1e-12f);
     }
     // G' = G log2(e): every decay factor below is an exact power of two of a
-    // difference of G' values
+    // difference of G' values.  g is in the G scratch (rows < len; the rest
+    // read as 0), raw v and w in the B operand area.
     constexpr float kLog2e = 1.4426950408889634f;
-    float *Gs = reinterpret_cast<float *>(sm + C::oBWU);
+    if (!mbar_wait(&bar_g, phase)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
+    if (!mbar_wait(&bar_vw, phase)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
+    phase ^= 1u;
+    // this thread's v and w chunks; w v goes to its operand image after the
+    // scan's barriers (it overwrites the raw rows)
+    uint4 rv[NJ], rw[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-        const int cb = 8 * (seg + 4 * j);
-        float4 a = graw[2 * j], b = graw[2 * j + 1];
-        a.x *= kLog2e; a.y *= kLog2e; a.z *= kLog2e; a.w *= kLog2e;
-        b.x *= kLog2e; b.y *= kLog2e; b.z *= kLog2e; b.w *= kLog2e;
-        *reinterpret_cast<float4 *>(Gs + gidx<D>(t, cb)) = a;
-        *reinterpret_cast<float4 *>(Gs + gidx<D>(t, cb + 4)) = b;
+        rv[j] = rw[j] = z4;
+        if (live) {
+            rv[j] = *reinterpret_cast<const uint4 *>(raw_v + (t * D + 8 * (seg + 4 * j)) * 2);
+            if (p.has_w) rw[j] = *reinterpret_cast<const uint4 *>(raw_w + (t * D + 8 * (seg + 4 * j)) * 2);
+        }
     }
-    __syncthreads();
+    const int glen = p.has_g ? len : 0;
     float *tot = reinterpret_cast<float *>(sm + C::oTab);  // [PARTS][D], before the tables
     {
-        // rows come in groups of 8, so the (t & 7) swizzle of each row in a
-        // group is a compile-time constant
         const int ch = tid % D, part = tid / D;
-        const int c4 = ch >> 2, c3 = ch & 3;
-        float *base = Gs + part * ROWS * D + c3;
+        float *base = Gs + part * ROWS * D + ch;
         float acc = 0.f;
 #pragma unroll 1
         for (int r8 = 0; r8 < ROWS; r8 += 8) {
             float *b8 = base + r8 * D;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                float *a = b8 + k * D + ((c4 ^ k) << 2);
-                acc += *a;
-                *a = acc;
+                const int row = part * ROWS + r8 + k;
+                acc += row < glen ? __fmul_rn(b8[k * D], kLog2e) : 0.f;
+                b8[k * D] = acc;
             }
         }
         tot[part * D + ch] = acc;
@@ -226,11 +260,21 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
             for (int r8 = 0; r8 < ROWS; r8 += 8) {
                 float *b8 = base + r8 * D;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) b8[k * D + ((c4 ^ k) << 2)] += off;
+                for (int k = 0; k < 8; ++k) b8[k * D] += off;
             }
         }
     }
     __syncthreads();
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        const int cb = 8 * (seg + 4 * j);
+        float vv[8], ww[8], xv[8];
+        unpack8_bf(rv[j], vv);
+        unpack8_bf(rw[j], ww);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) xv[x] = (p.has_w || !live) ? ww[x] * vv[x] : vv[x];
+        *reinterpret_cast<uint4 *>(sm + C::oBWU + ((D + cb) / 64) * 8192 + swz(t, (cb % 64) / 8)) = pack8_h(xv);
+    }
     float *gE = reinterpret_cast<float *>(sm + C::oTab);  // G' at E_J
     float *tGB = gE + 4 * D;                              // e^{G_{B_I}}
     float *tI = tGB + 4 * D;                              // e^{G_{B_I} - G_{E_I}}
@@ -238,7 +282,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     if (tid < D) {
         float e[4];
 #pragma unroll
-        for (int J = 0; J < 4; ++J) e[J] = Gs[gidx<D>(min(16 * J + 15, len - 1), tid)];
+        for (int J = 0; J < 4; ++J) e[J] = Gs[min(16 * J + 15, len - 1) * D + tid];
 #pragma unroll
         for (int J = 0; J < 4; ++J) {
             const float b = J > 0 ? e[J - 1] : 0.f;
@@ -254,8 +298,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         const int cb = 8 * (seg + 4 * j);
-        const float4 a = *reinterpret_cast<const float4 *>(Gs + gidx<D>(t, cb));
-        const float4 b = *reinterpret_cast<const float4 *>(Gs + gidx<D>(t, cb + 4));
+        const float4 a = *reinterpret_cast<const float4 *>(Gs + t * D + cb);
+        const float4 b = *reinterpret_cast<const float4 *>(Gs + t * D + cb + 4);
         Gr[8 * j + 0] = a.x; Gr[8 * j + 1] = a.y; Gr[8 * j + 2] = a.z; Gr[8 * j + 3] = a.w;
         Gr[8 * j + 4] = b.x; Gr[8 * j + 5] = b.y; Gr[8 * j + 6] = b.z; Gr[8 * j + 7] = b.w;
     }
@@ -265,33 +309,28 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         const int cb = 8 * (seg + 4 * j);
-        float kk[8], qq[8], bb[8], vv[8], ww[8];
+        float kk[8], qq[8], bb[8];
         unpack8_bf(nk, kk);
         unpack8_bf(nq, qq);
-        unpack8_bf(nv, vv);
         unpack8_bf(nb, bb);
-        unpack8_bf(nw, ww);
         if (!p.has_beta && live) {
 #pragma unroll
             for (int x = 0; x < 8; ++x) bb[x] = 1.f;
         }
-        if (!p.has_w && live) {
-#pragma unroll
-            for (int x = 0; x < 8; ++x) ww[x] = 1.f;
-        }
-        if (j + 1 < NJ && live) {  // fetch the next chunk while this one is processed
-            const int cn = 8 * (seg + 4 * (j + 1));
-            nk = ldg16(kp + cn);
-            nq = ldg16(qp + cn);
-            nv = ldg16(vp + cn);
-            if (p.has_beta) nb = ldg16(bp + cn);
-            if (p.has_w) nw = ldg16(wp + cn);
+        nk = mk;
+        nq = mq;
+        nb = mb;
+        if (j + 2 < NJ && live) {  // fetch two chunks ahead
+            const int cn = 8 * (seg + 4 * (j + 2));
+            mk = ldg16(kp + cn);
+            mq = ldg16(qp + cn);
+            if (p.has_beta) mb = ldg16(bp + cn);
         }
         // outputs packed two channels per 32-bit word as they are produced
-        uint32_t wLk[4], wLq[4], wkr[4], wX1[4], wX2[4], wQe[4], wKd[4], wr0[4], wr2[4], wr3[4];
+        uint32_t wLk[4], wLq[4], wkr[4], wX1[4], wQe[4], wKd[4], wr0[4], wr2[4], wr3[4];
 #pragma unroll
         for (int x2 = 0; x2 < 4; ++x2) {
-            float lk[2], lq[2], kr[2], x1[2], xv[2], qe[2], kd[2], r0[2], r2[2], r3[2];
+            float lk[2], lq[2], kr[2], x1[2], qe[2], kd[2], r0[2], r2[2], r3[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int x = 2 * x2 + e;
@@ -309,7 +348,6 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
                 x1[e] = lk[e] * eGB;
                 qe[e] = lq[e] * eGB;
                 kd[e] = kx * eL;
-                xv[e] = ww[x] * vv[x];
                 r0[e] = kr[e] * tI[I * D + ci];                       // row of R_I
                 const float f2 = t2[(I & 1) * D + ci];                // e^{G_{E_{I+1}} - G_{E_I}}
                 r2[e] = kr[e] * f2;                                   // row of R_{I+2}, I <= 1
@@ -322,7 +360,6 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
             wr2[x2] = pack_bf2(r2[0], r2[1]);
             wr3[x2] = pack_bf2(r3[0], r3[1]);
             wX1[x2] = pack_h2(x1[0], x1[1]);
-            wX2[x2] = pack_h2(xv[0], xv[1]);
             wQe[x2] = pack_h2(qe[0], qe[1]);
             wKd[x2] = pack_h2(kd[0], kd[1]);
         }
@@ -337,7 +374,6 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         if (I + 2 < 4) *reinterpret_cast<uint4 *>(rt + swz(C::row_R(I + 2) + t, chunk)) = u4(wr2);
         if (I == 0) *reinterpret_cast<uint4 *>(rt + swz(C::row_R(3) + t, chunk)) = u4(wr3);
         *reinterpret_cast<uint4 *>(sm + C::oBWU + (cb / 64) * 8192 + swz(t, chunk)) = u4(wX1);
-        *reinterpret_cast<uint4 *>(sm + C::oBWU + ((D + cb) / 64) * 8192 + swz(t, chunk)) = u4(wX2);
         *reinterpret_cast<uint4 *>(rec + Rec<D>::A1 + kb * 16384 + swz(t, chunk)) = u4(wQe);
         *reinterpret_cast<uint4 *>(rec + Rec<D>::KdT + kb * 8192 + swz(t, chunk)) = u4(wKd);
     }
@@ -375,11 +411,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
         const uint32_t mycol0 = 16u * (Ir * (Ir + 1) / 2);
         const uint32_t mycols = 16u * (Ir + 1);
         __syncwarp();
-#pragma unroll 1
-        for (uint32_t cg = cbeg; cg < cend; cg += 32) {
-            uint32_t v[16];
-            tmem_ld16(tm + (static_cast<uint32_t>(32 * wq) << 16) + cg, v);
-            tmem_ld_wait();
+        auto keep = [&](uint32_t cg, const uint32_t (&v)[16]) {
             if (cg >= mycol0 && cg < mycol0 + mycols) {
                 const int s0 = static_cast<int>(cg - mycol0);
                 if (r < 64) {
@@ -405,16 +437,21 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
                     }
                 }
             }
+        };
+#pragma unroll 1
+        for (uint32_t cg = cbeg; cg < cend; cg += 32) {
+            uint32_t v0[16];
+            tmem_ld16(tm + (static_cast<uint32_t>(32 * wq) << 16) + cg, v0);
+            tmem_ld_wait();
+            keep(cg, v0);
         }
         if (r >= 64 && warp < 4) {  // P columns past this row's block are zero
             for (int chunk = 2 * (Ir + 1); chunk < 8; ++chunk)
                 *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, chunk)) = make_uint4(0, 0, 0, 0);
         }
     }
-    // the operand registers are free: start the next item's loads (the last
-    // item re-reads its own inputs, so the prefetch registers are always
-    // redefined here and are dead in the first half of the loop body)
-    fetch(it + static_cast<int>(gridDim.x) < total ? it + static_cast<int>(gridDim.x) : it);
+    const bool has_next = it + static_cast<int>(gridDim.x) < total;
+    if (has_next) meta(it + static_cast<int>(gridDim.x));
     tc_fence_before();
     __syncthreads();
 
@@ -504,6 +541,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (has_next && warp == 7) stage_g();  // the solver matrices are dead: the G scratch is free
 
     // ---- 5. [Wt | Ut] = T x [X1 | X2] (fp16) -----------------------------------
     if (tid == 0) {
@@ -515,6 +553,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     }
     if (!mbar_wait(&bar_mma, 1)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
     tc_fence_after();
+    if (has_next && warp == 2) stage_vw();  // the W/U product has read the B operand area
 
     // ---- 6. Wt -> A1 rows 64-127, Ut -> Ut image (fp16) -------------------------
     if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {

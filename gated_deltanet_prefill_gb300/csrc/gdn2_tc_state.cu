@@ -13,10 +13,11 @@
 // which is the FlashRT page's WY chain (chunk_h then output_o) fused into one
 // pass, with burn-gdn2's "in-loop output phase".
 //
-// Warp roles (16 warps): 0 bulk-copy producer, 1 MMA issuer (and TMEM owner),
-// 4-11 state epilogue (S -> fp16 operand, S *= eGL; two warps per TMEM lane
-// quarter, each half of the columns), 2-3 and 14-15 U epilogue (the Wt S rows
-// live in lane quarters 2 and 3), 12-13 output epilogue.  Every wait is time-bounded; a timeout sets the device
+// Warp roles (24 warps): 0 bulk-copy producer, 1 MMA issuer (and TMEM owner),
+// 8-23 state epilogue (S -> fp16 operand, S *= eGL; four warps per TMEM lane
+// quarter, one 32-column group each), 2-3 and 6-7 U epilogue (the Wt S rows
+// live in lane quarters 2 and 3; two warps per quarter, half the columns
+// each), 4-5 output epilogue.  Every wait is time-bounded; a timeout sets the device
 // status word and the CTA unwinds.  Operands are fp16 (10-bit mantissa,
 // saturating at +-65504); accumulation and the carried state are fp32.
 #include "gdn2_internal.cuh"
@@ -29,7 +30,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStateThreads = 512;
+constexpr int kStateThreads = 768;
 
 template <int D, int VT, int NSTAGE>
 struct StateCfg {
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
-        mbar_init(&s_ready, 256);
+        mbar_init(&s_ready, 512);
         mbar_init(&u_ready, 128);
         mbar_init(&s_full, 1);
         mbar_init(&drain, 1);
@@ -161,13 +162,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             mma_commit(&drain);
             if (!mbar_wait(&drain, 0)) set_timeout(p);
         }
-    } else if (warp >= 4 && warp < 12) {
+    } else if (warp >= 8) {
         // ------------------------------------- state epilogue (S rows = key channels)
         const int q = warp & 3;
         const int row = 32 * q + lane;
-        const bool active = row < D;
+        const int grp = (warp - 8) >> 2;  // 32-column group of this warp
+        const bool active = row < D && grp < VT / 32;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        const int j0 = warp < 8 ? 0 : VT / 64, j1 = warp < 8 ? VT / 64 : VT / 32;  // 32-column groups
+        const int j0 = grp, j1 = grp + 1;
         if (active) {
             const float *h0 = p.h0 ? p.h0 + ((static_cast<size_t>(n) * p.HV + hv) * D + row) * D + v0 : nullptr;
 #pragma unroll 1
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                                     __uint_as_float(r[e + 3]));
             }
         }
-    } else if (warp == 12 || warp == 13) {
+    } else if (warp == 4 || warp == 5) {
         // ----------------------------------------- output epilogue (tokens 0-63)
         const int q = warp & 3;  // 0 or 1
         const int t = 32 * q + lane;
@@ -276,7 +278,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             tc_fence_before();
             mbar_arrive(&d1_free[b]);
         }
-    } else if (warp == 2 || warp == 3 || warp == 14 || warp == 15) {
+    } else if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
         // ----------------------------------- U epilogue (D1 rows 64-127 = Wt S)
         const int q = warp & 3;  // 2 or 3
         const int t = 32 * (q - 2) + lane;
