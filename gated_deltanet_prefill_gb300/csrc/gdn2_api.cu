@@ -1,6 +1,9 @@
 // C ABI of the GDN-2 chunked prefill forward: argument checks, workspace
 // layout and the launch sequence.  See include/gdn2.h for the contract.
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
 #include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "gdn2_internal.cuh"
@@ -8,6 +11,44 @@
 namespace gdn2 {
 
 namespace {
+
+// cuTensorMapEncodeTiled from the driver (looked up once; nullptr if absent)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+        }
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// Tensor map over a token-major [T, heads, D] tensor (element strides st_t,
+// st_h; channel stride 1) whose box is 64 tokens x D channels of one head,
+// written to shared memory as [64][D].  The two outer dimensions go in
+// increasing stride order (*order = 0: (channel, head, token), 1: (channel,
+// token, head)).  False if the driver rejects the layout.
+bool encode_rows(CUtensorMap *map, int *order, const void *base, CUtensorMapDataType type, int64_t esize,
+                 int64_t D, int64_t heads, int64_t T, int64_t st_t, int64_t st_h) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || !base || T < 1 || T > INT32_MAX || heads < 1) return false;
+    const bool head_inner = st_h < st_t;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(head_inner ? heads : T),
+                                static_cast<cuuint64_t>(head_inner ? T : heads)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>((head_inner ? st_h : st_t) * esize),
+                                   static_cast<cuuint64_t>((head_inner ? st_t : st_h) * esize)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), head_inner ? 1u : 64u, head_inner ? 64u : 1u};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    *order = head_inner ? 0 : 1;
+    return enc(map, type, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -236,6 +277,19 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
             2ll * d->N * d->HV <= sms)
             p.vtile = 64;
+    }
+    // tensor maps for the intra kernel's g / v / w tiles (GDN2_ROW_COPIES=1
+    // forces the row-by-row copies)
+    if (d->impl == GDN2_IMPL_TC) {
+        const char *rows = getenv("GDN2_ROW_COPIES");
+        const bool force_rows = rows && rows[0] == '1';
+        p.tmap = !force_rows &&
+                 (!p.has_g || encode_rows(&p.tm_g, &p.tm_order_g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d->K,
+                                          d->HV, d->T_tot, p.sg_t, p.sg_h)) &&
+                 encode_rows(&p.tm_v, &p.tm_order_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->V, d->HV,
+                             d->T_tot, p.sv_t, p.sv_h) &&
+                 (!p.has_w || encode_rows(&p.tm_w, &p.tm_order_w, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->V,
+                                          d->HV, d->T_tot, p.sw_t, p.sw_h));
     }
     p.q_in = p.q; p.k_in = p.k;
     p.sq_in_t = p.sq_t; p.sq_in_h = p.sq_h; p.sk_in_t = p.sk_t; p.sk_in_h = p.sk_h;

@@ -2,6 +2,7 @@
 // Not part of the public ABI (that is include/gdn2.h).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -50,6 +51,13 @@ struct Params {
     bf16 *vnew;                 // [T_tot, HV, V]  u_t (v_new) per token
     uint8_t *rec;               // [NCmax, HV] records of the tensor-core path
     int vtile;                  // V columns per state CTA (tensor-core path)
+    // TMA tensor maps over the rows of g, v, w (tensor-core intra kernel): a
+    // box is 64 tokens x D channels of one head.  tm_order = 0: coordinates
+    // (channel, head, token); 1: (channel, token, head).  tmap = 0: the maps
+    // are not set and the kernel copies the rows one by one.
+    CUtensorMap tm_g, tm_v, tm_w;
+    int tmap;
+    int tm_order_g, tm_order_v, tm_order_w;
 };
 
 // Workspace layout (byte offsets), a function of the problem only.

@@ -85,6 +85,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Tile of a 3-D tensor map (box given by the map) -> shared memory, completing
+// on an mbarrier.  tmap: generic address of a CUtensorMap in kernel-parameter,
+// constant or global memory; c0 (innermost) .. c2: element coordinates, with
+// c0 * element size a multiple of 16 bytes.  dst 128-byte aligned.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0, int c1, int c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Per-thread 16-byte global -> shared copy (L2 only); src_bytes = 0 writes
 // zeros without reading src.  Completion: cp_async_wait_all by the issuing
 // thread, then a block barrier before other threads read the data.

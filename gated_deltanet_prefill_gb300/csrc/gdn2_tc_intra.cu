@@ -86,7 +86,7 @@ struct IntraCfg {
 __device__ __forceinline__ uint4 ldg16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
 
 template <int D>
-__global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params p) {
+__global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const __grid_constant__ Params p) {
     using C = IntraCfg<D>;
     constexpr int NJ = D / 32;         // 8-channel chunks per thread
     constexpr int PARTS = kIntraThreads / D;
@@ -136,7 +136,20 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
     float *Gs = reinterpret_cast<float *>(sm + C::oG);
     uint8_t *raw_v = sm + C::oBWU;
     uint8_t *raw_w = sm + C::oBWU + 64 * D * 2;
+    // TMA tile coordinates of token row t0 of head hh (the tile covers 64 rows;
+    // rows past the chunk hold other tokens or zeros and are never used)
+    auto tile = [&](void *dst, const CUtensorMap *map, int order, int hh, uint64_t *bar) {
+        const int t0 = static_cast<int>(nstart);
+        tma_load_3d(dst, map, 0, order ? t0 : hh, order ? hh : t0, bar);
+    };
     auto stage_g = [&]() {  // warp 7
+        if (p.tmap) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar_g, p.has_g ? 64u * D * 4 : 0u);
+                if (p.has_g) tile(Gs, &p.tm_g, p.tm_order_g, nhv, &bar_g);
+            }
+            return;
+        }
         const uint32_t rows = p.has_g ? static_cast<uint32_t>(nlen) : 0u;
         if (lane == 0) mbar_arrive_expect_tx(&bar_g, rows * D * 4);
         __syncwarp();
@@ -144,6 +157,14 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(Params 
             bulk_g2s(Gs + r * D, p.g + (nstart + r) * p.sg_t + static_cast<int64_t>(nhv) * p.sg_h, D * 4, &bar_g);
     };
     auto stage_vw = [&]() {  // warp 2
+        if (p.tmap) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bar_vw, 64u * D * 2 * (p.has_w ? 2u : 1u));
+                tile(raw_v, &p.tm_v, p.tm_order_v, nhv, &bar_vw);
+                if (p.has_w) tile(raw_w, &p.tm_w, p.tm_order_w, nhv, &bar_vw);
+            }
+            return;
+        }
         const uint32_t rows = static_cast<uint32_t>(nlen);
         if (lane == 0) mbar_arrive_expect_tx(&bar_vw, rows * D * 2 * (p.has_w ? 2u : 1u));
         __syncwarp();

@@ -160,6 +160,11 @@ GDN2_API gdn2_status gdn2_check_args(const void *q, const void *k, const void *v
  * Returns GDN2_OK once all kernels are enqueued.  cu_seqlens is checked on
  * the device; a bad cu_seqlens makes every kernel a no-op and is reported by
  * gdn2_device_status.
+ *
+ * The tensor-core path reads g, v and w through TMA tensor maps encoded on
+ * the host at each call (no device state).  Where the driver rejects a layout
+ * (for example a zero head stride) it copies those rows one by one instead;
+ * the environment variable GDN2_ROW_COPIES=1 forces that path (diagnostics).
  */
 GDN2_API gdn2_status gdn2_chunk_fwd(const void *q, const void *k, const void *v, const void *g,
                            const void *beta, const void *w, float scale,

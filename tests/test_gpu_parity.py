@@ -120,6 +120,41 @@ def test_strided_inputs_and_int64_cu(cuda_lib, impl):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
+def test_head_major_layout(cuda_lib, impl):
+    """Tensors stored head-major ([heads, T, D] memory, viewed as [T, heads,
+    D]): the head stride exceeds the token stride."""
+    wl = inputs.small("headmajor", [90, 64, 3], H=2, HV=4, K=128, V=128, g_max=0.5, beta_max=2.0,
+                      h0_std=0.05, seed=36)
+    d = inputs.generate(wl)
+    o_ref, h_ref = run_oracle(d)
+    dd = to_dev(d)
+    for key in ("q", "k", "v", "beta", "w", "g"):
+        x = dd[key]
+        dd[key] = x.transpose(0, 1).contiguous().transpose(0, 1)
+        assert dd[key].stride(1) > dd[key].stride(0)
+    o, hT = run_gpu(cuda_lib, dd, impl)
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_tc_row_copies(cuda_lib, monkeypatch, D):
+    """The tensor-core intra kernel's row-by-row copies of g, v, w (used when
+    the tensor maps cannot be encoded; GDN2_ROW_COPIES=1 forces them), with
+    ragged chunks and no w."""
+    monkeypatch.setenv("GDN2_ROW_COPIES", "1")
+    wl = inputs.small("rows", [1, 70, 129], H=1, HV=2, K=D, V=D, g_max=1.0, beta_max=2.0, h0_std=0.05,
+                      seed=37)
+    check_full(cuda_lib, wl, "tc")
+    d = inputs.generate(wl)
+    d["w"] = None
+    o_ref, h_ref = run_oracle(d)
+    o, hT = run_gpu(cuda_lib, to_dev(d), "tc")
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
+
+
+@pytest.mark.parametrize("impl", IMPLS)
 def test_split_sequence_matches_one_pass(cuda_lib, impl):
     """Prefill in two calls carrying the final state equals one call
     (FlashGDN-2 quick start: prefill, then continue from the state)."""
