@@ -290,6 +290,13 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
                              d->T_tot, p.sv_t, p.sv_h) &&
                  (!p.has_w || encode_rows(&p.tm_w, &p.tm_order_w, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->V,
                                           d->HV, d->T_tot, p.sw_t, p.sw_h));
+        p.tpre = p.tmap &&
+                 encode_rows(&p.tm_k, &p.tm_order_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->K, d->H,
+                             d->T_tot, p.sk_t, p.sk_h) &&
+                 encode_rows(&p.tm_q, &p.tm_order_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->K, d->H,
+                             d->T_tot, p.sq_t, p.sq_h) &&
+                 (!p.has_beta || encode_rows(&p.tm_b, &p.tm_order_b, beta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                             d->K, d->HV, d->T_tot, p.sb_t, p.sb_h));
     }
     p.q_in = p.q; p.k_in = p.k;
     p.sq_in_t = p.sq_t; p.sq_in_h = p.sq_h; p.sk_in_t = p.sk_t; p.sk_in_h = p.sk_h;

@@ -58,6 +58,11 @@ struct Params {
     CUtensorMap tm_g, tm_v, tm_w;
     int tmap;
     int tm_order_g, tm_order_v, tm_order_w;
+    // maps over k, q (key heads) and beta (value heads) with the same box,
+    // used only to prefetch the next item's tiles into L2 (tpre = 0: none)
+    CUtensorMap tm_k, tm_q, tm_b;
+    int tpre;
+    int tm_order_k, tm_order_q, tm_order_b;
 };
 
 // Workspace layout (byte offsets), a function of the problem only.

@@ -97,6 +97,13 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int c0,
         : "memory");
 }
 
+// Prefetch a tile of a 3-D tensor map into L2 (no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(c0),
+                 "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // Per-thread 16-byte global -> shared copy (L2 only); src_bytes = 0 writes
 // zeros without reading src.  Completion: cp_async_wait_all by the issuing
 // thread, then a block barrier before other threads read the data.
@@ -106,6 +113,12 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Named barrier `id` (1..15) over `nthreads` threads of the block (a
+// multiple of 32, whole warps); id 0 is __syncthreads.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 // Make generic-proxy shared-memory writes visible to the async proxy
 // (tcgen05.mma operand reads, bulk copies).

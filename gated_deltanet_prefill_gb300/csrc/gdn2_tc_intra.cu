@@ -89,8 +89,6 @@ template <int D>
 __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const __grid_constant__ Params p) {
     using C = IntraCfg<D>;
     constexpr int NJ = D / 32;         // 8-channel chunks per thread
-    constexpr int PARTS = kIntraThreads / D;
-    constexpr int ROWS = 64 / PARTS;   // rows per scan part
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t &bar_mma = *reinterpret_cast<uint64_t *>(sm + C::oBar);
@@ -186,13 +184,78 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         qp = p.q + tok * p.sq_t + static_cast<int64_t>(h) * p.sq_h;
         bp = p.beta + tok * p.sb_t + static_cast<int64_t>(hv) * p.sb_h;
     };
+    // G' = G log2(e): every decay factor below is an exact power of two of a
+    // difference of G' values.  The staged item's prefix sums (in place in the
+    // G scratch) and per-channel decay tables are computed by the four warps
+    // that are idle in the W/U epilogue: warps 2, 3, 6, 7 (named barrier 1).
+    constexpr float kLog2e = 1.4426950408889634f;
+    constexpr int P4 = 128 / D;     // scan parts (rows split in P4 ranges)
+    constexpr int R4 = 64 / P4;     // rows per part
+    float *gE = reinterpret_cast<float *>(sm + C::oTab);  // G' at E_J
+    float *tGB = gE + 4 * D;                              // e^{G_{B_I}}
+    float *tI = tGB + 4 * D;                              // e^{G_{B_I} - G_{E_I}}
+    float *t2 = tI + 4 * D;                               // e^{G_{E_{I+1}} - G_{E_I}}, I = 0, 1
+    uint32_t gph = 0, vph = 0;  // parities of the g and v/w staging barriers
+    const bool aux = (warp & 2) != 0;
+    auto scan_tables = [&](int ilen, uint8_t *irec) {
+        const int lt = 32 * ((warp & 1) + 2 * (warp >> 2)) + lane;  // 0 .. 127
+        if (!mbar_wait(&bar_g, gph)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
+        const int glen = p.has_g ? ilen : 0;  // rows past it read as 0
+        const int ch = lt % D, part = lt / D;
+        float *base = Gs + part * R4 * D + ch;
+        float acc = 0.f;
+#pragma unroll 1
+        for (int r8 = 0; r8 < R4; r8 += 8) {
+            float *b8 = base + r8 * D;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int row = part * R4 + r8 + k;
+                acc += row < glen ? __fmul_rn(b8[k * D], kLog2e) : 0.f;
+                b8[k * D] = acc;
+            }
+        }
+        if (P4 > 1) {
+            float *tot = reinterpret_cast<float *>(sm + C::oTab);  // [P4][D], before the tables
+            tot[part * D + ch] = acc;
+            named_sync(1, 128);
+            float off = 0.f;
+            for (int pp = 0; pp < part; ++pp) off += tot[pp * D + ch];
+            if (part > 0) {
+#pragma unroll 1
+                for (int r8 = 0; r8 < R4; r8 += 8) {
+                    float *b8 = base + r8 * D;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) b8[k * D] += off;
+                }
+            }
+        }
+        named_sync(1, 128);
+        if (lt < D) {
+            float e[4];
+#pragma unroll
+            for (int J = 0; J < 4; ++J) e[J] = Gs[min(16 * J + 15, ilen - 1) * D + lt];
+#pragma unroll
+            for (int J = 0; J < 4; ++J) {
+                const float b = J > 0 ? e[J - 1] : 0.f;
+                gE[J * D + lt] = e[J];
+                tGB[J * D + lt] = ex2(b);
+                tI[J * D + lt] = ex2(b - e[J]);
+            }
+            t2[lt] = ex2(e[1] - e[0]);
+            t2[D + lt] = ex2(e[2] - e[1]);
+            reinterpret_cast<float *>(irec + Rec<D>::eGL)[lt] = ex2(e[3]);
+        }
+    };
+    auto rec_of = [&](int ic, int ihv) { return p.rec + (static_cast<size_t>(ic) * p.HV + ihv) * Rec<D>::bytes; };
+
     if (static_cast<int>(blockIdx.x) < total) meta(blockIdx.x);
     __syncthreads();  // barriers initialised
     if (static_cast<int>(blockIdx.x) < total) {
         if (warp == 7) stage_g();
         if (warp == 2) stage_vw();
+        if (aux) scan_tables(nlen, rec_of(nc, nhv));
     }
-    uint32_t phase = 0;  // parity of the staging barriers for the current item
+    gph ^= 1u;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -201,19 +264,15 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
 #pragma unroll 1
     for (int it = blockIdx.x; it < total; it += gridDim.x) {
     adopt();
-    uint8_t *rec = p.rec + (static_cast<size_t>(c) * p.HV + hv) * Rec<D>::bytes;
+    uint8_t *rec = rec_of(c, hv);
 
     // ---- 1. cumsum (g is in the G scratch) ----------------------------------------
     nk = nq = nb = z4;
-    uint4 mk = z4, mq = z4, mb = z4;
-    if (live) {  // first two operand chunks; later chunks are fetched two ahead
+    if (live) {  // first operand chunk; later chunks are fetched one ahead
         const int cb = 8 * seg;
         nk = ldg16(kp + cb);
         nq = ldg16(qp + cb);
         if (p.has_beta) nb = ldg16(bp + cb);
-        mk = ldg16(kp + cb + 32);
-        mq = ldg16(qp + cb + 32);
-        if (p.has_beta) mb = ldg16(bp + cb + 32);
     }
     float kscale = 1.f, qscale = 1.f;
     if (p.l2norm) {
@@ -238,82 +297,22 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         kscale = 1.f / fmaxf(sqrtf(sk), 1e-12f);
         qscale = 1.f / fmaxf(sqrtf(sq), 1e-12f);
     }
-    // G' = G log2(e): every decay factor below is an exact power of two of a
-    // difference of G' values.  g is in the G scratch (rows < len; the rest
-    // read as 0), raw v and w in the B operand area.
-    constexpr float kLog2e = 1.4426950408889634f;
-    if (!mbar_wait(&bar_g, phase)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
-    if (!mbar_wait(&bar_vw, phase)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
-    phase ^= 1u;
-    // this thread's v and w chunks; w v goes to its operand image after the
-    // scan's barriers (it overwrites the raw rows)
-    uint4 rv[NJ], rw[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        rv[j] = rw[j] = z4;
-        if (live) {
-            rv[j] = *reinterpret_cast<const uint4 *>(raw_v + (t * D + 8 * (seg + 4 * j)) * 2);
-            if (p.has_w) rw[j] = *reinterpret_cast<const uint4 *>(raw_w + (t * D + 8 * (seg + 4 * j)) * 2);
-        }
-    }
-    const int glen = p.has_g ? len : 0;
-    float *tot = reinterpret_cast<float *>(sm + C::oTab);  // [PARTS][D], before the tables
-    {
-        const int ch = tid % D, part = tid / D;
-        float *base = Gs + part * ROWS * D + ch;
-        float acc = 0.f;
-#pragma unroll 1
-        for (int r8 = 0; r8 < ROWS; r8 += 8) {
-            float *b8 = base + r8 * D;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int row = part * ROWS + r8 + k;
-                acc += row < glen ? __fmul_rn(b8[k * D], kLog2e) : 0.f;
-                b8[k * D] = acc;
-            }
-        }
-        tot[part * D + ch] = acc;
-        __syncthreads();
-        float off = 0.f;
-        for (int pp = 0; pp < part; ++pp) off += tot[pp * D + ch];
-        if (part > 0) {
-#pragma unroll 1
-            for (int r8 = 0; r8 < ROWS; r8 += 8) {
-                float *b8 = base + r8 * D;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) b8[k * D] += off;
-            }
-        }
-    }
-    __syncthreads();
+    // G' prefix sums and tables are ready (computed during the previous item's
+    // W/U epilogue, or before the loop); raw v and w are in the B operand area
+    if (!mbar_wait(&bar_vw, vph)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
+    vph ^= 1u;
+    // w v for this thread's chunks, stored to its operand image after the
+    // barrier below (it overwrites the raw rows)
+    uint4 wX2[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         const int cb = 8 * (seg + 4 * j);
-        float vv[8], ww[8], xv[8];
-        unpack8_bf(rv[j], vv);
-        unpack8_bf(rw[j], ww);
+        float vv[8], ww[8];
+        unpack8_bf(live ? *reinterpret_cast<const uint4 *>(raw_v + (t * D + cb) * 2) : z4, vv);
+        unpack8_bf(live && p.has_w ? *reinterpret_cast<const uint4 *>(raw_w + (t * D + cb) * 2) : z4, ww);
 #pragma unroll
-        for (int x = 0; x < 8; ++x) xv[x] = (p.has_w || !live) ? ww[x] * vv[x] : vv[x];
-        *reinterpret_cast<uint4 *>(sm + C::oBWU + ((D + cb) / 64) * 8192 + swz(t, (cb % 64) / 8)) = pack8_h(xv);
-    }
-    float *gE = reinterpret_cast<float *>(sm + C::oTab);  // G' at E_J
-    float *tGB = gE + 4 * D;                              // e^{G_{B_I}}
-    float *tI = tGB + 4 * D;                              // e^{G_{B_I} - G_{E_I}}
-    float *t2 = tI + 4 * D;                               // e^{G_{E_{I+1}} - G_{E_I}}, I = 0, 1
-    if (tid < D) {
-        float e[4];
-#pragma unroll
-        for (int J = 0; J < 4; ++J) e[J] = Gs[min(16 * J + 15, len - 1) * D + tid];
-#pragma unroll
-        for (int J = 0; J < 4; ++J) {
-            const float b = J > 0 ? e[J - 1] : 0.f;
-            gE[J * D + tid] = e[J];
-            tGB[J * D + tid] = ex2(b);
-            tI[J * D + tid] = ex2(b - e[J]);
-        }
-        t2[tid] = ex2(e[1] - e[0]);
-        t2[D + tid] = ex2(e[2] - e[1]);
-        reinterpret_cast<float *>(rec + Rec<D>::eGL)[tid] = ex2(e[3]);
+        for (int x = 0; x < 8; ++x) ww[x] = (p.has_w || !live) ? ww[x] * vv[x] : vv[x];
+        wX2[j] = pack8_h(ww);
     }
     float Gr[8 * NJ];
 #pragma unroll
@@ -324,7 +323,12 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         Gr[8 * j + 0] = a.x; Gr[8 * j + 1] = a.y; Gr[8 * j + 2] = a.z; Gr[8 * j + 3] = a.w;
         Gr[8 * j + 4] = b.x; Gr[8 * j + 5] = b.y; Gr[8 * j + 6] = b.z; Gr[8 * j + 7] = b.w;
     }
-    __syncthreads();  // G scratch is dead from here on; the tables are visible
+    __syncthreads();  // G scratch and raw v, w are dead from here on
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        const int cb = 8 * (seg + 4 * j);
+        *reinterpret_cast<uint4 *>(sm + C::oBWU + ((D + cb) / 64) * 8192 + swz(t, (cb % 64) / 8)) = wX2[j];
+    }
 
     // ---- 2. operand images -------------------------------------------------------
 #pragma unroll
@@ -338,14 +342,11 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
 #pragma unroll
             for (int x = 0; x < 8; ++x) bb[x] = 1.f;
         }
-        nk = mk;
-        nq = mq;
-        nb = mb;
-        if (j + 2 < NJ && live) {  // fetch two chunks ahead
-            const int cn = 8 * (seg + 4 * (j + 2));
-            mk = ldg16(kp + cn);
-            mq = ldg16(qp + cn);
-            if (p.has_beta) mb = ldg16(bp + cn);
+        if (j + 1 < NJ && live) {  // fetch the next chunk
+            const int cn = 8 * (seg + 4 * (j + 1));
+            nk = ldg16(kp + cn);
+            nq = ldg16(qp + cn);
+            if (p.has_beta) nb = ldg16(bp + cn);
         }
         // outputs packed two channels per 32-bit word as they are produced
         uint32_t wLk[4], wLq[4], wkr[4], wX1[4], wQe[4], wKd[4], wr0[4], wr2[4], wr3[4];
@@ -474,11 +475,19 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     const bool has_next = it + static_cast<int>(gridDim.x) < total;
     if (has_next) meta(it + static_cast<int>(gridDim.x));
     tc_fence_before();
-    __syncthreads();
 
     // ---- 4. T = (I + A)^{-1}, blocked forward substitution (fp32) ---------------
+    // The diagonal inverses start once the A warps (0, 1, 4, 5) have written
+    // A (named barrier 2); the P warps are still storing P meanwhile.
     float *Tf = reinterpret_cast<float *>(sm + C::oTf);
     float *Yb = reinterpret_cast<float *>(sm + C::oY);
+    if (!aux) named_sync(2, 128);
+    if (has_next && p.tpre && warp == 6 && lane == 0) {  // next item's k, q, beta into L2
+        const int t0 = static_cast<int>(nstart), nh = nhv / p.group;
+        tma_prefetch_3d(&p.tm_k, 0, p.tm_order_k ? t0 : nh, p.tm_order_k ? nh : t0);
+        tma_prefetch_3d(&p.tm_q, 0, p.tm_order_q ? t0 : nh, p.tm_order_q ? nh : t0);
+        if (p.has_beta) tma_prefetch_3d(&p.tm_b, 0, p.tm_order_b ? t0 : nhv, p.tm_order_b ? nhv : t0);
+    }
     if (tid < 64) {  // diagonal 16x16 blocks, one thread per (block, column)
         const int Ib = tid / 16, j = tid % 16, o = 16 * Ib;
         float x[16];
@@ -575,6 +584,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     if (!mbar_wait(&bar_mma, 1)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
     tc_fence_after();
     if (has_next && warp == 2) stage_vw();  // the W/U product has read the B operand area
+    if (has_next && aux) scan_tables(nlen, rec_of(nc, nhv));  // the next item's G' and tables
+    if (has_next) gph ^= 1u;
 
     // ---- 6. Wt -> A1 rows 64-127, Ut -> Ut image (fp16) -------------------------
     if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
