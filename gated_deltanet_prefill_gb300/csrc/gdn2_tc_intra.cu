@@ -25,9 +25,11 @@
 //  5. tcgen05 (fp16): [Wt | Ut] = T x [beta k e^G | w v]  (M=128, N=2D, K=64).
 //  6. write Qe, Kd^T, P, Wt, Ut (fp16) and eGL (fp32) as shared-memory images.
 //
-// Thread (t = tid / 4, seg = tid % 4) owns token row t and the 8-channel
-// chunks seg, seg + 4, seg + 8, ...: the four segments of a row fall in
-// different shared-memory banks for every per-channel table read.
+// Thread (t, seg = tid % 4) owns token row t and the 8-channel chunks seg,
+// seg + 4, seg + 8, ...: the four segments of a row fall in different
+// shared-memory banks for every per-channel table read.  Warp w covers rows
+// 8w .. 8w + 7, its quarter-warps rows k and k + 4, which land in the two
+// halves of the 128-byte swizzle pattern (conflict-free 16-byte stores).
 #include "gdn2_internal.cuh"
 #include "gdn2_record.cuh"
 #include "gdn2_tc.cuh"
@@ -97,7 +99,11 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     uint64_t &bar_vw = *reinterpret_cast<uint64_t *>(sm + C::oBar + 24);
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int t = tid / 4, seg = tid % 4;
+    // thread (t, seg): a warp covers 8 rows; lanes 8k .. 8k+7 take rows k and
+    // k + 4 of them, so a quarter-warp's 16-byte stores into a 128-byte
+    // swizzled row pair hit 8 different chunks
+    const int seg = tid % 4;
+    const int t = 8 * warp + (((lane >> 2) & 1) << 2) + (lane >> 3);
     const int I = t / 16;
     const int total = p.status[0] == GDN2_OK ? p.status[1] * p.HV : 0;  // (chunk, value head) items
 
@@ -350,19 +356,29 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         }
         // outputs packed two channels per 32-bit word as they are produced
         uint32_t wLk[4], wLq[4], wkr[4], wX1[4], wQe[4], wKd[4], wr0[4], wr2[4], wr3[4];
+        auto cmp = [](const float4 &v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; };
+        const float4 z4f = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int x2 = 0; x2 < 4; ++x2) {
+            // per-channel tables for channels cb + 4 (x2 / 2) .. + 3 (16-byte loads)
+            const int c4 = cb + 4 * (x2 / 2);
+            const float4 vB = I > 0 ? *reinterpret_cast<const float4 *>(gE + (I - 1) * D + c4) : z4f;
+            const float4 vE = *reinterpret_cast<const float4 *>(gE + I * D + c4);
+            const float4 vL = *reinterpret_cast<const float4 *>(gE + 3 * D + c4);
+            const float4 vG = *reinterpret_cast<const float4 *>(tGB + I * D + c4);
+            const float4 vI = *reinterpret_cast<const float4 *>(tI + I * D + c4);
+            const float4 v2 = *reinterpret_cast<const float4 *>(t2 + (I & 1) * D + c4);
+            const float4 v3 = *reinterpret_cast<const float4 *>(t2 + D + c4);
             float lk[2], lq[2], kr[2], x1[2], qe[2], kd[2], r0[2], r2[2], r3[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int x = 2 * x2 + e;
-                const int ci = cb + x;
-                const float gB = I > 0 ? gE[(I - 1) * D + ci] : 0.f;
+                const int ce = x & 3;  // component in the 16-byte table loads
                 const float gt = Gr[8 * j + x];
-                const float F = ex2(gt - gB);                         // e^{G_t - G_{B_I}}
-                const float eR = ex2(gE[I * D + ci] - gt);            // e^{G_{E_I} - G_t}
-                const float eL = ex2(gE[3 * D + ci] - gt);            // e^{G_L - G_t}
-                const float eGB = tGB[I * D + ci];                    // e^{G_{B_I}}
+                const float F = ex2(gt - cmp(vB, ce));                // e^{G_t - G_{B_I}}
+                const float eR = ex2(cmp(vE, ce) - gt);               // e^{G_{E_I} - G_t}
+                const float eL = ex2(cmp(vL, ce) - gt);               // e^{G_L - G_t}
+                const float eGB = cmp(vG, ce);                        // e^{G_{B_I}}
                 const float kx = kk[x] * kscale;
                 lk[e] = bb[x] * kx * F;
                 lq[e] = qq[x] * qscale * F;
@@ -370,10 +386,9 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
                 x1[e] = lk[e] * eGB;
                 qe[e] = lq[e] * eGB;
                 kd[e] = kx * eL;
-                r0[e] = kr[e] * tI[I * D + ci];                       // row of R_I
-                const float f2 = t2[(I & 1) * D + ci];                // e^{G_{E_{I+1}} - G_{E_I}}
-                r2[e] = kr[e] * f2;                                   // row of R_{I+2}, I <= 1
-                r3[e] = r2[e] * t2[D + ci];                           // row of R_3, I = 0
+                r0[e] = kr[e] * cmp(vI, ce);                          // row of R_I
+                r2[e] = kr[e] * cmp(v2, ce);                          // row of R_{I+2}, I <= 1
+                r3[e] = r2[e] * cmp(v3, ce);                          // row of R_3, I = 0
             }
             wLk[x2] = pack_bf2(lk[0], lk[1]);
             wLq[x2] = pack_bf2(lq[0], lq[1]);
@@ -494,8 +509,15 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             float acc = (i == j) ? 1.f : 0.f;
+            const float *arow = Af + (o + i) * kLD + o;  // 16-byte aligned (kLD = 68)
 #pragma unroll
-            for (int m = 0; m < i; ++m) acc -= Af[(o + i) * kLD + o + m] * x[m];
+            for (int m4 = 0; m4 < i; m4 += 4) {
+                const float4 a = *reinterpret_cast<const float4 *>(arow + m4);
+                acc -= a.x * x[m4];
+                if (m4 + 1 < i) acc -= a.y * x[m4 + 1];
+                if (m4 + 2 < i) acc -= a.z * x[m4 + 2];
+                if (m4 + 3 < i) acc -= a.w * x[m4 + 3];
+            }
             x[i] = (i < j) ? 0.f : acc;
         }
 #pragma unroll
@@ -510,21 +532,29 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         const int r0 = 16 * (Ib + 1), c0 = 16 * Ib;
         float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float a = Af[(r0 + i) * kLD + c0 + m];
-            const float2 tv = *reinterpret_cast<const float2 *>(Tf + (c0 + m) * kLD + c0 + j0);
-            y0 += a * tv.x;
-            y1 += a * tv.y;
+        for (int m4 = 0; m4 < 16; m4 += 4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(Af + (r0 + i) * kLD + c0 + m4);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                const float2 tv = *reinterpret_cast<const float2 *>(Tf + (c0 + m4 + mm) * kLD + c0 + j0);
+                y0 += av[mm] * tv.x;
+                y1 += av[mm] * tv.y;
+            }
         }
         *reinterpret_cast<float2 *>(Yb + b * 256 + i * 16 + j0) = make_float2(y0, y1);
         __syncthreads();
         float z0 = 0.f, z1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float tv = Tf[(r0 + i) * kLD + r0 + m];
-            const float2 yv = *reinterpret_cast<const float2 *>(Yb + b * 256 + m * 16 + j0);
-            z0 -= tv * yv.x;
-            z1 -= tv * yv.y;
+        for (int m4 = 0; m4 < 16; m4 += 4) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(Tf + (r0 + i) * kLD + r0 + m4);
+            const float tvv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                const float2 yv = *reinterpret_cast<const float2 *>(Yb + b * 256 + (m4 + mm) * 16 + j0);
+                z0 -= tvv[mm] * yv.x;
+                z1 -= tvv[mm] * yv.y;
+            }
         }
         *reinterpret_cast<float2 *>(Tf + (r0 + i) * kLD + c0 + j0) = make_float2(z0, z1);
     }
@@ -535,22 +565,32 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     {
         const int i0 = 2 * (tid / 16), j0 = 2 * (tid % 16);
         float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
-#pragma unroll 4
-        for (int m = j0 & ~15; m < 32; ++m) {
-            const float a0 = Af[(32 + i0) * kLD + m], a1 = Af[(33 + i0) * kLD + m];
-            const float2 tv = *reinterpret_cast<const float2 *>(Tf + m * kLD + j0);
-            x00 += a0 * tv.x; x01 += a0 * tv.y; x10 += a1 * tv.x; x11 += a1 * tv.y;
+#pragma unroll 2
+        for (int m4 = j0 & ~15; m4 < 32; m4 += 4) {
+            const float4 p0 = *reinterpret_cast<const float4 *>(Af + (32 + i0) * kLD + m4);
+            const float4 p1 = *reinterpret_cast<const float4 *>(Af + (33 + i0) * kLD + m4);
+            const float a0v[4] = {p0.x, p0.y, p0.z, p0.w}, a1v[4] = {p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                const float2 tv = *reinterpret_cast<const float2 *>(Tf + (m4 + mm) * kLD + j0);
+                x00 += a0v[mm] * tv.x; x01 += a0v[mm] * tv.y; x10 += a1v[mm] * tv.x; x11 += a1v[mm] * tv.y;
+            }
         }
         *reinterpret_cast<float2 *>(Yb + i0 * 32 + j0) = make_float2(x00, x01);
         *reinterpret_cast<float2 *>(Yb + (i0 + 1) * 32 + j0) = make_float2(x10, x11);
         __syncthreads();
         float z00 = 0.f, z01 = 0.f, z10 = 0.f, z11 = 0.f;
         const int mend = (i0 & ~15) + 16;
-#pragma unroll 4
-        for (int m = 0; m < mend; ++m) {
-            const float t0 = Tf[(32 + i0) * kLD + 32 + m], t1 = Tf[(33 + i0) * kLD + 32 + m];
-            const float2 xv = *reinterpret_cast<const float2 *>(Yb + m * 32 + j0);
-            z00 -= t0 * xv.x; z01 -= t0 * xv.y; z10 -= t1 * xv.x; z11 -= t1 * xv.y;
+#pragma unroll 2
+        for (int m4 = 0; m4 < mend; m4 += 4) {
+            const float4 p0 = *reinterpret_cast<const float4 *>(Tf + (32 + i0) * kLD + 32 + m4);
+            const float4 p1 = *reinterpret_cast<const float4 *>(Tf + (33 + i0) * kLD + 32 + m4);
+            const float t0v[4] = {p0.x, p0.y, p0.z, p0.w}, t1v[4] = {p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                const float2 xv = *reinterpret_cast<const float2 *>(Yb + (m4 + mm) * 32 + j0);
+                z00 -= t0v[mm] * xv.x; z01 -= t0v[mm] * xv.y; z10 -= t1v[mm] * xv.x; z11 -= t1v[mm] * xv.y;
+            }
         }
         *reinterpret_cast<float2 *>(Tf + (32 + i0) * kLD + j0) = make_float2(z00, z01);
         *reinterpret_cast<float2 *>(Tf + (33 + i0) * kLD + j0) = make_float2(z10, z11);
@@ -559,12 +599,12 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     // T -> fp16 K-major image [64 t][64 s]; zeros above the diagonal
     for (int e = tid; e < 64 * 8; e += kIntraThreads) {
         const int tt = e / 8, chunk = e % 8;
+        const float4 lo = *reinterpret_cast<const float4 *>(Tf + tt * kLD + 8 * chunk);
+        const float4 hi = *reinterpret_cast<const float4 *>(Tf + tt * kLD + 8 * chunk + 4);
+        const float tv8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
         float f[8];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-            const int s = 8 * chunk + x;
-            f[x] = s <= tt ? Tf[tt * kLD + s] : 0.f;
-        }
+        for (int x = 0; x < 8; ++x) f[x] = 8 * chunk + x <= tt ? tv8[x] : 0.f;
         *reinterpret_cast<uint4 *>(sm + C::oTimg + swz(tt, chunk)) = pack8_h(f);
     }
     fence_proxy_async();
