@@ -42,7 +42,7 @@ DEFAULT_WORKLOAD = 5
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
@@ -110,12 +110,39 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha():
+def strip_comments(src):
+    """C/C++ source without comments and blank lines (string literals kept)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            while i < n and src[i] != "\n":
+                i += 1
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).splitlines()]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
+def kernel_source_sha(read=None):
+    """Hash of the CUDA sources' code (comments and blank lines ignored), to
+    tell whether a committed ncu summary was taken on the current kernels."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_prefill_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            txt = read(f) if read else open(os.path.join(csrc, f), encoding="utf-8").read()
+            h.update(f.encode() + b"\0" + strip_comments(txt).encode() + b"\0")
     return h.hexdigest()[:16]
 
 
@@ -159,17 +186,17 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        time.sleep(0.1)
         return self
 
     def __exit__(self, *a):
         self.out = ""
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.05)
             self.proc.terminate()
             try:
                 self.out, _ = self.proc.communicate(timeout=5)

@@ -1,13 +1,17 @@
 // Tensor-core intra-chunk kernel: everything of a 64-token chunk that does
 // not depend on the incoming state, written as the record the state kernel
 // consumes (gdn2_record.cuh).  Persistent: two CTAs of 256 threads per SM walk
-// the (chunk, value head) items; each CTA loads its next item's inputs while
-// the current one is in its solve and epilogues.
+// the (chunk, value head) items.  While an item is being processed the next
+// one is prepared: its g, v, w tiles arrive by TMA (tensor maps built on the
+// host, row copies when a layout cannot be mapped), its k, q, beta tiles are
+// prefetched into L2, and the four warps idle in the W/U epilogue compute its
+// prefix sums and decay tables.
 //
 // Steps (FlashRT gated-delta-attention page: norm/cumsum, kkt, solve_tril,
 // recompute_wu; fused into one kernel here, with GDN-2's channel-wise gates):
-//  1. load g, k, q (key head), v, w, beta (value head); optional q/k L2 norm;
-//     G = chunk-local inclusive cumsum of g (two-part scan in shared memory).
+//  1. G = chunk-local inclusive cumsum of g (log2-scaled, in shared memory);
+//     k, q (key head), beta (value head) read per thread one channel chunk
+//     ahead; optional q/k L2 norm; w v formed from the staged v, w tiles.
 //  2. decay factors through 16-token sub-chunk references (burn-gdn2 README,
 //     "Numerical stability"): with B_I the row before sub-chunk I and E_J the
 //     last row of sub-chunk J,
