@@ -45,6 +45,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--op", choices=["prefill", "decode"], default="prefill",
+                    help="prefill: the chunked forward (default); decode: the token-by-token "
+                         "recurrence from a carried state (gdn2_recurrent_fwd)")
+    ap.add_argument("--decode-batch", type=int, default=128)
+    ap.add_argument("--decode-tokens", type=int, default=1)
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
     ap.add_argument("--kernels", choices=["tc", "simt"], default=os.environ.get("GDN2_BENCH_KERNELS", "tc"))
     ap.add_argument("--e2e-steps", type=int, default=3)
@@ -450,10 +455,78 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def decode_bytes(wl):
+    """Algorithmic HBM bytes of one recurrent call: the state read and written
+    once per (sequence, value head), each token's inputs read once (q, k per
+    key head) and its output written once."""
+    K, V = wl.K, wl.V
+    per_tok_hv = V * 2 + V * 2 + K * 2 + K * 4 + V * 2          # v, w, beta, g, o
+    per_tok_h = 2 * K * 2                                         # q, k
+    state = (2 if wl.h0_std else 1) * wl.N * wl.HV * K * V * 4
+    return state + wl.T_tot * (wl.HV * per_tok_hv + wl.H * per_tok_h)
+
+
+def run_decode(args):
+    """The token-by-token recurrence (decode) on one GPU: one JSON line with
+    its own metric, roofline and oracle baseline (not the headline)."""
+    import torch
+    from gated_deltanet_prefill_gb300 import build as gbuild
+    from gated_deltanet_prefill_gb300 import gdn2, inputs
+
+    torch.cuda.set_device(0)
+    gbuild.build()
+    gdn2.load()
+    wl = inputs.decode_workload(args.decode_batch, args.decode_tokens)
+    d = inputs.generate(wl, device="cuda")
+    out = torch.empty((wl.T_tot, wl.HV, wl.V), dtype=torch.bfloat16, device="cuda")
+    fs = torch.empty((wl.N, wl.HV, wl.K, wl.V), dtype=torch.float32, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        gdn2.recurrent_gdn2_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                                initial_state=d["h0"], cu_seqlens=d["cu_seqlens"], out=out, final_state=fs,
+                                workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(0) as clk:
+        start.record(stream)
+        for _ in range(K):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / K
+    peak, peak_kind = load_peaks()
+    nbytes = decode_bytes(wl)
+    ach = nbytes / (ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+            "traffic": ncu_traffic("recurrent", "recurrent", wl.name), "kernel": "recurrent",
+            "timed": "whole call (cu_seqlens check + recurrence), CUDA events",
+            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
+    cpu = None if args.no_cpu_baseline else cpu_baseline(d, wl, args.cpu_seconds)
+    line = {"metric": "GDN-2 decode tokens/s (token-by-token from a carried state)",
+            "value": wl.T_tot / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.N, "T": wl.lens[0], "H": wl.H, "HV": wl.HV, "K": wl.K,
+                       "V": wl.V, "initial_state": "N(0,%g)" % wl.h0_std,
+                       "l2": "state in + out (%.2f GB) larger than L2 (129 MB); no flush" % (nbytes / 1e9)},
+            "roofline": roof, "e2e": None, "cpu_baseline": cpu, "gpu_launches": 2 * K,
+            "clocks": clk.summary(), "source_sha": kernel_source_sha()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "decode":
+        run_decode(args)
     else:
         run_ours(args)
 

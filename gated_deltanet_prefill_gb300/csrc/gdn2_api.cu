@@ -54,12 +54,6 @@ size_t align_up(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 int64_t nc_max(const gdn2_dims &d) { return d.T_tot / kChunk + d.N; }
 
-bool shape_ok(const gdn2_dims &d) {
-    if (d.T_tot < 0 || d.N < 0 || d.H <= 0 || d.HV <= 0 || d.HV % d.H != 0) return false;
-    if (d.K != d.V || (d.K != 64 && d.K != 128)) return false;
-    if (nc_max(d) > (1ll << 30)) return false;
-    return true;
-}
 
 // Byte range [lo, hi) covered by a strided token-major tensor.
 struct Range {
@@ -91,6 +85,13 @@ bool strides_ok(const void *base, const int64_t *st, size_t esize, int heads, in
 }
 
 }  // namespace
+
+bool shape_ok(const gdn2_dims &d) {
+    if (d.T_tot < 0 || d.N < 0 || d.H <= 0 || d.HV <= 0 || d.HV % d.H != 0) return false;
+    if (d.K != d.V || (d.K != 64 && d.K != 128)) return false;
+    if (nc_max(d) > (1ll << 30)) return false;
+    return true;
+}
 
 WsLayout workspace_layout(const gdn2_dims &d) {
     WsLayout L;
@@ -169,13 +170,17 @@ size_t gdn2_workspace_bytes(const gdn2_dims *d) {
     return workspace_layout(*d).total;
 }
 
-gdn2_status gdn2_check_args(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                            const void *w, const float *initial_state, const void *cu_seqlens,
-                            const void *out, const float *final_state, const gdn2_dims *d,
-                            const void *workspace, size_t workspace_bytes) {
+}  // extern "C"
+
+namespace gdn2 {
+
+gdn2_status check_args(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                       const void *w, const float *initial_state, const void *cu_seqlens, const void *out,
+                       const float *final_state, const gdn2_dims *d, const void *workspace,
+                       size_t workspace_bytes, bool recurrent) {
     if (!d) return GDN2_ERR_NULL;
     if (d->dtype_qkv != GDN2_DTYPE_BF16 || d->dtype_g != GDN2_DTYPE_F32) return GDN2_ERR_DTYPE;
-    if (d->impl != GDN2_IMPL_TC && d->impl != GDN2_IMPL_SIMT) return GDN2_ERR_IMPL;
+    if (!recurrent && d->impl != GDN2_IMPL_TC && d->impl != GDN2_IMPL_SIMT) return GDN2_ERR_IMPL;
     if (!shape_ok(*d)) return GDN2_ERR_SHAPE;
     if (!cu_seqlens || !workspace) return GDN2_ERR_NULL;
     if (d->T_tot > 0 && (!q || !k || !v || !out)) return GDN2_ERR_NULL;
@@ -194,18 +199,46 @@ gdn2_status gdn2_check_args(const void *q, const void *k, const void *v, const v
     const size_t state_bytes = static_cast<size_t>(d->N) * d->HV * d->K * d->V * sizeof(float);
     const Range r_out = tensor_range(out, T, d->HV, d->V, d->o_stride, 2);
     const Range r_fs = flat_range(final_state, state_bytes);
+    // the recurrent call may update the state in place (the same pointer)
+    const bool in_place = recurrent && initial_state && initial_state == final_state;
     const Range ins[] = {
         tensor_range(q, T, d->H, d->K, d->q_stride, 2),     tensor_range(k, T, d->H, d->K, d->k_stride, 2),
         tensor_range(v, T, d->HV, d->V, d->v_stride, 2),    tensor_range(w, T, d->HV, d->V, d->w_stride, 2),
         tensor_range(beta, T, d->HV, d->K, d->beta_stride, 2), tensor_range(g, T, d->HV, d->K, d->g_stride, 4),
-        flat_range(initial_state, state_bytes),
         flat_range(cu_seqlens, (static_cast<size_t>(d->N) + 1) * (d->cu_seqlens_i64 ? 8 : 4)),
         flat_range(workspace, workspace_bytes)};
     for (const Range &r : ins)
         if (overlap(r_out, r) || overlap(r_fs, r)) return GDN2_ERR_ALIAS;
+    const Range r_is = flat_range(initial_state, state_bytes);
+    if (overlap(r_out, r_is) || (!in_place && overlap(r_fs, r_is))) return GDN2_ERR_ALIAS;
     if (overlap(r_out, r_fs)) return GDN2_ERR_ALIAS;
-    if (workspace_bytes < workspace_layout(*d).total) return GDN2_ERR_WORKSPACE;
+    const size_t need = recurrent ? kRecurrentWorkspaceBytes : workspace_layout(*d).total;
+    if (workspace_bytes < need) return GDN2_ERR_WORKSPACE;
     return GDN2_OK;
+}
+
+bool device_is_sm103(int *dev_out) {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (dev_out) *dev_out = dev;
+    return major == 10 && minor == 3;
+}
+
+}  // namespace gdn2
+
+extern "C" {
+
+gdn2_status gdn2_check_args(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                            const void *w, const float *initial_state, const void *cu_seqlens,
+                            const void *out, const float *final_state, const gdn2_dims *d,
+                            const void *workspace, size_t workspace_bytes) {
+    return check_args(q, k, v, g, beta, w, initial_state, cu_seqlens, out, final_state, d, workspace,
+                      workspace_bytes, false);
 }
 
 namespace {
@@ -223,14 +256,8 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
                                            d, workspace, workspace_bytes);
     if (st != GDN2_OK) return st;
     if (events && n_events < gdn2_num_stages(d) + 1) return GDN2_ERR_NULL;
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return GDN2_ERR_ARCH;
-    }
-    if (major != 10 || minor != 3) return GDN2_ERR_ARCH;
+    int dev = 0;
+    if (!device_is_sm103(&dev)) return GDN2_ERR_ARCH;
 
     const WsLayout L = workspace_layout(*d);
     char *ws = static_cast<char *>(workspace);

@@ -73,6 +73,21 @@ struct WsLayout {
 
 WsLayout workspace_layout(const gdn2_dims &d);
 
+// Workspace of the recurrent (decode) call: the status words only.
+constexpr size_t kRecurrentWorkspaceBytes = 64;
+
+// Host-side argument checks shared by the chunked and the recurrent calls
+// (the recurrent one allows initial_state == final_state and needs only
+// kRecurrentWorkspaceBytes of workspace).
+gdn2_status check_args(const void *q, const void *k, const void *v, const void *g, const void *beta,
+                       const void *w, const float *initial_state, const void *cu_seqlens, const void *out,
+                       const float *final_state, const gdn2_dims *d, const void *workspace,
+                       size_t workspace_bytes, bool recurrent);
+// True if the current device is compute capability 10.3 (its index in *dev).
+bool device_is_sm103(int *dev);
+// Shapes the library supports (K = V in {64, 128}, HV a multiple of H, ...).
+bool shape_ok(const gdn2_dims &d);
+
 __device__ __forceinline__ int64_t cu_at(const Params &p, int i) {
     return p.cu64 ? static_cast<const int64_t *>(p.cu)[i]
                   : static_cast<int64_t>(static_cast<const int32_t *>(p.cu)[i]);

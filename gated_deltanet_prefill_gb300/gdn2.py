@@ -27,7 +27,8 @@ DTYPE_BF16, DTYPE_F32 = 0, 2
 
 EXPORTS = ("gdn2_workspace_bytes", "gdn2_dims_init", "gdn2_check_args", "gdn2_chunk_fwd",
            "gdn2_chunk_fwd_staged", "gdn2_num_stages", "gdn2_stage_name", "gdn2_launch_count",
-           "gdn2_device_status", "gdn2_chunk_fwd_noalloc", "gdn2_status_string", "gdn2_version")
+           "gdn2_device_status", "gdn2_chunk_fwd_noalloc", "gdn2_recurrent_workspace_bytes",
+           "gdn2_recurrent_fwd", "gdn2_status_string", "gdn2_version")
 
 
 class Gdn2Error(RuntimeError):
@@ -88,6 +89,11 @@ def load(path: Optional[str] = None):
     lib.gdn2_chunk_fwd_noalloc.argtypes = [vp] * 6 + [ctypes.c_float, vp, vp, vp, vp,
                                                       ctypes.POINTER(Dims), vp]
     lib.gdn2_chunk_fwd_noalloc.restype = ctypes.c_int
+    lib.gdn2_recurrent_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+    lib.gdn2_recurrent_workspace_bytes.restype = sz
+    lib.gdn2_recurrent_fwd.argtypes = [vp] * 6 + [ctypes.c_float, vp, vp, vp, vp,
+                                                  ctypes.POINTER(Dims), vp, sz, vp]
+    lib.gdn2_recurrent_fwd.restype = ctypes.c_int
     lib.gdn2_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.gdn2_device_status.restype = ctypes.c_int
     lib.gdn2_status_string.argtypes = [ctypes.c_int]
@@ -210,6 +216,42 @@ def chunk_gdn2_fwd_noalloc(q, k, v, g=None, beta=None, w=None, scale=None, initi
                                     ctypes.byref(dims), stream)
     if st != GDN2_OK:
         raise Gdn2Error(st, "gdn2_chunk_fwd_noalloc")
+    return out, final_state
+
+
+def recurrent_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=None,
+                       cu_seqlens=None, output_final_state=True, use_qk_l2norm=False, out=None,
+                       final_state=None, workspace=None, stream=None):
+    """Token-by-token recurrence from a carried state through
+    ``gdn2_recurrent_fwd`` (decode steps, short continuations).  Same layouts
+    as ``chunk_gdn2_fwd``; ``final_state`` may be ``initial_state`` itself
+    (updated in place).  Returns (out, final_state)."""
+    lib = load()
+    if cu_seqlens is None:
+        raise ValueError("cu_seqlens is required (packed input only)")
+    for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens", cu_seqlens)):
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+    T, H, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty((T, HV, V), dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, HV, K, V), dtype=torch.float32, device=q.device)
+    if initial_state is not None and not initial_state.is_contiguous():
+        raise ValueError("initial_state must be contiguous [N, HV, K, V] fp32")
+    dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm)
+    if workspace is None:
+        workspace = torch.empty(256, dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    st = lib.gdn2_recurrent_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(w),
+                                ctypes.c_float(0.0 if scale is None else float(scale)),
+                                _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                ctypes.byref(dims), _ptr(workspace), workspace.numel(), stream)
+    if st != GDN2_OK:
+        raise Gdn2Error(st, "gdn2_recurrent_fwd")
     return out, final_state
 
 

@@ -101,6 +101,15 @@ def workload(index: int) -> Workload:
     raise ValueError(index)
 
 
+def decode_workload(batch: int = 128, tokens: int = 1) -> Workload:
+    """Decode steps from a carried state: ``batch`` sequences of ``tokens``
+    tokens each, H = HV = 32, K = V = 128, initial state N(0, 0.05)."""
+    return Workload("decode_B%d_T%d_H32_D128" % (batch, tokens), (tokens,) * batch, 32, 32, 128, 128,
+                    g_max=0.5, beta_max=2.0, h0_std=0.05, seed=6,
+                    description="%d sequences x %d token(s) from a carried state N(0,0.05), "
+                                "H=HV=32 K=V=128, g=-U(0,0.5), beta=U(0,2)" % (batch, tokens))
+
+
 def small(name: str, lens, H=2, HV=2, K=64, V=64, **kw) -> Workload:
     """A small ad-hoc workload for parity and edge-case tests."""
     return Workload(name, tuple(int(x) for x in lens), H, HV, K, V, **kw)

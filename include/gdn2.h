@@ -200,11 +200,41 @@ GDN2_API const char *gdn2_stage_name(const gdn2_dims *dims, int32_t i);
 GDN2_API int32_t gdn2_launch_count(const gdn2_dims *dims);
 
 /*
- * Read the device-side status that the last gdn2_chunk_fwd on this workspace
- * wrote into *status: GDN2_OK, GDN2_ERR_CU_SEQLENS, or GDN2_ERR_TIMEOUT (a
- * tensor-core kernel waited more than 2 s on one of its own barriers and
- * unwound; its outputs are then invalid).  This call SYNCHRONISES `stream`.
- * Returns GDN2_ERR_CUDA if the copy fails.
+ * Workspace bytes of gdn2_recurrent_fwd for `dims` (a 64-byte status area; 0
+ * if the shape is unsupported).  Host-only.
+ */
+GDN2_API size_t gdn2_recurrent_workspace_bytes(const gdn2_dims *dims);
+
+/*
+ * Token-by-token GDN-2 recurrence from a carried state: decode steps and short
+ * continuations of a prefill (FlashGDN-2 README quick start: prefill, then
+ * decode from the returned state).  Per token, the FlashInfer docs'
+ * recurrence (chunk_gated_delta_rule2, op description): decay by e^{g},
+ * erase read with beta, write with w, output after the write.
+ *
+ * Arguments, layouts, defaults and errors are those of gdn2_chunk_fwd, with
+ * two differences: `workspace` needs only gdn2_recurrent_workspace_bytes
+ * (the status words read by gdn2_device_status), and `final_state` may be the
+ * same pointer as `initial_state` (the state is updated in place; any other
+ * overlap is GDN2_ERR_ALIAS).  dims->impl is ignored.  Each token costs a
+ * pass over the state held on chip; the state is read and written once per
+ * call, so the call suits few tokens per sequence (gdn2_chunk_fwd is the
+ * prefill path).  Two launches: a cu_seqlens check, then one CTA per
+ * (sequence, value head, 32 value columns).
+ */
+GDN2_API gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void *v, const void *g,
+                                        const void *beta, const void *w, float scale,
+                                        const float *initial_state, const void *cu_seqlens, void *out,
+                                        float *final_state, const gdn2_dims *dims, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
+/*
+ * Read the device-side status that the last gdn2_chunk_fwd or
+ * gdn2_recurrent_fwd on this workspace wrote into *status: GDN2_OK,
+ * GDN2_ERR_CU_SEQLENS, or GDN2_ERR_TIMEOUT (a tensor-core kernel waited more
+ * than 2 s on one of its own barriers and unwound; its outputs are then
+ * invalid).  This call SYNCHRONISES `stream`.  Returns GDN2_ERR_CUDA if the
+ * copy fails.
  */
 GDN2_API gdn2_status gdn2_device_status(const void *workspace, void *stream, int32_t *status);
 

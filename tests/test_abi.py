@@ -150,3 +150,32 @@ def test_product_package_does_not_import_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle", src, re.M), f
                 assert "gdn2_oracle" not in src, f
+
+
+def _recurrent(lib, d, p, ws_bytes=64, **over):
+    p = {**p, **over}
+    return lib.gdn2_recurrent_fwd(p["q"], p["k"], p["v"], p["g"], p["beta"], p["w"], ctypes.c_float(0.0),
+                                  p["h0"], p["cu"], p["out"], p["hT"], ctypes.byref(d), p["ws"], ws_bytes, None)
+
+
+def test_recurrent_argument_checks(lib):
+    """gdn2_recurrent_fwd: a 64-byte workspace, the state may be updated in
+    place (same pointer), any other state overlap is refused; the checks run
+    before any CUDA call (without a device a valid call reports ERR_ARCH)."""
+    d = _dims(lib)
+    assert lib.gdn2_recurrent_workspace_bytes(ctypes.byref(d)) == 64
+    bad = _dims(lib)
+    bad.K = 96
+    assert lib.gdn2_recurrent_workspace_bytes(ctypes.byref(bad)) == 0
+    p = _ptrs(d, 64)
+    no_gpu = 6  # GDN2_ERR_ARCH: argument checks passed, no sm_103 device here
+    if torch.cuda.is_available():
+        pytest.skip("the valid-call cases would launch on this machine's GPU")
+    assert _recurrent(lib, d, p) == no_gpu
+    assert _recurrent(lib, d, p, hT=p["h0"]) == no_gpu          # in place
+    assert _recurrent(lib, d, p, hT=p["h0"] + 1024) == 4       # partial overlap: ERR_ALIAS
+    assert _recurrent(lib, d, p, ws_bytes=32) == 5              # ERR_WORKSPACE
+    assert _recurrent(lib, d, p, ws=0) == 1                      # ERR_NULL
+    assert _recurrent(lib, d, p, out=p["q"]) == 4                # out overlaps an input
+    # the chunked call keeps refusing an in-place state
+    assert _check(lib, d, p, hT=p["h0"]) == 4
