@@ -126,7 +126,7 @@ using namespace gdn2;
 
 extern "C" {
 
-int32_t gdn2_version(void) { return (1 << 16) | 0; }
+int32_t gdn2_version(void) { return (1 << 16) | 1; }
 
 const char *gdn2_status_string(int status) {
     switch (status) {
@@ -138,7 +138,7 @@ const char *gdn2_status_string(int status) {
         case GDN2_ERR_WORKSPACE: return "workspace missing or smaller than gdn2_workspace_bytes()";
         case GDN2_ERR_ARCH: return "current CUDA device is not compute capability 10.3 (sm_103a)";
         case GDN2_ERR_LAUNCH: return "kernel launch failed";
-        case GDN2_ERR_DTYPE: return "unsupported dtype (q/k/v/beta/w/out bf16, g fp32)";
+        case GDN2_ERR_DTYPE: return "unsupported dtype or layout (q/k/v/beta/w/out bf16 or fp16; g fp32, bf16 or fp16; states fp32 or bf16; the SIMT path: defaults only)";
         case GDN2_ERR_CU_SEQLENS: return "cu_seqlens invalid on the device (cu[0] != 0, decreasing, or cu[N] != T_tot)";
         case GDN2_ERR_CUDA: return "CUDA runtime error";
         case GDN2_ERR_IMPL: return "unknown implementation selector";
@@ -162,6 +162,8 @@ gdn2_status gdn2_dims_init(gdn2_dims *d, int64_t T_tot, int32_t N, int32_t H, in
     d->dtype_qkv = GDN2_DTYPE_BF16;
     d->dtype_g = GDN2_DTYPE_F32;
     d->impl = GDN2_IMPL_TC;
+    d->state_v_major = 0;
+    d->dtype_state = GDN2_DTYPE_F32;
     return shape_ok(*d) ? GDN2_OK : GDN2_ERR_SHAPE;
 }
 
@@ -175,19 +177,29 @@ size_t gdn2_workspace_bytes(const gdn2_dims *d) {
 namespace gdn2 {
 
 gdn2_status check_args(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                       const void *w, const float *initial_state, const void *cu_seqlens, const void *out,
-                       const float *final_state, const gdn2_dims *d, const void *workspace,
+                       const void *w, const void *initial_state, const void *cu_seqlens, const void *out,
+                       const void *final_state, const gdn2_dims *d, const void *workspace,
                        size_t workspace_bytes, bool recurrent) {
     if (!d) return GDN2_ERR_NULL;
-    if (d->dtype_qkv != GDN2_DTYPE_BF16 || d->dtype_g != GDN2_DTYPE_F32) return GDN2_ERR_DTYPE;
+    if (d->dtype_qkv != GDN2_DTYPE_BF16 && d->dtype_qkv != GDN2_DTYPE_F16) return GDN2_ERR_DTYPE;
+    if (d->dtype_g != GDN2_DTYPE_F32 && d->dtype_g != GDN2_DTYPE_BF16 && d->dtype_g != GDN2_DTYPE_F16)
+        return GDN2_ERR_DTYPE;
+    if (d->dtype_state != GDN2_DTYPE_F32 && d->dtype_state != GDN2_DTYPE_BF16) return GDN2_ERR_DTYPE;
+    if (d->state_v_major != 0 && d->state_v_major != 1) return GDN2_ERR_DTYPE;
     if (!recurrent && d->impl != GDN2_IMPL_TC && d->impl != GDN2_IMPL_SIMT) return GDN2_ERR_IMPL;
+    if (!recurrent && d->impl == GDN2_IMPL_SIMT &&
+        (d->dtype_qkv != GDN2_DTYPE_BF16 || d->dtype_g != GDN2_DTYPE_F32 || d->dtype_state != GDN2_DTYPE_F32 ||
+         d->state_v_major != 0))
+        return GDN2_ERR_DTYPE;  // the SIMT path supports the default dtypes and layout only
+    const size_t g_es = d->dtype_g == GDN2_DTYPE_F32 ? 4 : 2;
+    const size_t s_es = d->dtype_state == GDN2_DTYPE_F32 ? 4 : 2;
     if (!shape_ok(*d)) return GDN2_ERR_SHAPE;
     if (!cu_seqlens || !workspace) return GDN2_ERR_NULL;
     if (d->T_tot > 0 && (!q || !k || !v || !out)) return GDN2_ERR_NULL;
     const int64_t T = d->T_tot;
     if (!strides_ok(q, d->q_stride, 2, d->H, d->K) || !strides_ok(k, d->k_stride, 2, d->H, d->K) ||
         !strides_ok(v, d->v_stride, 2, d->HV, d->V) || !strides_ok(w, d->w_stride, 2, d->HV, d->V) ||
-        !strides_ok(beta, d->beta_stride, 2, d->HV, d->K) || !strides_ok(g, d->g_stride, 4, d->HV, d->K) ||
+        !strides_ok(beta, d->beta_stride, 2, d->HV, d->K) || !strides_ok(g, d->g_stride, g_es, d->HV, d->K) ||
         !strides_ok(out, d->o_stride, 2, d->HV, d->V))
         return GDN2_ERR_STRIDE;
     if ((initial_state && reinterpret_cast<uintptr_t>(initial_state) % 16) ||
@@ -196,7 +208,7 @@ gdn2_status check_args(const void *q, const void *k, const void *v, const void *
     // out rows must not overlap each other
     if (T > 0 && (d->o_stride[1] < d->V || d->o_stride[0] < static_cast<int64_t>(d->HV - 1) * d->o_stride[1] + d->V))
         return GDN2_ERR_ALIAS;
-    const size_t state_bytes = static_cast<size_t>(d->N) * d->HV * d->K * d->V * sizeof(float);
+    const size_t state_bytes = static_cast<size_t>(d->N) * d->HV * d->K * d->V * s_es;
     const Range r_out = tensor_range(out, T, d->HV, d->V, d->o_stride, 2);
     const Range r_fs = flat_range(final_state, state_bytes);
     // the recurrent call may update the state in place (the same pointer)
@@ -204,7 +216,7 @@ gdn2_status check_args(const void *q, const void *k, const void *v, const void *
     const Range ins[] = {
         tensor_range(q, T, d->H, d->K, d->q_stride, 2),     tensor_range(k, T, d->H, d->K, d->k_stride, 2),
         tensor_range(v, T, d->HV, d->V, d->v_stride, 2),    tensor_range(w, T, d->HV, d->V, d->w_stride, 2),
-        tensor_range(beta, T, d->HV, d->K, d->beta_stride, 2), tensor_range(g, T, d->HV, d->K, d->g_stride, 4),
+        tensor_range(beta, T, d->HV, d->K, d->beta_stride, 2), tensor_range(g, T, d->HV, d->K, d->g_stride, g_es),
         flat_range(cu_seqlens, (static_cast<size_t>(d->N) + 1) * (d->cu_seqlens_i64 ? 8 : 4)),
         flat_range(workspace, workspace_bytes)};
     for (const Range &r : ins)
@@ -234,8 +246,8 @@ bool device_is_sm103(int *dev_out) {
 extern "C" {
 
 gdn2_status gdn2_check_args(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                            const void *w, const float *initial_state, const void *cu_seqlens,
-                            const void *out, const float *final_state, const gdn2_dims *d,
+                            const void *w, const void *initial_state, const void *cu_seqlens,
+                            const void *out, const void *final_state, const gdn2_dims *d,
                             const void *workspace, size_t workspace_bytes) {
     return check_args(q, k, v, g, beta, w, initial_state, cu_seqlens, out, final_state, d, workspace,
                       workspace_bytes, false);
@@ -249,7 +261,7 @@ const char *const kTcStages[] = {"chunk_map", "intra", "state_output"};
 constexpr int kNumTcStages = 3;
 
 gdn2_status run(const void *q, const void *k, const void *v, const void *g, const void *beta, const void *w,
-                float scale, const float *initial_state, const void *cu_seqlens, void *out, float *final_state,
+                float scale, const void *initial_state, const void *cu_seqlens, void *out, void *final_state,
                 const gdn2_dims *d, void *workspace, size_t workspace_bytes, void *stream,
                 void *const *events, int32_t n_events) {
     const gdn2_status st = gdn2_check_args(q, k, v, g, beta, w, initial_state, cu_seqlens, out, final_state,
@@ -281,6 +293,10 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d->K));
     p.has_g = g != nullptr; p.has_beta = beta != nullptr; p.has_w = w != nullptr;
     p.l2norm = d->use_qk_l2norm ? 1 : 0;
+    p.in_f16 = d->dtype_qkv == GDN2_DTYPE_F16;
+    p.g_dtype = d->dtype_g;
+    p.state_vmajor = d->state_v_major;
+    p.state_bf16 = d->dtype_state == GDN2_DTYPE_BF16;
     p.NCmax = static_cast<int>(d->T_tot / kChunk + d->N);
     p.status = reinterpret_cast<int *>(ws + L.status);
     p.chunk_seq = reinterpret_cast<int *>(ws + L.chunk_seq);
@@ -310,20 +326,23 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     if (d->impl == GDN2_IMPL_TC) {
         const char *rows = getenv("GDN2_ROW_COPIES");
         const bool force_rows = rows && rows[0] == '1';
+        // 16-bit inputs: the maps only move bytes, so fp16 and bf16 share them
+        const CUtensorMapDataType t16 =
+            p.in_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const CUtensorMapDataType tg = d->dtype_g == GDN2_DTYPE_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : d->dtype_g == GDN2_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const int64_t g_es = d->dtype_g == GDN2_DTYPE_F32 ? 4 : 2;
         p.tmap = !force_rows &&
-                 (!p.has_g || encode_rows(&p.tm_g, &p.tm_order_g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, d->K,
-                                          d->HV, d->T_tot, p.sg_t, p.sg_h)) &&
-                 encode_rows(&p.tm_v, &p.tm_order_v, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->V, d->HV,
-                             d->T_tot, p.sv_t, p.sv_h) &&
-                 (!p.has_w || encode_rows(&p.tm_w, &p.tm_order_w, w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->V,
-                                          d->HV, d->T_tot, p.sw_t, p.sw_h));
+                 (!p.has_g || encode_rows(&p.tm_g, &p.tm_order_g, g, tg, g_es, d->K, d->HV, d->T_tot, p.sg_t,
+                                          p.sg_h)) &&
+                 encode_rows(&p.tm_v, &p.tm_order_v, v, t16, 2, d->V, d->HV, d->T_tot, p.sv_t, p.sv_h) &&
+                 (!p.has_w || encode_rows(&p.tm_w, &p.tm_order_w, w, t16, 2, d->V, d->HV, d->T_tot, p.sw_t, p.sw_h));
         p.tpre = p.tmap &&
-                 encode_rows(&p.tm_k, &p.tm_order_k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->K, d->H,
-                             d->T_tot, p.sk_t, p.sk_h) &&
-                 encode_rows(&p.tm_q, &p.tm_order_q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d->K, d->H,
-                             d->T_tot, p.sq_t, p.sq_h) &&
-                 (!p.has_beta || encode_rows(&p.tm_b, &p.tm_order_b, beta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                                             d->K, d->HV, d->T_tot, p.sb_t, p.sb_h));
+                 encode_rows(&p.tm_k, &p.tm_order_k, k, t16, 2, d->K, d->H, d->T_tot, p.sk_t, p.sk_h) &&
+                 encode_rows(&p.tm_q, &p.tm_order_q, q, t16, 2, d->K, d->H, d->T_tot, p.sq_t, p.sq_h) &&
+                 (!p.has_beta ||
+                  encode_rows(&p.tm_b, &p.tm_order_b, beta, t16, 2, d->K, d->HV, d->T_tot, p.sb_t, p.sb_h));
     }
     p.q_in = p.q; p.k_in = p.k;
     p.sq_in_t = p.sq_t; p.sq_in_h = p.sq_h; p.sk_in_t = p.sk_t; p.sk_in_h = p.sk_h;
@@ -389,16 +408,16 @@ int32_t gdn2_launch_count(const gdn2_dims *d) {
 }
 
 gdn2_status gdn2_chunk_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                           const void *w, float scale, const float *initial_state, const void *cu_seqlens,
-                           void *out, float *final_state, const gdn2_dims *d, void *workspace,
+                           const void *w, float scale, const void *initial_state, const void *cu_seqlens,
+                           void *out, void *final_state, const gdn2_dims *d, void *workspace,
                            size_t workspace_bytes, void *stream) {
     return run(q, k, v, g, beta, w, scale, initial_state, cu_seqlens, out, final_state, d, workspace,
                workspace_bytes, stream, nullptr, 0);
 }
 
 gdn2_status gdn2_chunk_fwd_staged(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                                  const void *w, float scale, const float *initial_state, const void *cu_seqlens,
-                                  void *out, float *final_state, const gdn2_dims *d, void *workspace,
+                                  const void *w, float scale, const void *initial_state, const void *cu_seqlens,
+                                  void *out, void *final_state, const gdn2_dims *d, void *workspace,
                                   size_t workspace_bytes, void *stream, void *const *events, int32_t n_events) {
     if (!events) return GDN2_ERR_NULL;
     return run(q, k, v, g, beta, w, scale, initial_state, cu_seqlens, out, final_state, d, workspace,

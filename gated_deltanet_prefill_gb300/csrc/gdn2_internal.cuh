@@ -4,6 +4,7 @@
 
 #include <cuda.h>  // CUtensorMap
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,15 +29,18 @@ struct Params {
     int64_t sq_in_t, sq_in_h, sk_in_t, sk_in_h;
     const float *g;
     int64_t sq_t, sq_h, sk_t, sk_h, sv_t, sv_h, sg_t, sg_h, sb_t, sb_h, sw_t, sw_h, so_t, so_h;
-    bf16 *o;
-    const float *h0;
-    float *hT;
+    bf16 *o;                    // dtype of the inputs (in_f16: the bits are fp16)
+    const void *h0;             // states: fp32 or bf16 (state_bf16), [K][V] per
+    void *hT;                   // (sequence, value head) or [V][K] (state_vmajor)
     const void *cu;
     int cu64;
     int64_t T_tot;
     int N, H, HV, K, V, group;  // group = HV / H
     float scale;
     int has_g, has_beta, has_w, l2norm;
+    int in_f16;                 // q, k, v, beta, w, out are fp16 (else bf16)
+    int g_dtype;                // gdn2_dtype of g
+    int state_vmajor, state_bf16;
     int NCmax;                  // upper bound on the chunk count: T_tot/64 + N
     // ---- workspace ----
     int *status;                // [0] cu_seqlens status, [1] chunk count NC, [2] wait timeout
@@ -80,13 +84,39 @@ constexpr size_t kRecurrentWorkspaceBytes = 64;
 // (the recurrent one allows initial_state == final_state and needs only
 // kRecurrentWorkspaceBytes of workspace).
 gdn2_status check_args(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                       const void *w, const float *initial_state, const void *cu_seqlens, const void *out,
-                       const float *final_state, const gdn2_dims *d, const void *workspace,
+                       const void *w, const void *initial_state, const void *cu_seqlens, const void *out,
+                       const void *final_state, const gdn2_dims *d, const void *workspace,
                        size_t workspace_bytes, bool recurrent);
 // True if the current device is compute capability 10.3 (its index in *dev).
 bool device_is_sm103(int *dev);
 // Shapes the library supports (K = V in {64, 128}, HV a multiple of H, ...).
 bool shape_ok(const gdn2_dims &d);
+
+// One element of a 16-bit input (bf16, or fp16 when f16) as fp32.
+__device__ __forceinline__ float in_ld(const bf16 *base, int64_t i, bool f16) {
+    const unsigned short b = reinterpret_cast<const unsigned short *>(base)[i];
+    return f16 ? __half2float(__ushort_as_half(b)) : __bfloat162float(__ushort_as_bfloat16(b));
+}
+// One element of g (fp32, bf16 or fp16) as fp32.
+__device__ __forceinline__ float g_ld(const float *base, int64_t i, int dtype) {
+    if (dtype == GDN2_DTYPE_F32) return base[i];
+    const unsigned short b = reinterpret_cast<const unsigned short *>(base)[i];
+    return dtype == GDN2_DTYPE_F16 ? __half2float(__ushort_as_half(b)) : __bfloat162float(__ushort_as_bfloat16(b));
+}
+// Offset of element (key channel c, value channel j) in one (sequence, head)
+// state block: [K][V] (K-major) or [V][K] (V-major).
+__device__ __forceinline__ size_t state_off(int c, int j, int K, int V, bool vmajor) {
+    return vmajor ? static_cast<size_t>(j) * K + c : static_cast<size_t>(c) * V + j;
+}
+__device__ __forceinline__ float state_ld(const void *base, size_t i, bool is_bf16) {
+    return is_bf16 ? __bfloat162float(static_cast<const bf16 *>(base)[i]) : static_cast<const float *>(base)[i];
+}
+__device__ __forceinline__ void state_st(void *base, size_t i, float x, bool is_bf16) {
+    if (is_bf16)
+        static_cast<bf16 *>(base)[i] = __float2bfloat16_rn(x);
+    else
+        static_cast<float *>(base)[i] = x;
+}
 
 __device__ __forceinline__ int64_t cu_at(const Params &p, int i) {
     return p.cu64 ? static_cast<const int64_t *>(p.cu)[i]

@@ -40,8 +40,8 @@ void *scratch_address(int dev) {
 
 extern "C" gdn2_status gdn2_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *g,
                                              const void *beta, const void *w, float scale,
-                                             const float *initial_state, const void *cu_seqlens, void *out,
-                                             float *final_state, const gdn2_dims *dims, void *stream) {
+                                             const void *initial_state, const void *cu_seqlens, void *out,
+                                             void *final_state, const gdn2_dims *dims, void *stream) {
     if (!dims) return GDN2_ERR_NULL;
     if (gdn2_workspace_bytes(dims) > static_cast<size_t>(GDN2_NOALLOC_SCRATCH_BYTES))
         return GDN2_ERR_NOALLOC_LIMIT;

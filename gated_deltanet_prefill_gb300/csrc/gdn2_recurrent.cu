@@ -28,15 +28,16 @@ struct RecParams {
     const bf16 *q, *k, *v, *beta, *w;
     const float *g;
     int64_t sq_t, sq_h, sk_t, sk_h, sv_t, sv_h, sg_t, sg_h, sb_t, sb_h, sw_t, sw_h, so_t, so_h;
-    bf16 *o;
-    const float *h0;
-    float *hT;
+    bf16 *o;          // at the inputs' dtype
+    const void *h0;   // fp32 or bf16, [K][V] or [V][K] per (sequence, head)
+    void *hT;
     const void *cu;
     int cu64;
     int64_t T_tot;
     int N, HV, group;
     float scale;
     int has_g, has_beta, has_w, l2norm;
+    int in_f16, g_dtype, state_vmajor, state_bf16;
     int *status;  // [0] cu_seqlens status, [1] 0, [2] 0
 };
 
@@ -77,13 +78,12 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
     float S[32];
 #pragma unroll
     for (int r = 0; r < 32; ++r)
-        S[r] = p.h0 ? p.h0[sbase + static_cast<size_t>(32 * wp + r) * K + j] : 0.f;
+        S[r] = p.h0 ? state_ld(p.h0, sbase + state_off(32 * wp + r, j, K, K, p.state_vmajor), p.state_bf16) : 0.f;
     for (int64_t t = t0; t < t1; ++t) {
-        float kc = __bfloat162float(p.k[t * p.sk_t + static_cast<int64_t>(h) * p.sk_h + tid]);
-        float qc = __bfloat162float(p.q[t * p.sq_t + static_cast<int64_t>(h) * p.sq_h + tid]);
-        const float bc =
-            p.has_beta ? __bfloat162float(p.beta[t * p.sb_t + static_cast<int64_t>(hv) * p.sb_h + tid]) : 1.f;
-        const float gc = p.has_g ? p.g[t * p.sg_t + static_cast<int64_t>(hv) * p.sg_h + tid] : 0.f;
+        float kc = in_ld(p.k, t * p.sk_t + static_cast<int64_t>(h) * p.sk_h + tid, p.in_f16);
+        float qc = in_ld(p.q, t * p.sq_t + static_cast<int64_t>(h) * p.sq_h + tid, p.in_f16);
+        const float bc = p.has_beta ? in_ld(p.beta, t * p.sb_t + static_cast<int64_t>(hv) * p.sb_h + tid, p.in_f16) : 1.f;
+        const float gc = p.has_g ? g_ld(p.g, t * p.sg_t + static_cast<int64_t>(hv) * p.sg_h + tid, p.g_dtype) : 0.f;
         float a0 = kc * kc, a1 = qc * qc, a2 = qc * kc;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
             kc *= ik; qc *= iq; qk *= ik * iq;
         }
         s_k[tid] = kc; s_bk[tid] = bc * kc; s_q[tid] = qc; s_eg[tid] = expf(gc);
-        const float vj = __bfloat162float(p.v[t * p.sv_t + static_cast<int64_t>(hv) * p.sv_h + j]);
-        const float wj = p.has_w ? __bfloat162float(p.w[t * p.sw_t + static_cast<int64_t>(hv) * p.sw_h + j]) : 1.f;
+        const float vj = in_ld(p.v, t * p.sv_t + static_cast<int64_t>(hv) * p.sv_h + j, p.in_f16);
+        const float wj = p.has_w ? in_ld(p.w, t * p.sw_t + static_cast<int64_t>(hv) * p.sw_h + j, p.in_f16) : 1.f;
         __syncthreads();
         float pr = 0.f, po = 0.f;
 #pragma unroll
@@ -118,13 +118,20 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
         const float u = wj * vj - rj;
 #pragma unroll
         for (int r = 0; r < 32; ++r) S[r] += s_k[32 * wp + r] * u;
-        if (wp == 0)
-            p.o[t * p.so_t + static_cast<int64_t>(hv) * p.so_h + j] = __float2bfloat16_rn(p.scale * (oj + qk * u));
+        if (wp == 0) {  // o at the inputs' dtype
+            const float ov = p.scale * (oj + qk * u);
+            const int64_t oi = t * p.so_t + static_cast<int64_t>(hv) * p.so_h + j;
+            if (p.in_f16)
+                reinterpret_cast<__half *>(p.o)[oi] = __float2half_rn(ov);
+            else
+                p.o[oi] = __float2bfloat16_rn(ov);
+        }
         __syncthreads();
     }
     if (p.hT) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) p.hT[sbase + static_cast<size_t>(32 * wp + r) * K + j] = S[r];
+        for (int r = 0; r < 32; ++r)
+            state_st(p.hT, sbase + state_off(32 * wp + r, j, K, K, p.state_vmajor), S[r], p.state_bf16);
     }
 }
 
@@ -142,8 +149,8 @@ size_t gdn2_recurrent_workspace_bytes(const gdn2_dims *d) {
 }
 
 gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void *v, const void *g, const void *beta,
-                               const void *w, float scale, const float *initial_state, const void *cu_seqlens,
-                               void *out, float *final_state, const gdn2_dims *d, void *workspace,
+                               const void *w, float scale, const void *initial_state, const void *cu_seqlens,
+                               void *out, void *final_state, const gdn2_dims *d, void *workspace,
                                size_t workspace_bytes, void *stream) {
     const gdn2_status st = check_args(q, k, v, g, beta, w, initial_state, cu_seqlens, out, final_state, d,
                                       workspace, workspace_bytes, true);
@@ -178,6 +185,10 @@ gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void *v, cons
     p.has_beta = beta != nullptr;
     p.has_w = w != nullptr;
     p.l2norm = d->use_qk_l2norm ? 1 : 0;
+    p.in_f16 = d->dtype_qkv == GDN2_DTYPE_F16;
+    p.g_dtype = d->dtype_g;
+    p.state_vmajor = d->state_v_major;
+    p.state_bf16 = d->dtype_state == GDN2_DTYPE_BF16;
     p.status = static_cast<int *>(workspace);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);

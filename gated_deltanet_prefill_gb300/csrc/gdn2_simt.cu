@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(D) gdn2_simt_state_kernel(Params p) {
     float S[VT];
     const size_t sbase = ((static_cast<size_t>(n) * p.HV + hv) * D + c) * D + v0;
 #pragma unroll
-    for (int j = 0; j < VT; ++j) S[j] = p.h0 ? p.h0[sbase + j] : 0.f;
+    for (int j = 0; j < VT; ++j) S[j] = p.h0 ? static_cast<const float *>(p.h0)[sbase + j] : 0.f;  // fp32, K-major
 
     const int first = p.seq_first[n], last = p.seq_first[n + 1];
     for (int ck = first; ck < last; ++ck) {
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(D) gdn2_simt_state_kernel(Params p) {
     }
     if (p.hT) {
 #pragma unroll
-        for (int j = 0; j < VT; ++j) p.hT[sbase + j] = S[j];
+        for (int j = 0; j < VT; ++j) static_cast<float *>(p.hT)[sbase + j] = S[j];
     }
 }
 

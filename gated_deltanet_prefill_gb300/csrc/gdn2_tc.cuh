@@ -263,6 +263,11 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
     return r;
 }
+// a -> low half, IEEE round-to-nearest (overflow gives inf, as a cast would)
+__device__ __forceinline__ uint32_t pack_f16_rn(float a, float b) {
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
 __device__ __forceinline__ float2 unpack_h2(uint32_t x) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&x));
 }
@@ -278,6 +283,24 @@ __device__ __forceinline__ uint4 pack8_h(const float (&f)[8]) {
 }
 __device__ __forceinline__ uint4 pack8_bf(const float (&f)[8]) {
     return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));
+}
+// eight fp16 values of a 16-byte chunk
+__device__ __forceinline__ void unpack8_f16(const uint4 &u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 a = unpack_h2(w[i]);
+        f[2 * i] = a.x;
+        f[2 * i + 1] = a.y;
+    }
+}
+// eight 16-bit inputs (fp16 when f16, else bf16)
+__device__ __forceinline__ void unpack8_bf(const uint4 &u, float (&f)[8]);
+__device__ __forceinline__ void unpack8_in(const uint4 &u, float (&f)[8], bool f16) {
+    if (f16)
+        unpack8_f16(u, f);
+    else
+        unpack8_bf(u, f);
 }
 __device__ __forceinline__ void unpack8_bf(const uint4 &u, float (&f)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};

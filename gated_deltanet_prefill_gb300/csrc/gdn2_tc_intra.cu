@@ -91,7 +91,9 @@ struct IntraCfg {
 
 __device__ __forceinline__ uint4 ldg16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
 
-template <int D>
+// F16: q, k, v, beta, w are fp16 (else bf16); a template parameter so that the
+// operand-image loop carries no dtype branch
+template <int D, bool F16>
 __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const __grid_constant__ Params p) {
     using C = IntraCfg<D>;
     constexpr int NJ = D / 32;         // 8-channel chunks per thread
@@ -150,19 +152,25 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         const int t0 = static_cast<int>(nstart);
         tma_load_3d(dst, map, 0, order ? t0 : hh, order ? hh : t0, bar);
     };
+    // g rows: fp32 straight into the G scratch; 16-bit g into its upper half
+    // (converted by the prefix-sum warps)
+    const uint32_t g_es = p.g_dtype == GDN2_DTYPE_F32 ? 4u : 2u;
+    uint8_t *g_dst = reinterpret_cast<uint8_t *>(Gs) + (g_es == 4u ? 0u : 64u * D * 2u);
     auto stage_g = [&]() {  // warp 7
         if (p.tmap) {
             if (lane == 0) {
-                mbar_arrive_expect_tx(&bar_g, p.has_g ? 64u * D * 4 : 0u);
-                if (p.has_g) tile(Gs, &p.tm_g, p.tm_order_g, nhv, &bar_g);
+                mbar_arrive_expect_tx(&bar_g, p.has_g ? 64u * D * g_es : 0u);
+                if (p.has_g) tile(g_dst, &p.tm_g, p.tm_order_g, nhv, &bar_g);
             }
             return;
         }
         const uint32_t rows = p.has_g ? static_cast<uint32_t>(nlen) : 0u;
-        if (lane == 0) mbar_arrive_expect_tx(&bar_g, rows * D * 4);
+        if (lane == 0) mbar_arrive_expect_tx(&bar_g, rows * D * g_es);
         __syncwarp();
+        const uint8_t *gb = reinterpret_cast<const uint8_t *>(p.g);
         for (uint32_t r = lane; r < rows; r += 32)
-            bulk_g2s(Gs + r * D, p.g + (nstart + r) * p.sg_t + static_cast<int64_t>(nhv) * p.sg_h, D * 4, &bar_g);
+            bulk_g2s(g_dst + r * D * g_es,
+                     gb + ((nstart + r) * p.sg_t + static_cast<int64_t>(nhv) * p.sg_h) * g_es, D * g_es, &bar_g);
     };
     auto stage_vw = [&]() {  // warp 2
         if (p.tmap) {
@@ -214,6 +222,31 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         const int ch = lt % D, part = lt / D;
         float *base = Gs + part * R4 * D + ch;
         float acc = 0.f;
+        if (g_es == 2u) {
+            // 16-bit g in the upper half of the scratch: rows in blocks of 8 are
+            // read, then (after a barrier) written back as fp32 prefix sums; the
+            // fp32 rows of block b overwrite only 16-bit rows <= 8b + 7
+            const unsigned short *g16 = reinterpret_cast<const unsigned short *>(g_dst);
+            const bool gf16 = p.g_dtype == GDN2_DTYPE_F16;
+#pragma unroll 1
+            for (int b = 0; b < 8; ++b) {
+                float x[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int row = 8 * b + k;
+                    const unsigned short u = lt < D && row < glen ? g16[row * D + lt] : 0;
+                    x[k] = gf16 ? __half2float(__ushort_as_half(u)) : __bfloat162float(__ushort_as_bfloat16(u));
+                }
+                named_sync(1, 128);
+                if (lt < D) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        acc += __fmul_rn(x[k], kLog2e);
+                        Gs[(8 * b + k) * D + lt] = acc;
+                    }
+                }
+            }
+        } else {
 #pragma unroll 1
         for (int r8 = 0; r8 < R4; r8 += 8) {
             float *b8 = base + r8 * D;
@@ -224,7 +257,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
                 b8[k * D] = acc;
             }
         }
-        if (P4 > 1) {
+        }
+        if (P4 > 1 && g_es == 4u) {
             float *tot = reinterpret_cast<float *>(sm + C::oTab);  // [P4][D], before the tables
             tot[part * D + ch] = acc;
             named_sync(1, 128);
@@ -291,8 +325,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
 #pragma unroll
             for (int j = 0; j < NJ; ++j) {
                 float a[8], b[8];
-                unpack8_bf(ldg16(kp + 8 * (seg + 4 * j)), a);
-                unpack8_bf(ldg16(qp + 8 * (seg + 4 * j)), b);
+                unpack8_in(ldg16(kp + 8 * (seg + 4 * j)), a, F16);
+                unpack8_in(ldg16(qp + 8 * (seg + 4 * j)), b, F16);
 #pragma unroll
                 for (int x = 0; x < 8; ++x) {
                     sk += a[x] * a[x];
@@ -318,8 +352,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     for (int j = 0; j < NJ; ++j) {
         const int cb = 8 * (seg + 4 * j);
         float vv[8], ww[8];
-        unpack8_bf(live ? *reinterpret_cast<const uint4 *>(raw_v + (t * D + cb) * 2) : z4, vv);
-        unpack8_bf(live && p.has_w ? *reinterpret_cast<const uint4 *>(raw_w + (t * D + cb) * 2) : z4, ww);
+        unpack8_in(live ? *reinterpret_cast<const uint4 *>(raw_v + (t * D + cb) * 2) : z4, vv, F16);
+        unpack8_in(live && p.has_w ? *reinterpret_cast<const uint4 *>(raw_w + (t * D + cb) * 2) : z4, ww, F16);
 #pragma unroll
         for (int x = 0; x < 8; ++x) ww[x] = (p.has_w || !live) ? ww[x] * vv[x] : vv[x];
         wX2[j] = pack8_h(ww);
@@ -345,9 +379,9 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     for (int j = 0; j < NJ; ++j) {
         const int cb = 8 * (seg + 4 * j);
         float kk[8], qq[8], bb[8];
-        unpack8_bf(nk, kk);
-        unpack8_bf(nq, qq);
-        unpack8_bf(nb, bb);
+        unpack8_in(nk, kk, F16);
+        unpack8_in(nq, qq, F16);
+        unpack8_in(nb, bb, F16);
         if (!p.has_beta && live) {
 #pragma unroll
             for (int x = 0; x < 8; ++x) bb[x] = 1.f;
@@ -670,10 +704,10 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_intra(const Params &p, cudaStream_t s) {
     using C = IntraCfg<D>;
-    auto kern = gdn2_tc_intra_kernel<D>;
+    auto kern = gdn2_tc_intra_kernel<D, F16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -691,7 +725,8 @@ cudaError_t launch_intra(const Params &p, cudaStream_t s) {
 size_t tc_record_bytes(int D) { return D == 64 ? Rec<64>::bytes : Rec<128>::bytes; }
 
 cudaError_t launch_tc_intra(const Params &p, cudaStream_t s) {
-    return p.K == 64 ? launch_intra<64>(p, s) : launch_intra<128>(p, s);
+    if (p.K == 64) return p.in_f16 ? launch_intra<64, true>(p, s) : launch_intra<64, false>(p, s);
+    return p.in_f16 ? launch_intra<128, true>(p, s) : launch_intra<128, false>(p, s);
 }
 
 }  // namespace gdn2

@@ -170,16 +170,27 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
         const bool active = row < D && grp < VT / 32;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         const int j0 = grp, j1 = grp + 1;
+        const size_t sblk = (static_cast<size_t>(n) * p.HV + hv) * D * D;  // this (sequence, head) block
+        const bool plain = !p.state_vmajor && !p.state_bf16;           // fp32 [K][V]
         if (active) {
-            const float *h0 = p.h0 ? p.h0 + ((static_cast<size_t>(n) * p.HV + hv) * D + row) * D + v0 : nullptr;
 #pragma unroll 1
             for (int j = j0; j < j1; ++j) {
                 uint32_t r[32];
+                if (p.h0 && plain) {
+                    const float *h0 = static_cast<const float *>(p.h0) + sblk + static_cast<size_t>(row) * D + v0;
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    float4 x = h0 ? *reinterpret_cast<const float4 *>(h0 + 32 * j + e) : make_float4(0, 0, 0, 0);
-                    r[e] = __float_as_uint(x.x); r[e + 1] = __float_as_uint(x.y);
-                    r[e + 2] = __float_as_uint(x.z); r[e + 3] = __float_as_uint(x.w);
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(h0 + 32 * j + e);
+                        r[e] = __float_as_uint(x.x); r[e + 1] = __float_as_uint(x.y);
+                        r[e + 2] = __float_as_uint(x.z); r[e + 3] = __float_as_uint(x.w);
+                    }
+                } else {  // zero, bf16 or V-major: element by element (lanes = consecutive rows)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        r[e] = __float_as_uint(
+                            p.h0 ? state_ld(p.h0, sblk + state_off(row, v0 + 32 * j + e, D, D, p.state_vmajor),
+                                            p.state_bf16)
+                                 : 0.f);
                 }
                 tmem_st32(tS + lane_base + 32 * j, r);
             }
@@ -228,17 +239,24 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
         }
         tc_fence_after();
         if (ok && active && p.hT) {
-            float *hT = p.hT + ((static_cast<size_t>(n) * p.HV + hv) * D + row) * D + v0;
 #pragma unroll 1
             for (int j = j0; j < j1; ++j) {
                 uint32_t r[32];
                 tmem_ld32(tS + lane_base + 32 * j, r);
                 tmem_ld_wait();
+                if (plain) {
+                    float *hT = static_cast<float *>(p.hT) + sblk + static_cast<size_t>(row) * D + v0;
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4 *>(hT + 32 * j + e) =
-                        make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
-                                    __uint_as_float(r[e + 3]));
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(hT + 32 * j + e) =
+                            make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                        __uint_as_float(r[e + 3]));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        state_st(p.hT, sblk + state_off(row, v0 + 32 * j + e, D, D, p.state_vmajor),
+                                 __uint_as_float(r[e]), p.state_bf16);
+                }
             }
         }
     } else if (warp == 4 || warp == 5) {
@@ -267,10 +285,16 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         uint4 v;
-                        v.x = pack_bf2(__uint_as_float(r[8 * cc + 0]) * p.scale, __uint_as_float(r[8 * cc + 1]) * p.scale);
-                        v.y = pack_bf2(__uint_as_float(r[8 * cc + 2]) * p.scale, __uint_as_float(r[8 * cc + 3]) * p.scale);
-                        v.z = pack_bf2(__uint_as_float(r[8 * cc + 4]) * p.scale, __uint_as_float(r[8 * cc + 5]) * p.scale);
-                        v.w = pack_bf2(__uint_as_float(r[8 * cc + 6]) * p.scale, __uint_as_float(r[8 * cc + 7]) * p.scale);
+                        // output at the inputs' dtype (plain round-to-nearest)
+                        auto pk = [&](int e) {
+                            const float a = __uint_as_float(r[8 * cc + e]) * p.scale;
+                            const float b = __uint_as_float(r[8 * cc + e + 1]) * p.scale;
+                            return p.in_f16 ? pack_f16_rn(a, b) : pack_bf2(a, b);
+                        };
+                        v.x = pk(0);
+                        v.y = pk(2);
+                        v.z = pk(4);
+                        v.w = pk(6);
                         reinterpret_cast<uint4 *>(orow + 32 * j)[cc] = v;
                     }
                 }

@@ -23,7 +23,8 @@ STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_STRIDE", 4: "ERR
                 13: "ERR_NOALLOC_LIMIT"}
 NOALLOC_SCRATCH_BYTES = 64 << 20
 IMPL = {"tc": 0, "simt": 1}
-DTYPE_BF16, DTYPE_F32 = 0, 2
+DTYPE_BF16, DTYPE_F16, DTYPE_F32 = 0, 1, 2
+_DTYPE_CODE = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16, torch.float32: DTYPE_F32}
 
 EXPORTS = ("gdn2_workspace_bytes", "gdn2_dims_init", "gdn2_check_args", "gdn2_chunk_fwd",
            "gdn2_chunk_fwd_staged", "gdn2_num_stages", "gdn2_stage_name", "gdn2_launch_count",
@@ -47,6 +48,7 @@ class Dims(ctypes.Structure):
                 ("o_stride", ctypes.c_int64 * 2), ("dtype_qkv", ctypes.c_int32),
                 ("dtype_g", ctypes.c_int32), ("cu_seqlens_i64", ctypes.c_int32),
                 ("use_qk_l2norm", ctypes.c_int32), ("impl", ctypes.c_int32),
+                ("state_v_major", ctypes.c_int32), ("dtype_state", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
 
 
@@ -124,7 +126,8 @@ def _strides(t, name):
     return (t.stride(0), t.stride(1))
 
 
-def make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm=False, impl="tc") -> Dims:
+def make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm=False, impl="tc", state_v_major=False,
+              state_dtype=torch.float32) -> Dims:
     T, H, K = q.shape
     HV, V = v.shape[1], v.shape[2]
     d = Dims()
@@ -132,15 +135,28 @@ def make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm=False, impl="t
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("w", w), ("o", out)):
         s = _strides(t, name)
         getattr(d, name + "_stride")[0], getattr(d, name + "_stride")[1] = s
-    d.dtype_qkv = DTYPE_BF16 if q.dtype == torch.bfloat16 else 99
-    d.dtype_g = DTYPE_F32 if (g is None or g.dtype == torch.float32) else 99
-    for t in (k, v, beta, w):
+    # q, k, v, beta, w, out share one 16-bit dtype; anything else is refused
+    d.dtype_qkv = _DTYPE_CODE.get(q.dtype, 99) if q.dtype != torch.float32 else 99
+    for t in (k, v, beta, w, out):
         if t is not None and t.dtype != q.dtype:
             d.dtype_qkv = 99
+    d.dtype_g = DTYPE_F32 if g is None else _DTYPE_CODE.get(g.dtype, 99)
+    d.state_v_major = 1 if state_v_major else 0
+    d.dtype_state = _DTYPE_CODE.get(state_dtype, 99) if state_dtype != torch.float16 else 99
     d.cu_seqlens_i64 = 1 if cu_seqlens.dtype == torch.int64 else 0
     d.use_qk_l2norm = 1 if use_qk_l2norm else 0
     d.impl = IMPL[impl]
     return d
+
+
+def _state_dtype(initial_state, final_state, state_dtype):
+    """dtype of the states: the one given, else that of the tensors passed, else fp32."""
+    ts = [t.dtype for t in (initial_state, final_state) if t is not None]
+    if state_dtype is None:
+        state_dtype = ts[0] if ts else torch.float32
+    if any(x != state_dtype for x in ts):
+        raise ValueError("initial_state and final_state must have the same dtype (%s)" % state_dtype)
+    return state_dtype
 
 
 def workspace_bytes(dims: Dims) -> int:
@@ -149,7 +165,8 @@ def workspace_bytes(dims: Dims) -> int:
 
 def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=None,
                    cu_seqlens=None, output_final_state=True, use_qk_l2norm=False, out=None,
-                   final_state=None, workspace=None, impl="tc", stream=None, stage_events=None):
+                   final_state=None, workspace=None, impl="tc", stream=None, stage_events=None,
+                   state_v_major=False, state_dtype=None):
     """GDN-2 chunked prefill forward through ``gdn2_chunk_fwd``.
 
     Packed layout (FlashInfer docs, chunk_gated_delta_rule2): q, k [T, H, K];
@@ -168,11 +185,12 @@ def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state
     N = cu_seqlens.numel() - 1
     if out is None:
         out = torch.empty((T, HV, V), dtype=q.dtype, device=q.device)
+    sdt = _state_dtype(initial_state, final_state, state_dtype)
     if final_state is None and output_final_state:
-        final_state = torch.empty((N, HV, K, V), dtype=torch.float32, device=q.device)
+        final_state = torch.empty((N, HV, K, V), dtype=sdt, device=q.device)
     if initial_state is not None and not initial_state.is_contiguous():
         raise ValueError("initial_state must be contiguous [N, HV, K, V] fp32")
-    dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, impl)
+    dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, impl, state_v_major, sdt)
     nbytes = workspace_bytes(dims)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
@@ -194,7 +212,7 @@ def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state
 
 def chunk_gdn2_fwd_noalloc(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=None,
                            cu_seqlens=None, output_final_state=True, use_qk_l2norm=False, out=None,
-                           final_state=None, impl="tc", stream=None):
+                           final_state=None, impl="tc", stream=None, state_v_major=False, state_dtype=None):
     """The forward through ``gdn2_chunk_fwd_noalloc``: no workspace argument;
     the library's fixed device scratch (NOALLOC_SCRATCH_BYTES) is used, so
     calls must not overlap on the GPU.  Outputs are allocated here only when
@@ -205,9 +223,10 @@ def chunk_gdn2_fwd_noalloc(q, k, v, g=None, beta=None, w=None, scale=None, initi
     N = cu_seqlens.numel() - 1
     if out is None:
         out = torch.empty((T, HV, V), dtype=q.dtype, device=q.device)
+    sdt = _state_dtype(initial_state, final_state, state_dtype)
     if final_state is None and output_final_state:
-        final_state = torch.empty((N, HV, K, V), dtype=torch.float32, device=q.device)
-    dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, impl)
+        final_state = torch.empty((N, HV, K, V), dtype=sdt, device=q.device)
+    dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, impl, state_v_major, sdt)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     st = lib.gdn2_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(w),
@@ -221,7 +240,7 @@ def chunk_gdn2_fwd_noalloc(q, k, v, g=None, beta=None, w=None, scale=None, initi
 
 def recurrent_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=None,
                        cu_seqlens=None, output_final_state=True, use_qk_l2norm=False, out=None,
-                       final_state=None, workspace=None, stream=None):
+                       final_state=None, workspace=None, stream=None, state_v_major=False, state_dtype=None):
     """Token-by-token recurrence from a carried state through
     ``gdn2_recurrent_fwd`` (decode steps, short continuations).  Same layouts
     as ``chunk_gdn2_fwd``; ``final_state`` may be ``initial_state`` itself
@@ -237,11 +256,12 @@ def recurrent_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_s
     N = cu_seqlens.numel() - 1
     if out is None:
         out = torch.empty((T, HV, V), dtype=q.dtype, device=q.device)
+    sdt = _state_dtype(initial_state, final_state, state_dtype)
     if final_state is None and output_final_state:
-        final_state = torch.empty((N, HV, K, V), dtype=torch.float32, device=q.device)
+        final_state = torch.empty((N, HV, K, V), dtype=sdt, device=q.device)
     if initial_state is not None and not initial_state.is_contiguous():
         raise ValueError("initial_state must be contiguous [N, HV, K, V] fp32")
-    dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm)
+    dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, "tc", state_v_major, sdt)
     if workspace is None:
         workspace = torch.empty(256, dtype=torch.uint8, device=q.device)
     if stream is None:

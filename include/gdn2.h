@@ -67,6 +67,7 @@ typedef enum gdn2_status {
 
 typedef enum gdn2_dtype {
     GDN2_DTYPE_BF16 = 0,
+    GDN2_DTYPE_F16 = 1,
     GDN2_DTYPE_F32 = 2
 } gdn2_dtype;
 
@@ -83,14 +84,21 @@ typedef enum gdn2_impl {
  * to be contiguous").  Strides are in ELEMENTS of that tensor's dtype and,
  * like base pointers, must be multiples of 16 bytes.
  *
- *   q, k          [T_tot, H,  K]   bf16
- *   v, w          [T_tot, HV, V]   bf16
- *   g             [T_tot, HV, K]   fp32  (natural-log decay, <= 0)
- *   beta          [T_tot, HV, K]   bf16  (erase gate, post-sigmoid; [0, 2] allowed)
- *   out           [T_tot, HV, V]   bf16
- *   initial_state [N, HV, K, V]    fp32, contiguous, K-major (row c = key channel)
- *   final_state   [N, HV, K, V]    fp32, contiguous
+ *   q, k          [T_tot, H,  K]   dtype_qkv (bf16 or fp16)
+ *   v, w          [T_tot, HV, V]   dtype_qkv
+ *   g             [T_tot, HV, K]   dtype_g: fp32, bf16 or fp16 (natural-log decay, <= 0)
+ *   beta          [T_tot, HV, K]   dtype_qkv (erase gate, post-sigmoid; [0, 2] allowed)
+ *   out           [T_tot, HV, V]   dtype_qkv
+ *   initial_state [N, HV, K, V]    dtype_state (fp32 or bf16), contiguous, K-major
+ *                                  (row c = key channel); [N, HV, V, K] when
+ *                                  state_v_major = 1 (the FlashInfer docs' layout)
+ *   final_state   same dtype and layout as initial_state
  *   cu_seqlens    [N + 1]          int32 (or int64 with cu_seqlens_i64 = 1)
+ *
+ * (FlashInfer docs, chunk_gated_delta_rule2 parameters: q/k/v fp16 or bf16,
+ * beta and w read at q's dtype, g fp32/bf16/fp16, state fp32 or bf16.)  The
+ * SIMT implementation supports only the defaults (bf16, fp32 g, fp32 K-major
+ * state); other combinations with impl = GDN2_IMPL_SIMT are GDN2_ERR_DTYPE.
  *
  * Supported sizes: K = V in {64, 128}; HV a positive multiple of H; N >= 0;
  * T_tot >= 0 (T_tot = 0 writes only final_state = initial_state).
@@ -100,13 +108,15 @@ typedef struct gdn2_dims {
     int32_t N, H, HV, K, V;
     int64_t q_stride[2], k_stride[2], v_stride[2], g_stride[2];
     int64_t beta_stride[2], w_stride[2], o_stride[2];
-    int32_t dtype_qkv;      /* GDN2_DTYPE_BF16                                    */
-    int32_t dtype_g;        /* GDN2_DTYPE_F32                                     */
+    int32_t dtype_qkv;      /* GDN2_DTYPE_BF16 or GDN2_DTYPE_F16 (q, k, v, beta, w, out) */
+    int32_t dtype_g;        /* GDN2_DTYPE_F32, GDN2_DTYPE_BF16 or GDN2_DTYPE_F16  */
     int32_t cu_seqlens_i64; /* 0: int32 cu_seqlens, 1: int64                      */
     int32_t use_qk_l2norm;  /* 1: divide q, k rows by max(||x||_2, 1e-12) first   */
                             /* (FlashInfer docs: use_qk_l2norm_in_kernel)         */
     int32_t impl;           /* gdn2_impl                                          */
-    int32_t reserved;
+    int32_t state_v_major;  /* 0: states [N, HV, K, V]; 1: [N, HV, V, K]          */
+    int32_t dtype_state;    /* GDN2_DTYPE_F32 or GDN2_DTYPE_BF16                  */
+    int32_t reserved;       /* 0                                                  */
 } gdn2_dims;
 
 /*
@@ -120,7 +130,7 @@ GDN2_API size_t gdn2_workspace_bytes(const gdn2_dims *dims);
 /*
  * Fill `dims` for contiguous tensors of the given sizes (strides = packed
  * row-major), dtype_qkv = bf16, dtype_g = fp32, int32 cu_seqlens, no L2
- * norm, impl = GDN2_IMPL_TC.  Host-only.
+ * norm, impl = GDN2_IMPL_TC, fp32 K-major states.  Host-only.
  */
 GDN2_API gdn2_status gdn2_dims_init(gdn2_dims *dims, int64_t T_tot, int32_t N, int32_t H, int32_t HV,
                            int32_t K, int32_t V);
@@ -131,8 +141,8 @@ GDN2_API gdn2_status gdn2_dims_init(gdn2_dims *dims, int64_t T_tot, int32_t N, i
  * Host-only; returns the status gdn2_chunk_fwd would return before launching.
  */
 GDN2_API gdn2_status gdn2_check_args(const void *q, const void *k, const void *v, const void *g,
-                            const void *beta, const void *w, const float *initial_state,
-                            const void *cu_seqlens, const void *out, const float *final_state,
+                            const void *beta, const void *w, const void *initial_state,
+                            const void *cu_seqlens, const void *out, const void *final_state,
                             const gdn2_dims *dims, const void *workspace,
                             size_t workspace_bytes);
 
@@ -168,8 +178,8 @@ GDN2_API gdn2_status gdn2_check_args(const void *q, const void *k, const void *v
  */
 GDN2_API gdn2_status gdn2_chunk_fwd(const void *q, const void *k, const void *v, const void *g,
                            const void *beta, const void *w, float scale,
-                           const float *initial_state, const void *cu_seqlens, void *out,
-                           float *final_state, const gdn2_dims *dims, void *workspace,
+                           const void *initial_state, const void *cu_seqlens, void *out,
+                           void *final_state, const gdn2_dims *dims, void *workspace,
                            size_t workspace_bytes, void *stream);
 
 /*
@@ -182,8 +192,8 @@ GDN2_API gdn2_status gdn2_chunk_fwd(const void *q, const void *k, const void *v,
  */
 GDN2_API gdn2_status gdn2_chunk_fwd_staged(const void *q, const void *k, const void *v, const void *g,
                                            const void *beta, const void *w, float scale,
-                                           const float *initial_state, const void *cu_seqlens,
-                                           void *out, float *final_state, const gdn2_dims *dims,
+                                           const void *initial_state, const void *cu_seqlens,
+                                           void *out, void *final_state, const gdn2_dims *dims,
                                            void *workspace, size_t workspace_bytes, void *stream,
                                            void *const *events, int32_t n_events);
 
@@ -224,8 +234,8 @@ GDN2_API size_t gdn2_recurrent_workspace_bytes(const gdn2_dims *dims);
  */
 GDN2_API gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void *v, const void *g,
                                         const void *beta, const void *w, float scale,
-                                        const float *initial_state, const void *cu_seqlens, void *out,
-                                        float *final_state, const gdn2_dims *dims, void *workspace,
+                                        const void *initial_state, const void *cu_seqlens, void *out,
+                                        void *final_state, const gdn2_dims *dims, void *workspace,
                                         size_t workspace_bytes, void *stream);
 
 /*
@@ -274,8 +284,8 @@ GDN2_API gdn2_status gdn2_device_status(const void *workspace, void *stream, int
  */
 GDN2_API gdn2_status gdn2_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *g,
                                             const void *beta, const void *w, float scale,
-                                            const float *initial_state, const void *cu_seqlens, void *out,
-                                            float *final_state, const gdn2_dims *dims, void *stream);
+                                            const void *initial_state, const void *cu_seqlens, void *out,
+                                            void *final_state, const gdn2_dims *dims, void *stream);
 
 /* Static, human-readable text for a status code.  Host-only. */
 GDN2_API const char *gdn2_status_string(int status);

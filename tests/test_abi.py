@@ -99,11 +99,20 @@ def test_check_args_errors(lib):
     assert _check(lib, d, p, out=p["hT"]) == 4
     # optional gates may be NULL
     assert _check(lib, d, p, g=None, beta=None, w=None, h0=None, hT=None) == 0
-    for field, val, code in (("K", 96, 2), ("HV", 3, 2), ("N", -1, 2), ("dtype_qkv", 1, 8),
-                             ("dtype_g", 0, 8), ("impl", 7, 11)):
+    for field, val, code in (("K", 96, 2), ("HV", 3, 2), ("N", -1, 2), ("dtype_qkv", 2, 8),
+                             ("dtype_qkv", 7, 8), ("dtype_g", 7, 8), ("dtype_state", 1, 8),
+                             ("state_v_major", 2, 8), ("impl", 7, 11)):
         d2 = _dims(lib)
         setattr(d2, field, val)
         assert _check(lib, d2, p, ws_bytes=1 << 30) == code, field
+    # the variants the FlashInfer docs list: fp16 inputs, bf16/fp16 g, bf16 and
+    # V-major states (tensor-core path); the SIMT path keeps the defaults
+    for field, val in (("dtype_qkv", 1), ("dtype_g", 0), ("dtype_g", 1), ("dtype_state", 0), ("state_v_major", 1)):
+        d2 = _dims(lib)
+        setattr(d2, field, val)
+        assert _check(lib, d2, p, ws_bytes=1 << 30) == 0, field
+        d2.impl = 1
+        assert _check(lib, d2, p, ws_bytes=1 << 30) == 8, field
     d3 = _dims(lib)
     d3.q_stride[0] = 2 * 64 + 4                           # 264 bytes: not a multiple of 16
     assert _check(lib, d3, p) == 3
