@@ -299,40 +299,96 @@ def launch_count(dims: Dims) -> int:
 class HostRunner:
     """End-to-end call from HOST buffers: pinned host inputs are copied to
     preallocated device buffers, the forward runs, and the output and final
-    state are copied back into pinned host buffers, all on one stream.  The
-    device buffers and workspace are allocated once (torch) and reused."""
+    state are copied back into pinned host buffers.  The sequences are taken
+    in contiguous groups (at most ``groups``, balanced by tokens): the
+    host-to-device copy of group i + 1, the forward of group i and the
+    device-to-host copy of group i - 1 run on three streams at once, so the
+    call is bounded by the host link rather than by the kernels.  The caller's
+    stream waits for the last copy.  Device buffers and the workspace are
+    allocated once (torch) and reused."""
 
-    def __init__(self, host: dict, impl="tc", use_qk_l2norm=False, output_final_state=True):
+    def __init__(self, host: dict, impl="tc", use_qk_l2norm=False, output_final_state=True, groups=4):
         self.host = host
         self.impl = impl
         self.l2 = use_qk_l2norm
         self.dev = {k: (torch.empty_like(v, device="cuda") if torch.is_tensor(v) else v)
                     for k, v in host.items()}
         T, HV, V = host["v"].shape
-        N = host["cu_seqlens"].numel() - 1
+        cu = [int(x) for x in host["cu_seqlens"].tolist()]
+        N = len(cu) - 1
         K = host["q"].shape[2]
+        sdt = host["h0"].dtype if host.get("h0") is not None else torch.float32
         self.out_host = torch.empty((T, HV, V), dtype=host["q"].dtype).pin_memory()
-        self.fs_host = (torch.empty((N, HV, K, V), dtype=torch.float32).pin_memory()
-                        if output_final_state else None)
+        self.fs_host = (torch.empty((N, HV, K, V), dtype=sdt).pin_memory() if output_final_state else None)
         self.out = torch.empty((T, HV, V), dtype=host["q"].dtype, device="cuda")
-        self.fs = torch.empty((N, HV, K, V), dtype=torch.float32, device="cuda") if output_final_state else None
+        self.fs = torch.empty((N, HV, K, V), dtype=sdt, device="cuda") if output_final_state else None
         dims = make_dims(self.dev["q"], self.dev["k"], self.dev["v"], self.dev["g"], self.dev["beta"],
-                         self.dev["w"], self.out, self.dev["cu_seqlens"], use_qk_l2norm, impl)
+                         self.dev["w"], self.out, self.dev["cu_seqlens"], use_qk_l2norm, impl, False, sdt)
         self.ws = torch.empty(max(workspace_bytes(dims), 256), dtype=torch.uint8, device="cuda")
+        # contiguous sequence groups with about T / groups tokens each
+        n_groups = max(1, min(groups, N))
+        bounds, n = [0], 0
+        for gi in range(1, n_groups):
+            target = cu[-1] * gi / n_groups
+            while n < N - (n_groups - gi) and cu[n + 1] <= target:
+                n += 1
+            n = max(n, bounds[-1] + 1)
+            bounds.append(n)
+        bounds.append(N)
+        self.bounds = sorted(set(bounds))
+        cu_dt = host["cu_seqlens"].dtype
+        self.cu_host = [torch.empty(b - a + 1, dtype=cu_dt).pin_memory()
+                        for a, b in zip(self.bounds[:-1], self.bounds[1:])]
+        self.cu_dev = [torch.empty_like(c, device="cuda") for c in self.cu_host]
+        self.cu_ev = [None] * len(self.cu_host)  # last copy out of each pinned cu buffer
+        self.streams = [torch.cuda.Stream() for _ in range(3)]
         self.h2d_bytes = sum(v.numel() * v.element_size() for v in host.values() if torch.is_tensor(v))
         self.d2h_bytes = self.out_host.numel() * self.out_host.element_size() + (
-            0 if self.fs_host is None else self.fs_host.numel() * 4)
+            0 if self.fs_host is None else self.fs_host.numel() * self.fs_host.element_size())
 
     def __call__(self):
-        for k, v in self.host.items():
-            if torch.is_tensor(v):
-                self.dev[k].copy_(v, non_blocking=True)
-        d = self.dev
-        chunk_gdn2_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d.get("scale"),
-                       initial_state=d.get("h0"), cu_seqlens=d["cu_seqlens"],
-                       use_qk_l2norm=self.l2, out=self.out, final_state=self.fs,
-                       output_final_state=self.fs is not None, workspace=self.ws, impl=self.impl)
-        self.out_host.copy_(self.out, non_blocking=True)
-        if self.fs is not None:
-            self.fs_host.copy_(self.fs, non_blocking=True)
+        s_in, s_cmp, s_out = self.streams
+        caller = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(caller)
+        for st in self.streams:
+            st.wait_event(start)
+        h, d = self.host, self.dev
+        cu = h["cu_seqlens"]
+        for gi, (n0, n1) in enumerate(zip(self.bounds[:-1], self.bounds[1:])):
+            t0, t1 = int(cu[n0]), int(cu[n1])
+            # the group's cu_seqlens, rebased to its first token (host arithmetic);
+            # the previous call's copy out of this pinned buffer must be done
+            if self.cu_ev[gi] is not None:
+                self.cu_ev[gi].synchronize()
+            torch.sub(cu[n0:n1 + 1], cu[n0], out=self.cu_host[gi])
+            with torch.cuda.stream(s_in):
+                for key in ("q", "k", "v", "g", "beta", "w"):
+                    if torch.is_tensor(h.get(key)):
+                        d[key][t0:t1].copy_(h[key][t0:t1], non_blocking=True)
+                if torch.is_tensor(h.get("h0")):
+                    d["h0"][n0:n1].copy_(h["h0"][n0:n1], non_blocking=True)
+                self.cu_dev[gi].copy_(self.cu_host[gi], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+                self.cu_ev[gi] = ev_in
+            s_cmp.wait_event(ev_in)
+            with torch.cuda.stream(s_cmp):
+                sl = lambda key: d[key][t0:t1] if torch.is_tensor(d.get(key)) else None
+                chunk_gdn2_fwd(sl("q"), sl("k"), sl("v"), sl("g"), sl("beta"), sl("w"), scale=d.get("scale"),
+                               initial_state=d["h0"][n0:n1] if torch.is_tensor(d.get("h0")) else None,
+                               cu_seqlens=self.cu_dev[gi], use_qk_l2norm=self.l2, out=self.out[t0:t1],
+                               final_state=None if self.fs is None else self.fs[n0:n1],
+                               output_final_state=self.fs is not None, workspace=self.ws, impl=self.impl,
+                               stream=s_cmp.cuda_stream)
+                ev_c = torch.cuda.Event()
+                ev_c.record(s_cmp)
+            s_out.wait_event(ev_c)
+            with torch.cuda.stream(s_out):
+                self.out_host[t0:t1].copy_(self.out[t0:t1], non_blocking=True)
+                if self.fs is not None:
+                    self.fs_host[n0:n1].copy_(self.fs[n0:n1], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(s_out)
+        caller.wait_event(done)
         return self.out_host, self.fs_host
