@@ -93,6 +93,37 @@ bool shape_ok(const gdn2_dims &d) {
     return true;
 }
 
+// Segments of the chunk-parallel state pass.  The chain of a sequence's
+// chunks is cut into P segments; the price is a transition pass over K + V
+// columns (2 x 128-column tiles per segment but the last), a combine of P - 1
+// steps and a replay pass.  P is the minimum of a time model per chunk of the
+// longest pass, counted in waves of a GB300's 152 SMs (one CTA per SM):
+// 2.2 us for a 64-column tile, 2.3 us for a transition tile, 3.1 us for a
+// 128-column tile, 8 us per combine step and 10 us per launch, measured on
+// the tensor-core state kernel.  Segments keep at least 8 chunks.
+int scan_segments(const gdn2_dims &d) {
+    if (d.impl != GDN2_IMPL_TC || d.K != 128 || d.V != 128 || d.N <= 0) return 1;
+    if (d.state_segments > 0) return d.state_segments;
+    constexpr int64_t kWave = 152;
+    const int64_t units = static_cast<int64_t>(d.N) * d.HV;
+    const int64_t chunks = d.T_tot / (static_cast<int64_t>(kChunk) * d.N);  // mean per sequence
+    auto waves = [](int64_t ctas) { return static_cast<double>((ctas + kWave - 1) / kWave); };
+    auto pass = [&](int64_t P) {  // one state pass over P segments per (sequence, head)
+        return 2 * units * P <= kWave ? 2.2 * waves(2 * units * P) : 3.1 * waves(units * P);
+    };
+    double best = 10.0 + chunks * pass(1);
+    int best_P = 1;
+    for (int64_t P = 2; P <= 16 && chunks >= 8 * P; ++P) {
+        const double L = static_cast<double>((chunks + P - 1) / P);
+        const double t = 3 * 10.0 + 8.0 * (P - 1) + L * (2.3 * waves(2 * units * (P - 1)) + pass(P));
+        if (t < best) {
+            best = t;
+            best_P = static_cast<int>(P);
+        }
+    }
+    return best_P;
+}
+
 WsLayout workspace_layout(const gdn2_dims &d) {
     WsLayout L;
     memset(&L, 0, sizeof(L));
@@ -115,6 +146,12 @@ WsLayout workspace_layout(const gdn2_dims &d) {
     } else {
         off = (off + 1023) & ~static_cast<size_t>(1023);  // records are 1 KB aligned
         L.rec = take(NC * d.HV * tc_record_bytes(d.K));
+        const size_t P = static_cast<size_t>(scan_segments(d));
+        if (P > 1) {
+            const size_t units = static_cast<size_t>(d.N) * (P - 1) * d.HV;
+            L.sc_tr = take(units * d.K * (d.K + d.V) * 4);
+            L.sc_si = take(units * d.K * d.V * 4);
+        }
     }
     L.total = off;
     return L;
@@ -186,6 +223,9 @@ gdn2_status check_args(const void *q, const void *k, const void *v, const void *
         return GDN2_ERR_DTYPE;
     if (d->dtype_state != GDN2_DTYPE_F32 && d->dtype_state != GDN2_DTYPE_BF16) return GDN2_ERR_DTYPE;
     if (d->state_v_major != 0 && d->state_v_major != 1) return GDN2_ERR_DTYPE;
+    if (d->state_segments < 0 || d->state_segments > 64) return GDN2_ERR_SHAPE;
+    if (!recurrent && d->state_segments > 1 && (d->impl != GDN2_IMPL_TC || d->K != 128 || d->V != 128))
+        return GDN2_ERR_SHAPE;  // the chunk-parallel state pass: tensor-core path, K = V = 128
     if (!recurrent && d->impl != GDN2_IMPL_TC && d->impl != GDN2_IMPL_SIMT) return GDN2_ERR_IMPL;
     if (!recurrent && d->impl == GDN2_IMPL_SIMT &&
         (d->dtype_qkv != GDN2_DTYPE_BF16 || d->dtype_g != GDN2_DTYPE_F32 || d->dtype_state != GDN2_DTYPE_F32 ||
@@ -314,11 +354,15 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     // State-kernel V tile: V columns of S evolve independently, so splitting V
     // is exact.  Two 64-column tiles per (sequence, head) when the untiled
     // grid would leave more than half of the SMs idle.
+    p.sc_P = d->impl == GDN2_IMPL_TC ? scan_segments(*d) : 1;
+    p.sc_mode = 0;
+    p.sc_tr = p.sc_P > 1 ? reinterpret_cast<float *>(ws + L.sc_tr) : nullptr;
+    p.sc_si = p.sc_P > 1 ? reinterpret_cast<float *>(ws + L.sc_si) : nullptr;
     p.vtile = d->K;
     if (d->K == 128) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-            2ll * d->N * d->HV <= sms)
+            2ll * d->N * d->HV * p.sc_P <= sms)
             p.vtile = 64;
     }
     // tensor maps for the intra kernel's g / v / w tiles (GDN2_ROW_COPIES=1
@@ -365,7 +409,18 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
         mark();
         if (p.N > 0 && launch_tc_intra(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
         mark();
-        if (p.N > 0 && launch_tc_state(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+        if (p.N > 0 && p.sc_P > 1) {  // chunk-parallel: transitions, combine, replay
+            Params pt = p;
+            pt.sc_mode = 1;
+            pt.vtile = 128;
+            if (launch_tc_state(pt, s) != cudaSuccess || launch_tc_scan_combine(p, s) != cudaSuccess)
+                return GDN2_ERR_LAUNCH;
+            Params pr = p;
+            pr.sc_mode = 2;
+            if (launch_tc_state(pr, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
+        } else if (p.N > 0 && launch_tc_state(p, s) != cudaSuccess) {
+            return GDN2_ERR_LAUNCH;
+        }
         mark();
     } else {
         if (p.N > 0 && launch_prep(p, s) != cudaSuccess) return GDN2_ERR_LAUNCH;
@@ -397,7 +452,8 @@ int32_t gdn2_launch_count(const gdn2_dims *d) {
     if (!d || !shape_ok(*d)) return 0;
     if (d->N == 0) return 1;
     const int64_t ncmax = nc_max(*d);
-    if (d->impl != GDN2_IMPL_SIMT) return 1 + (ncmax > 0 ? 1 : 0) + 1;  // map, intra, state
+    if (d->impl != GDN2_IMPL_SIMT)  // map, intra, state (+ transitions and combine when segmented)
+        return 1 + (ncmax > 0 ? 1 : 0) + 1 + (scan_segments(*d) > 1 ? 2 : 0);
     int n = 1;                                          // chunk map
     n += (d->use_qk_l2norm && d->T_tot > 0) ? 1 : 0;    // q/k L2 norm
     n += ncmax > 0 ? 1 : 0;                             // cumsum

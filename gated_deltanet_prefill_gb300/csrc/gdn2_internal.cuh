@@ -55,6 +55,13 @@ struct Params {
     bf16 *vnew;                 // [T_tot, HV, V]  u_t (v_new) per token
     uint8_t *rec;               // [NCmax, HV] records of the tensor-core path
     int vtile;                  // V columns per state CTA (tensor-core path)
+    // chunk-parallel state pass (tensor-core path, K = V = 128): each sequence's
+    // chunks in sc_P segments.  sc_mode 0: one sequential pass (sc_P = 1);
+    // 1: segment transitions [M | B] of S_out = M S_in + B for segments
+    // 0 .. P-2 into sc_tr [N, P-1, HV, K, K+V]; 2: every segment from its
+    // incoming state (h0, or sc_si [N, P-1, HV, K, V] from the combine kernel)
+    int sc_P, sc_mode;
+    float *sc_tr, *sc_si;
     // TMA tensor maps over the rows of g, v, w (tensor-core intra kernel): a
     // box is 64 tokens x D channels of one head.  tm_order = 0: coordinates
     // (channel, head, token); 1: (channel, token, head).  tmap = 0: the maps
@@ -71,7 +78,7 @@ struct Params {
 
 // Workspace layout (byte offsets), a function of the problem only.
 struct WsLayout {
-    size_t status, chunk_seq, chunk_len, chunk_start, seq_first, G, qn, kn, Wt, Ut, hbuf, vnew, rec;
+    size_t status, chunk_seq, chunk_len, chunk_start, seq_first, G, qn, kn, Wt, Ut, hbuf, vnew, rec, sc_tr, sc_si;
     size_t total;
 };
 
@@ -131,6 +138,9 @@ cudaError_t launch_simt_state(const Params &p, cudaStream_t s);
 cudaError_t launch_simt_output(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_intra(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_state(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_scan_combine(const Params &p, cudaStream_t s);
+// Segments per sequence of the chunk-parallel state pass for `d` (1 = none).
+int scan_segments(const gdn2_dims &d);
 size_t tc_record_bytes(int D);
 
 }  // namespace gdn2

@@ -65,8 +65,21 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
 
     if (p.status[0] != GDN2_OK) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int n = blockIdx.x, hv = blockIdx.y, v0 = blockIdx.z * VT;
-    const int first = p.seq_first[n], nck = p.seq_first[n + 1] - first;
+    // blockIdx.x = (sequence, segment); the segment's chunks are
+    // [seg L, seg L + L) of the sequence's, L = ceil(chunks / segments).  In the
+    // transition pass (sc_mode 1) blockIdx.z tiles the K + V columns of [M | B]:
+    // M columns start from the identity and take no Ut (S_out = M S_in + B).
+    const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
+    const int P = p.sc_mode == 0 ? 1 : p.sc_P;
+    const int n = blockIdx.x / segs, seg = blockIdx.x % segs, hv = blockIdx.y;
+    const bool trans = p.sc_mode == 1;
+    const int col0 = blockIdx.z * VT;               // first column of this tile
+    const bool is_m = trans && col0 < D;            // a tile of M
+    const int v0 = trans ? (is_m ? 0 : col0 - D) : col0;
+    const int seq0 = p.seq_first[n], nck_all = p.seq_first[n + 1] - seq0;
+    const int L = (nck_all + P - 1) / P;
+    const int c_lo = min(seg * L, nck_all), c_hi = min(c_lo + L, nck_all);
+    const int first = seq0 + c_lo, nck = c_hi - c_lo;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -172,11 +185,26 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
         const int j0 = grp, j1 = grp + 1;
         const size_t sblk = (static_cast<size_t>(n) * p.HV + hv) * D * D;  // this (sequence, head) block
         const bool plain = !p.state_vmajor && !p.state_bf16;           // fp32 [K][V]
+        // a later segment of the replay pass starts from the combined state
+        const float *si = p.sc_mode == 2 && seg > 0
+                              ? p.sc_si + ((static_cast<size_t>(n) * (P - 1) + seg - 1) * p.HV + hv) * D * D
+                              : nullptr;
         if (active) {
 #pragma unroll 1
             for (int j = j0; j < j1; ++j) {
                 uint32_t r[32];
-                if (p.h0 && plain) {
+                if (trans) {  // [I | 0]
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(is_m && row == col0 + 32 * j + e ? 1.f : 0.f);
+                } else if (si) {
+                    const float *src = si + static_cast<size_t>(row) * D + v0 + 32 * j;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(src + e);
+                        r[e] = __float_as_uint(x.x); r[e + 1] = __float_as_uint(x.y);
+                        r[e + 2] = __float_as_uint(x.z); r[e + 3] = __float_as_uint(x.w);
+                    }
+                } else if (p.h0 && plain) {
                     const float *h0 = static_cast<const float *>(p.h0) + sblk + static_cast<size_t>(row) * D + v0;
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
@@ -238,13 +266,25 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             ok = false;
         }
         tc_fence_after();
-        if (ok && active && p.hT) {
+        // final state: the transition pass writes [M | B]; the replay pass only
+        // from the last segment
+        const bool write_final = trans || (p.hT && (p.sc_mode != 2 || seg == P - 1));
+        if (ok && active && write_final) {
 #pragma unroll 1
             for (int j = j0; j < j1; ++j) {
                 uint32_t r[32];
                 tmem_ld32(tS + lane_base + 32 * j, r);
                 tmem_ld_wait();
-                if (plain) {
+                if (trans) {
+                    float *tr = p.sc_tr +
+                                ((static_cast<size_t>(n) * (P - 1) + seg) * p.HV + hv) * D * (2 * D) +
+                                static_cast<size_t>(row) * (2 * D) + col0 + 32 * j;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(tr + e) =
+                            make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                        __uint_as_float(r[e + 3]));
+                } else if (plain) {
                     float *hT = static_cast<float *>(p.hT) + sblk + static_cast<size_t>(row) * D + v0;
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
@@ -273,8 +313,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                 break;
             }
             tc_fence_after();
-            const int64_t tok = seq_start + static_cast<int64_t>(i) * kChunk + t;
-            const bool valid = tok < seq_end;
+            const int64_t tok = seq_start + static_cast<int64_t>(c_lo + i) * kChunk + t;
+            const bool valid = !trans && tok < seq_end;  // the transition pass writes no output
             bf16 *orow = p.o + tok * p.so_t + static_cast<int64_t>(hv) * p.so_h + v0;
 #pragma unroll 1
             for (int j = 0; j < VT / 32; ++j) {
@@ -324,7 +364,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                 const int blk = (32 * j) / 64, c0 = ((32 * j) % 64) / 8;
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(ut + blk * 8192 + swz(t, c0 + cc));
+                    const uint4 u = is_m ? make_uint4(0, 0, 0, 0)  // M columns: U = -Wt S
+                                         : *reinterpret_cast<const uint4 *>(ut + blk * 8192 + swz(t, c0 + cc));
                     const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
                     uint32_t ow[4];
 #pragma unroll
@@ -357,11 +398,61 @@ cudaError_t launch_state(const Params &p, cudaStream_t s) {
     auto kern = gdn2_tc_state_kernel<D, VT, NSTAGE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    if (p.N > 0) kern<<<dim3(p.N, p.HV, D / VT), kStateThreads, C::kSmem, s>>>(p);
+    const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
+    const int tiles = p.sc_mode == 1 ? 2 * D / VT : D / VT;
+    if (p.N > 0 && segs > 0) kern<<<dim3(p.N * segs, p.HV, tiles), kStateThreads, C::kSmem, s>>>(p);
     return cudaGetLastError();
 }
 
+// Chunk-parallel state pass, between the transition and the replay passes:
+// S_in(s + 1) = M_s S_in(s) + B_s for s = 0 .. P - 2, S_in(0) = the initial
+// state (or 0), into sc_si.  One CTA per (sequence, value head, 32 value
+// columns); fp32 on CUDA cores, the running 128 x 32 tile in shared memory.
+__global__ void __launch_bounds__(256) gdn2_scan_combine_kernel(Params p) {
+    constexpr int D = 128;
+    __shared__ float Ssm[D][33];
+    if (p.status[0] != GDN2_OK) return;
+    const int n = blockIdx.x, hv = blockIdx.y, c0 = 32 * blockIdx.z;
+    const int r = threadIdx.x >> 1, h16 = 16 * (threadIdx.x & 1);  // row r, 16 of the 32 columns
+    const int P = p.sc_P;
+    const size_t sblk = (static_cast<size_t>(n) * p.HV + hv) * D * D;
+#pragma unroll
+    for (int x = 0; x < 16; ++x)
+        Ssm[r][h16 + x] = p.h0 ? state_ld(p.h0, sblk + state_off(r, c0 + h16 + x, D, D, p.state_vmajor), p.state_bf16)
+                               : 0.f;
+    __syncthreads();
+    for (int sg = 0; sg < P - 1; ++sg) {
+        const size_t u = (static_cast<size_t>(n) * (P - 1) + sg) * p.HV + hv;
+        const float *tr = p.sc_tr + u * D * (2 * D) + static_cast<size_t>(r) * (2 * D);  // row r of [M | B]
+        float acc[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) acc[x] = tr[D + c0 + h16 + x];
+#pragma unroll 2
+        for (int c = 0; c < D; c += 4) {
+            const float4 m4 = *reinterpret_cast<const float4 *>(tr + c);
+            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int x = 0; x < 16; ++x) acc[x] += mv[k] * Ssm[c + k][h16 + x];
+        }
+        __syncthreads();
+        float *si = p.sc_si + u * D * D + static_cast<size_t>(r) * D + c0 + h16;
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            Ssm[r][h16 + x] = acc[x];
+            si[x] = acc[x];
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_tc_scan_combine(const Params &p, cudaStream_t s) {
+    if (p.N > 0 && p.sc_P > 1) gdn2_scan_combine_kernel<<<dim3(p.N, p.HV, 128 / 32), 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_tc_state(const Params &p, cudaStream_t s) {
     if (p.K == 64) return launch_state<64, 64, 3>(p, s);

@@ -49,7 +49,7 @@ class Dims(ctypes.Structure):
                 ("dtype_g", ctypes.c_int32), ("cu_seqlens_i64", ctypes.c_int32),
                 ("use_qk_l2norm", ctypes.c_int32), ("impl", ctypes.c_int32),
                 ("state_v_major", ctypes.c_int32), ("dtype_state", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("state_segments", ctypes.c_int32)]
 
 
 _lib = None
@@ -166,7 +166,7 @@ def workspace_bytes(dims: Dims) -> int:
 def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=None,
                    cu_seqlens=None, output_final_state=True, use_qk_l2norm=False, out=None,
                    final_state=None, workspace=None, impl="tc", stream=None, stage_events=None,
-                   state_v_major=False, state_dtype=None):
+                   state_v_major=False, state_dtype=None, state_segments=0):
     """GDN-2 chunked prefill forward through ``gdn2_chunk_fwd``.
 
     Packed layout (FlashInfer docs, chunk_gated_delta_rule2): q, k [T, H, K];
@@ -191,6 +191,7 @@ def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state
     if initial_state is not None and not initial_state.is_contiguous():
         raise ValueError("initial_state must be contiguous [N, HV, K, V] fp32")
     dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, impl, state_v_major, sdt)
+    dims.state_segments = int(state_segments)  # 0: chosen by the library
     nbytes = workspace_bytes(dims)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)

@@ -116,8 +116,24 @@ typedef struct gdn2_dims {
     int32_t impl;           /* gdn2_impl                                          */
     int32_t state_v_major;  /* 0: states [N, HV, K, V]; 1: [N, HV, V, K]          */
     int32_t dtype_state;    /* GDN2_DTYPE_F32 or GDN2_DTYPE_BF16                  */
-    int32_t reserved;       /* 0                                                  */
+    int32_t state_segments; /* chunk-parallel state pass; see below               */
 } gdn2_dims;
+/*
+ * state_segments (tensor-core path, K = V = 128): P > 1 splits each
+ * sequence's chunks into P segments of ceil(chunks / P).  Every segment's
+ * state map is affine, S_out = M S_in + B; the library computes [M | B] for
+ * segments 0 .. P - 2 in parallel, combines them in order (fp32) into each
+ * segment's incoming state, then replays all segments in parallel for o and
+ * the final state.  This shortens the sequential chain for few (sequence,
+ * head) pairs on long sequences (the FlashInfer docs, output_state: the
+ * cuDNN engine splits one sequence across CTAs).  0 = the library chooses
+ * P from a time model of the passes (P > 1 only for few (sequence, head)
+ * pairs on long sequences), 1 = one sequential pass, 2 .. 64 forced.
+ * Out of range, or > 1 with the SIMT path or K != 128: GDN2_ERR_SHAPE.  M is
+ * formed with the same 16-bit operands as the state pass, so results differ
+ * from the sequential pass by rounding only.  gdn2_recurrent_fwd checks only
+ * the range.
+ */
 
 /*
  * Bytes of device workspace gdn2_chunk_fwd needs for `dims` (0 if dims is

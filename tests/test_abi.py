@@ -188,3 +188,25 @@ def test_recurrent_argument_checks(lib):
     assert _recurrent(lib, d, p, out=p["q"]) == 4                # out overlaps an input
     # the chunked call keeps refusing an in-place state
     assert _check(lib, d, p, hT=p["h0"]) == 4
+
+
+def test_state_segments_host_logic(lib):
+    """The chunk-parallel state pass: argument range, where it is allowed,
+    the automatic choice (visible in the launch count) and its workspace."""
+    p = _ptrs(None, 0)
+    for val, impl, K, code in ((-1, 0, 128, 2), (65, 0, 128, 2), (64, 0, 128, 0), (4, 0, 64, 2),
+                               (4, 1, 128, 2), (1, 1, 128, 0), (1, 0, 64, 0)):
+        d = _dims(lib, K=K, V=K)
+        d.impl, d.state_segments = impl, val
+        assert _check(lib, d, p, ws_bytes=1 << 34) == code, (val, impl, K)
+    # few (sequence, head) pairs on long sequences: P >= 3 chosen automatically
+    few = _dims(lib, T=4096, N=1, H=16, HV=16, K=128, V=128)
+    assert gdn2.launch_count(few) == 5            # map, intra, transitions, combine, replay
+    seq = _dims(lib, T=4096, N=1, H=16, HV=16, K=128, V=128)
+    seq.state_segments = 1
+    assert gdn2.launch_count(seq) == 3            # map, intra, state
+    assert lib.gdn2_workspace_bytes(ctypes.byref(few)) > lib.gdn2_workspace_bytes(ctypes.byref(seq))
+    many = _dims(lib, T=4096, N=2, H=16, HV=16, K=128, V=128)   # 32 pairs: sequential
+    assert gdn2.launch_count(many) == 3
+    short = _dims(lib, T=1024, N=1, H=2, HV=2, K=128, V=128)    # 16 chunks: too short to split
+    assert gdn2.launch_count(short) == 3
