@@ -53,7 +53,9 @@ __device__ __forceinline__ void set_timeout(const Params &p) {
     atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
 }
 
-template <int D, int VT, int NSTAGE>
+// SCAN = false: the sequential pass (sc_mode 0), compiled without the
+// chunk-parallel modes' branches.
+template <int D, int VT, int NSTAGE, bool SCAN>
 __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params p) {
     using C = StateCfg<D, VT, NSTAGE>;
     extern __shared__ uint8_t smem_raw[];
@@ -69,10 +71,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
     // [seg L, seg L + L) of the sequence's, L = ceil(chunks / segments).  In the
     // transition pass (sc_mode 1) blockIdx.z tiles the K + V columns of [M | B]:
     // M columns start from the identity and take no Ut (S_out = M S_in + B).
-    const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
-    const int P = p.sc_mode == 0 ? 1 : p.sc_P;
+    const int mode = SCAN ? p.sc_mode : 0;
+    const int segs = mode == 1 ? p.sc_P - 1 : mode == 2 ? p.sc_P : 1;
+    const int P = mode == 0 ? 1 : p.sc_P;
     const int n = blockIdx.x / segs, seg = blockIdx.x % segs, hv = blockIdx.y;
-    const bool trans = p.sc_mode == 1;
+    const bool trans = mode == 1;
     const int col0 = blockIdx.z * VT;               // first column of this tile
     const bool is_m = trans && col0 < D;            // a tile of M
     const int v0 = trans ? (is_m ? 0 : col0 - D) : col0;
@@ -186,7 +189,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
         const size_t sblk = (static_cast<size_t>(n) * p.HV + hv) * D * D;  // this (sequence, head) block
         const bool plain = !p.state_vmajor && !p.state_bf16;           // fp32 [K][V]
         // a later segment of the replay pass starts from the combined state
-        const float *si = p.sc_mode == 2 && seg > 0
+        const float *si = mode == 2 && seg > 0
                               ? p.sc_si + ((static_cast<size_t>(n) * (P - 1) + seg - 1) * p.HV + hv) * D * D
                               : nullptr;
         if (active) {
@@ -268,7 +271,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
         tc_fence_after();
         // final state: the transition pass writes [M | B]; the replay pass only
         // from the last segment
-        const bool write_final = trans || (p.hT && (p.sc_mode != 2 || seg == P - 1));
+        const bool write_final = trans || (p.hT && (mode != 2 || seg == P - 1));
         if (ok && active && write_final) {
 #pragma unroll 1
             for (int j = j0; j < j1; ++j) {
@@ -392,10 +395,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
     }
 }
 
-template <int D, int VT, int NSTAGE>
+template <int D, int VT, int NSTAGE, bool SCAN>
 cudaError_t launch_state(const Params &p, cudaStream_t s) {
     using C = StateCfg<D, VT, NSTAGE>;
-    auto kern = gdn2_tc_state_kernel<D, VT, NSTAGE>;
+    auto kern = gdn2_tc_state_kernel<D, VT, NSTAGE, SCAN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
@@ -455,9 +458,11 @@ cudaError_t launch_tc_scan_combine(const Params &p, cudaStream_t s) {
 }
 
 cudaError_t launch_tc_state(const Params &p, cudaStream_t s) {
-    if (p.K == 64) return launch_state<64, 64, 3>(p, s);
-    if (p.vtile == 64) return launch_state<128, 64, 3>(p, s);
-    return launch_state<128, 128, 2>(p, s);
+    if (p.K == 64) return launch_state<64, 64, 3, false>(p, s);
+    if (p.sc_mode != 0)
+        return p.vtile == 64 ? launch_state<128, 64, 3, true>(p, s) : launch_state<128, 128, 2, true>(p, s);
+    if (p.vtile == 64) return launch_state<128, 64, 3, false>(p, s);
+    return launch_state<128, 128, 2, false>(p, s);
 }
 
 }  // namespace gdn2
