@@ -42,8 +42,10 @@ DEFAULT_WORKLOAD = 5
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 30 prefill forwards, 500 decode steps)")
+    ap.add_argument("--warmup", type=int, default=None,
+                    help="warm-up steps (default: 3 prefill forwards; decode: >= 3 steps and >= 0.3 s)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--op", choices=["prefill", "decode"], default="prefill",
                     help="prefill: the chunked forward (default); decode: the token-by-token "
@@ -52,11 +54,16 @@ def parse():
     ap.add_argument("--decode-tokens", type=int, default=1)
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
     ap.add_argument("--kernels", choices=["tc", "simt"], default=os.environ.get("GDN2_BENCH_KERNELS", "tc"))
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 500 if args.op == "decode" else 30
+    if args.warmup is None:
+        args.warmup = 3
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -414,20 +421,23 @@ def run_ours(args):
     if not args.no_e2e:
         host = {k: (v.cpu().pin_memory() if torch.is_tensor(v) else v) for k, v in d.items()}
         runner = gdn2.HostRunner(host, impl=args.kernels)
-        runner()
+        for _ in range(2):
+            runner()
         torch.cuda.synchronize()
-        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
         if world > 1:
             dist.barrier()
-        es.record(stream)
-        for _ in range(args.e2e_steps):
+        evs[0].record(stream)
+        for i in range(args.e2e_steps):
             runner()
-        ee.record(stream)
+            evs[i + 1].record(stream)
         torch.cuda.synchronize()
-        ems = gdist.max_over_ranks(es.elapsed_time(ee) / args.e2e_steps, device="cuda")
+        per = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.e2e_steps)]
+        ems = gdist.max_over_ranks(evs[0].elapsed_time(evs[-1]) / args.e2e_steps, device="cuda")
         e2e = {"value": gdist.aggregate_throughput(T, world, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
-               "ms_per_step": ems, "steps": args.e2e_steps}
+               "ms_per_step": ems, "steps": args.e2e_steps, "warmup": 2,
+               "ms_min": min(per), "ms_max": max(per)}
         del runner, host
 
     cpu = None
@@ -488,9 +498,14 @@ def run_decode(args):
                                 initial_state=d["h0"], cu_seqlens=d["cu_seqlens"], out=out, final_state=fs,
                                 workspace=ws)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
+    # warm up for >= 0.3 s as well as >= W steps: a decode step is ~0.1 ms, and
+    # a few steps leave the GPU at its idle clocks when the timed region starts
+    W, t0 = 0, time.perf_counter()
+    while W < max(3, args.warmup) or time.perf_counter() - t0 < 0.3:
+        for _ in range(50):
+            step()
+        W += 50
+        torch.cuda.synchronize()
     K = args.steps
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(0) as clk:
@@ -511,7 +526,7 @@ def run_decode(args):
     cpu = None if args.no_cpu_baseline else cpu_baseline(d, wl, args.cpu_seconds)
     line = {"metric": "GDN-2 decode tokens/s (token-by-token from a carried state)",
             "value": wl.T_tot / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": K,
-            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": wl.name, "B": wl.N, "T": wl.lens[0], "H": wl.H, "HV": wl.HV, "K": wl.K,
                        "V": wl.V, "initial_state": "N(0,%g)" % wl.h0_std,

@@ -62,9 +62,15 @@ __global__ void __launch_bounds__(256) gdn2_recurrent_check_kernel(RecParams p) 
     if (threadIdx.x == 0) p.status[0] = bad ? static_cast<int>(GDN2_ERR_CU_SEQLENS) : static_cast<int>(GDN2_OK);
 }
 
-template <int K>
+// GEN = false: bf16 inputs, fp32 g, fp32 K-major states through plain typed
+// loads and stores.  (The dtype-generic helpers cost this instance 4
+// registers, one CTA per SM less at K = 128, and 10 % of its time.)
+template <int K, bool GEN>
 __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
     constexpr int W = K / 32;
+    const bool f16 = GEN && p.in_f16, vmajor = GEN && p.state_vmajor, sbf16 = GEN && p.state_bf16;
+    const int gdt = GEN ? p.g_dtype : static_cast<int>(GDN2_DTYPE_F32);
+    auto ld16 = [&](const bf16 *b, int64_t i) { return GEN ? in_ld(b, i, f16) : __bfloat162float(b[i]); };
     __shared__ float s_k[K], s_bk[K], s_q[K], s_eg[K];
     __shared__ float s_part[2][W][32];
     __shared__ float s_red[3][W];
@@ -78,12 +84,15 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
     float S[32];
 #pragma unroll
     for (int r = 0; r < 32; ++r)
-        S[r] = p.h0 ? state_ld(p.h0, sbase + state_off(32 * wp + r, j, K, K, p.state_vmajor), p.state_bf16) : 0.f;
+        S[r] = !p.h0 ? 0.f
+               : GEN ? state_ld(p.h0, sbase + state_off(32 * wp + r, j, K, K, vmajor), sbf16)
+                     : static_cast<const float *>(p.h0)[sbase + static_cast<size_t>(32 * wp + r) * K + j];
     for (int64_t t = t0; t < t1; ++t) {
-        float kc = in_ld(p.k, t * p.sk_t + static_cast<int64_t>(h) * p.sk_h + tid, p.in_f16);
-        float qc = in_ld(p.q, t * p.sq_t + static_cast<int64_t>(h) * p.sq_h + tid, p.in_f16);
-        const float bc = p.has_beta ? in_ld(p.beta, t * p.sb_t + static_cast<int64_t>(hv) * p.sb_h + tid, p.in_f16) : 1.f;
-        const float gc = p.has_g ? g_ld(p.g, t * p.sg_t + static_cast<int64_t>(hv) * p.sg_h + tid, p.g_dtype) : 0.f;
+        float kc = ld16(p.k, t * p.sk_t + static_cast<int64_t>(h) * p.sk_h + tid);
+        float qc = ld16(p.q, t * p.sq_t + static_cast<int64_t>(h) * p.sq_h + tid);
+        const float bc = p.has_beta ? ld16(p.beta, t * p.sb_t + static_cast<int64_t>(hv) * p.sb_h + tid) : 1.f;
+        const float gc = p.has_g ? (GEN ? g_ld(p.g, t * p.sg_t + static_cast<int64_t>(hv) * p.sg_h + tid, gdt)
+                                 : p.g[t * p.sg_t + static_cast<int64_t>(hv) * p.sg_h + tid]) : 0.f;
         float a0 = kc * kc, a1 = qc * qc, a2 = qc * kc;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -101,8 +110,8 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
             kc *= ik; qc *= iq; qk *= ik * iq;
         }
         s_k[tid] = kc; s_bk[tid] = bc * kc; s_q[tid] = qc; s_eg[tid] = expf(gc);
-        const float vj = in_ld(p.v, t * p.sv_t + static_cast<int64_t>(hv) * p.sv_h + j, p.in_f16);
-        const float wj = p.has_w ? in_ld(p.w, t * p.sw_t + static_cast<int64_t>(hv) * p.sw_h + j, p.in_f16) : 1.f;
+        const float vj = ld16(p.v, t * p.sv_t + static_cast<int64_t>(hv) * p.sv_h + j);
+        const float wj = p.has_w ? ld16(p.w, t * p.sw_t + static_cast<int64_t>(hv) * p.sw_h + j) : 1.f;
         __syncthreads();
         float pr = 0.f, po = 0.f;
 #pragma unroll
@@ -121,7 +130,7 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
         if (wp == 0) {  // o at the inputs' dtype
             const float ov = p.scale * (oj + qk * u);
             const int64_t oi = t * p.so_t + static_cast<int64_t>(hv) * p.so_h + j;
-            if (p.in_f16)
+            if (f16)
                 reinterpret_cast<__half *>(p.o)[oi] = __float2half_rn(ov);
             else
                 p.o[oi] = __float2bfloat16_rn(ov);
@@ -131,7 +140,10 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
     if (p.hT) {
 #pragma unroll
         for (int r = 0; r < 32; ++r)
-            state_st(p.hT, sbase + state_off(32 * wp + r, j, K, K, p.state_vmajor), S[r], p.state_bf16);
+            if (GEN)
+                state_st(p.hT, sbase + state_off(32 * wp + r, j, K, K, vmajor), S[r], sbf16);
+            else
+                static_cast<float *>(p.hT)[sbase + static_cast<size_t>(32 * wp + r) * K + j] = S[r];
     }
 }
 
@@ -197,10 +209,11 @@ gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void *v, cons
     if (cudaGetLastError() != cudaSuccess) return GDN2_ERR_LAUNCH;
     if (d->N > 0) {
         const dim3 grid(d->N, d->HV, d->V / 32);
+        const bool gen = p.in_f16 || p.g_dtype != GDN2_DTYPE_F32 || p.state_vmajor || p.state_bf16;
         if (d->K == 64)
-            gdn2_recurrent_kernel<64><<<grid, 64, 0, s>>>(p);
+            (gen ? gdn2_recurrent_kernel<64, true> : gdn2_recurrent_kernel<64, false>)<<<grid, 64, 0, s>>>(p);
         else
-            gdn2_recurrent_kernel<128><<<grid, 128, 0, s>>>(p);
+            (gen ? gdn2_recurrent_kernel<128, true> : gdn2_recurrent_kernel<128, false>)<<<grid, 128, 0, s>>>(p);
         if (cudaGetLastError() != cudaSuccess) return GDN2_ERR_LAUNCH;
     }
     return GDN2_OK;
