@@ -135,6 +135,7 @@ WsLayout workspace_layout(const gdn2_dims &d) {
     L.chunk_len = take(NC * 4);
     L.chunk_start = take(NC * 8);
     L.seq_first = take((static_cast<size_t>(d.N) + 1) * 4);
+    L.seq_order = take(static_cast<size_t>(d.N) * 4);
     if (d.impl == GDN2_IMPL_SIMT) {
         L.G = take(T * d.HV * d.K * 4);
         L.qn = take(d.use_qk_l2norm ? T * d.H * d.K * 2 : 0);
@@ -343,6 +344,7 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     p.chunk_len = reinterpret_cast<int *>(ws + L.chunk_len);
     p.chunk_start = reinterpret_cast<int64_t *>(ws + L.chunk_start);
     p.seq_first = reinterpret_cast<int *>(ws + L.seq_first);
+    p.seq_order = reinterpret_cast<int *>(ws + L.seq_order);
     p.G = reinterpret_cast<float *>(ws + L.G);
     p.qn = reinterpret_cast<bf16 *>(ws + L.qn);
     p.kn = reinterpret_cast<bf16 *>(ws + L.kn);

@@ -48,6 +48,7 @@ struct Params {
     int *chunk_len;             // [NCmax]  tokens in chunk c (1..64)
     int64_t *chunk_start;       // [NCmax]  first token of chunk c
     int *seq_first;             // [N + 1]  first chunk of sequence n; [N] = NC
+    int *seq_order;             // [N]      sequences by chunk count, longest first
     float *G;                   // [T_tot, HV, K]  chunk-local inclusive cumsum of g
     bf16 *qn, *kn;              // [T_tot, H, K]   L2-normalised q, k (l2norm only)
     bf16 *Wt, *Ut;              // [T_tot, HV, K], [T_tot, HV, V]  WY pseudo-keys / values
@@ -78,7 +79,7 @@ struct Params {
 
 // Workspace layout (byte offsets), a function of the problem only.
 struct WsLayout {
-    size_t status, chunk_seq, chunk_len, chunk_start, seq_first, G, qn, kn, Wt, Ut, hbuf, vnew, rec, sc_tr, sc_si;
+    size_t status, chunk_seq, chunk_len, chunk_start, seq_first, seq_order, G, qn, kn, Wt, Ut, hbuf, vnew, rec, sc_tr, sc_si;
     size_t total;
 };
 

@@ -22,6 +22,7 @@ constexpr int kMapThreads = 1024;
 __global__ void __launch_bounds__(kMapThreads) gdn2_chunk_map_kernel(Params p) {
     __shared__ int s_bad;
     __shared__ int s_scan[kMapThreads];
+    __shared__ int s_pos[kMapThreads];  // chunk-count buckets of the sequence order
     __shared__ int s_total;
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -67,7 +68,31 @@ __global__ void __launch_bounds__(kMapThreads) gdn2_chunk_map_kernel(Params p) {
         p.status[0] = GDN2_OK;
         p.status[1] = NC;
     }
+    s_pos[tid] = 0;
     __syncthreads();  // seq_first (global, written above by this CTA) is now visible to it
+    // Sequence order for the state pass: longest first, so that the longest
+    // chunk chains start in the first wave of CTAs.  A counting sort over
+    // chunk counts (kMapThreads buckets, the last one open-ended); the order
+    // inside a bucket follows the shared-memory atomics and only decides
+    // which CTA starts first, never a result.
+    auto bucket = [&](int n) { return min(p.seq_first[n + 1] - p.seq_first[n], kMapThreads - 1); };
+    for (int n = tid; n < p.N; n += kMapThreads) atomicAdd(&s_pos[bucket(n)], 1);
+    __syncthreads();
+    {  // s_pos[b] = number of sequences in buckets above b (descending exclusive scan)
+        const int b = kMapThreads - 1 - tid;
+        const int cnt = s_pos[b];
+        s_scan[tid] = cnt;
+        __syncthreads();
+        for (int off = 1; off < kMapThreads; off <<= 1) {
+            const int x = tid >= off ? s_scan[tid - off] : 0;
+            __syncthreads();
+            s_scan[tid] += x;
+            __syncthreads();
+        }
+        s_pos[b] = s_scan[tid] - cnt;
+    }
+    __syncthreads();
+    for (int n = tid; n < p.N; n += kMapThreads) p.seq_order[atomicAdd(&s_pos[bucket(n)], 1)] = n;
     for (int c = tid; c < p.NCmax; c += kMapThreads) {
         if (c >= NC) {
             p.chunk_seq[c] = -1;

@@ -67,16 +67,23 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
 
     if (p.status[0] != GDN2_OK) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // blockIdx.x = (sequence, segment); the segment's chunks are
-    // [seg L, seg L + L) of the sequence's, L = ceil(chunks / segments).  In the
-    // transition pass (sc_mode 1) blockIdx.z tiles the K + V columns of [M | B]:
-    // M columns start from the identity and take no Ut (S_out = M S_in + B).
+    // A CTA takes one (sequence, segment, value head, tile); the segment's
+    // chunks are [seg L, seg L + L) of the sequence's, L = ceil(chunks /
+    // segments).  In the transition pass (sc_mode 1) the tiles cover the K + V
+    // columns of [M | B]: M columns start from the identity and take no Ut
+    // (S_out = M S_in + B).
     const int mode = SCAN ? p.sc_mode : 0;
     const int segs = mode == 1 ? p.sc_P - 1 : mode == 2 ? p.sc_P : 1;
     const int P = mode == 0 ? 1 : p.sc_P;
-    const int n = blockIdx.x / segs, seg = blockIdx.x % segs, hv = blockIdx.y;
+    // one-dimensional grid: V tile fastest, then value head, then segment,
+    // then the sequence's rank in the longest-first order
+    const int tiles = mode == 1 ? 2 * D / VT : D / VT;
+    const int tile = blockIdx.x % tiles;
+    const int hv = (blockIdx.x / tiles) % p.HV;
+    const int rs = blockIdx.x / (tiles * p.HV);
+    const int seg = rs % segs, n = p.seq_order[rs / segs];
     const bool trans = mode == 1;
-    const int col0 = blockIdx.z * VT;               // first column of this tile
+    const int col0 = tile * VT;                     // first column of this tile
     const bool is_m = trans && col0 < D;            // a tile of M
     const int v0 = trans ? (is_m ? 0 : col0 - D) : col0;
     const int seq0 = p.seq_first[n], nck_all = p.seq_first[n + 1] - seq0;
@@ -403,7 +410,9 @@ cudaError_t launch_state(const Params &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
     const int tiles = p.sc_mode == 1 ? 2 * D / VT : D / VT;
-    if (p.N > 0 && segs > 0) kern<<<dim3(p.N * segs, p.HV, tiles), kStateThreads, C::kSmem, s>>>(p);
+    const long long ctas = static_cast<long long>(p.N) * segs * p.HV * tiles;
+    if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+    if (ctas > 0) kern<<<static_cast<unsigned>(ctas), kStateThreads, C::kSmem, s>>>(p);
     return cudaGetLastError();
 }
 
