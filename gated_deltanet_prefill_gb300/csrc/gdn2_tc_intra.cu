@@ -359,11 +359,16 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         wX2[j] = pack8_h(ww);
     }
     float Gr[8 * NJ];
+    // G rows are 512 bytes apart, so the same channels of a warp's eight rows
+    // share banks; odd rows load each chunk's two halves in the other order,
+    // which spreads every load instruction over all 32 banks
+    const int gsw = (t & 1) ? 4 : 0;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         const int cb = 8 * (seg + 4 * j);
-        const float4 a = *reinterpret_cast<const float4 *>(Gs + t * D + cb);
-        const float4 b = *reinterpret_cast<const float4 *>(Gs + t * D + cb + 4);
+        const float4 x0 = *reinterpret_cast<const float4 *>(Gs + t * D + cb + gsw);
+        const float4 x1 = *reinterpret_cast<const float4 *>(Gs + t * D + cb + (4 - gsw));
+        const float4 a = gsw ? x1 : x0, b = gsw ? x0 : x1;
         Gr[8 * j + 0] = a.x; Gr[8 * j + 1] = a.y; Gr[8 * j + 2] = a.z; Gr[8 * j + 3] = a.w;
         Gr[8 * j + 4] = b.x; Gr[8 * j + 5] = b.y; Gr[8 * j + 6] = b.z; Gr[8 * j + 7] = b.w;
     }
