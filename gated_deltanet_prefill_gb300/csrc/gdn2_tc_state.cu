@@ -172,14 +172,16 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                     break;
                 }
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(tD1[b], desc_kmajor(st + C::sP, 128, kk), desc_mnmajor(sU, 64, kk), id1, 1);
+                // the state update first: the S epilogue (the chain) starts
+                // while the output product P U still runs
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_f16(tS, desc_mnmajor(st + C::sKdT, 64, kk), desc_mnmajor(sU, 64, kk), id3, 1);
-                mma_commit(&o_full[b]);
                 mma_commit(&s_full);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(tD1[b], desc_kmajor(st + C::sP, 128, kk), desc_mnmajor(sU, 64, kk), id1, 1);
+                mma_commit(&o_full[b]);
                 mma_commit(&empty_bar[s]);
             }
             mma_commit(&drain);
