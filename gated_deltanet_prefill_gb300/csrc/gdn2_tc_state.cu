@@ -20,6 +20,8 @@
 // each), 4-5 output epilogue.  Every wait is time-bounded; a timeout sets the device
 // status word and the CTA unwinds.  Operands are fp16 (10-bit mantissa,
 // saturating at +-65504); accumulation and the carried state are fp32.
+#include <stdlib.h>
+
 #include "gdn2_internal.cuh"
 #include "gdn2_record.cuh"
 #include "gdn2_tc.cuh"
@@ -470,6 +472,10 @@ cudaError_t launch_tc_scan_combine(const Params &p, cudaStream_t s) {
 
 cudaError_t launch_tc_state(const Params &p, cudaStream_t s) {
     if (p.K == 64) return launch_state<64, 64, 3, false>(p, s);
+    // 64-column tiles of the sequential pass: the one-chunk lookahead kernel
+    // (GDN2_STATE_LOOKAHEAD=0 selects the plain kernel, for comparison)
+    const char *la = getenv("GDN2_STATE_LOOKAHEAD");
+    if (p.vtile == 64 && p.sc_mode == 0 && !(la && la[0] == '0')) return launch_tc_state_la(p, s);
     if (p.sc_mode != 0)
         return p.vtile == 64 ? launch_state<128, 64, 3, true>(p, s) : launch_state<128, 128, 2, true>(p, s);
     if (p.vtile == 64) return launch_state<128, 64, 3, false>(p, s);

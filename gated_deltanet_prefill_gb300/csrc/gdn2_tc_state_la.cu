@@ -1,0 +1,418 @@
+// Tensor-core state-passing kernel with a one-chunk lookahead (K = V = 128,
+// 64-column V tiles, the sequential pass).
+//
+// The plain state kernel runs one dependent chain per chunk: S image ->
+// [Qe ; Wt] S -> U = Ut - Wt S -> S += Kd^T U -> next S image.  Here the next
+// chunk's product with the state is split along the state update.  With
+// A1 = [Qe ; Wt] (the record's 128-row A operand) and E_c = diag(eGL_c) S_c
+// (the state with its rows rescaled by e^{G_L}),
+//   A1_{c+1} S_{c+1} = A1_{c+1} E_c + (A1_{c+1} Kd_c^T) U_c,
+// so the first product and XY_{c+1} = A1_{c+1} Kd_c^T need no U and run ahead;
+// only XY_{c+1} U_c (K = 64) stands between U_c and U_{c+1}.  The rows Qe give
+// the output's inter-chunk term the same way.  Per chunk c (chunk 0 takes
+// D_0 = A1_0 S_0 directly):
+//   Ma  D_c  = A1_c img(E_{c-1})           fp16 image of E, MN-major B
+//   Mb  XY_c = A1_c Kd_{c-1}^T             fp32 in TMEM -> fp16 A operand in TMEM
+//   Mc  D_c += XY_c img(U_{c-1})           A from Tensor Memory
+//   epi U_c  = Ut_c - D_c[64:128]          fp16 image (two buffers)
+//   Me  S    = E_c + Kd_c^T U_c            S_{c+1}, fp32 in TMEM
+//   Md  D_c[0:64] += P_c U_c               output -> scale -> global
+// Tensor pipe order per chunk c: Ma_{c+1}; once U_c is ready Mc_{c+1} (the
+// chain), Me_c, Md_c; then Mb_{c+2}.  Accumulators D are triple-buffered so
+// that an output epilogue never delays the next chunk's first product.
+//
+// Warps (24): 0 bulk-copy producer, 1 MMA issuer (and TMEM owner), 2-3 and
+// 6-7 U epilogue (D rows 64-127 live in TMEM lane quarters 2 and 3), 4-5
+// output epilogue, 8-15 state epilogue (E = eGL S -> fp16 image and back to
+// TMEM), 16-23 XY epilogue (fp32 -> fp16 A operand).  Every wait is
+// time-bounded; a timeout sets the device status word and the CTA unwinds.
+#include "gdn2_internal.cuh"
+#include "gdn2_record.cuh"
+#include "gdn2_tc.cuh"
+
+namespace gdn2 {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kLaThreads = 768;
+
+struct LaCfg {
+    static constexpr int D = 128, VT = 64, NSTAGE = 3;
+    // a stage holds the record's P, A1, Kd^T (one contiguous copy) and the
+    // tile's 64 columns of Ut; the stages' eGL vectors live after the images
+    static constexpr uint32_t sP = 0;
+    static constexpr uint32_t sA1 = 8192;
+    static constexpr uint32_t sKdT = sA1 + 2 * 16384;
+    static constexpr uint32_t sUt = sKdT + 2 * 8192;
+    static constexpr uint32_t kStage = sUt + 8192;
+    static constexpr uint32_t oE = NSTAGE * kStage;         // E image: [128 K rows][64 columns] fp16
+    static constexpr uint32_t oU = oE + D * 128;            // two U images: [64 t][64 columns] fp16
+    static constexpr uint32_t oEGL = oU + 2 * 8192;         // eGL per stage, D fp32
+    static constexpr uint32_t kSmem = oEGL + NSTAGE * D * 4 + 1024;  // + alignment slack
+    static constexpr uint32_t kLoadBytes = Rec<D>::mma_prefix + 8192 + D * 4;
+    // TMEM columns: S (64), D x 3 (64 each), XY fp32 (64), XY fp16 A operand (32)
+    static constexpr uint32_t cS = 0, cD = 64, cXY = 256, cXa = 320, kTmemCols = 512;
+    static_assert(Rec<D>::mma_prefix == sUt, "P, A1 and Kd^T are one contiguous copy");
+    static_assert(kStage % 1024 == 0 && oE % 1024 == 0 && oU % 1024 == 0, "128B-swizzle operands");
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void set_timeout_la(const Params &p) {
+    atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
+}
+
+__global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params p) {
+    using C = LaCfg;
+    constexpr int D = C::D, VT = C::VT, NSTAGE = C::NSTAGE;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ uint64_t full_bar[NSTAGE], empty_bar[NSTAGE];
+    __shared__ uint64_t s_ready, s_full, u_ready, xy_full, xy_ready, drain;
+    __shared__ uint64_t d_full[3], o_full[3], d_free[3];
+    __shared__ uint32_t tmem_slot;
+
+    if (p.status[0] != GDN2_OK) return;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // one CTA per (sequence in longest-first order, value head, 64-column tile)
+    const int tile = blockIdx.x % 2;
+    const int hv = (blockIdx.x / 2) % p.HV;
+    const int n = p.seq_order[blockIdx.x / (2 * p.HV)];
+    const int v0 = tile * VT;
+    const int first = p.seq_first[n], nck = p.seq_first[n + 1] - first;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        mbar_init(&s_ready, 256);
+        mbar_init(&s_full, 1);
+        mbar_init(&u_ready, 128);
+        mbar_init(&xy_full, 1);
+        mbar_init(&xy_ready, 256);
+        mbar_init(&drain, 1);
+        for (int b = 0; b < 3; ++b) {
+            mbar_init(&d_full[b], 1);
+            mbar_init(&o_full[b], 1);
+            mbar_init(&d_free[b], 64);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS = tmem_slot + C::cS, tXY = tmem_slot + C::cXY, tXa = tmem_slot + C::cXa;
+    auto tD = [&](int c) { return tmem_slot + C::cD + 64u * static_cast<uint32_t>(c % 3); };
+    auto stage = [&](int c) { return sm + (c % NSTAGE) * C::kStage; };
+    const uint32_t sE = smem_u32(sm + C::oE);
+    auto sU = [&](int c) { return smem_u32(sm + C::oU + (c & 1) * 8192); };
+
+    if (warp == 0) {
+        // ------------------------------------------------ bulk-copy producer
+        if (lane == 0) {
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < nck && ok; ++i) {
+                const int s = i % NSTAGE;
+                if (i >= NSTAGE && !mbar_wait(&empty_bar[s], ((i / NSTAGE) - 1) & 1)) {
+                    set_timeout_la(p);
+                    ok = false;
+                    break;
+                }
+                const uint8_t *rec = p.rec + (static_cast<size_t>(first + i) * p.HV + hv) * Rec<D>::bytes;
+                mbar_arrive_expect_tx(&full_bar[s], C::kLoadBytes);
+                bulk_g2s(stage(i) + C::sP, rec + Rec<D>::P, Rec<D>::mma_prefix, &full_bar[s]);
+                bulk_g2s(stage(i) + C::sUt, rec + Rec<D>::Ut + tile * 8192, 8192, &full_bar[s]);
+                bulk_g2s(sm + C::oEGL + s * D * 4, rec + Rec<D>::eGL, D * 4, &full_bar[s]);
+                ++issued;
+            }
+            if (!ok) {  // let every copy in flight land before the CTA exits
+                for (int i = issued - NSTAGE > 0 ? issued - NSTAGE : 0; i < issued; ++i)
+                    mbar_wait(&full_bar[i % NSTAGE], (i / NSTAGE) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA issuer
+        if (lane == 0 && nck > 0) {
+            constexpr uint32_t idB = idesc_fp16(128, VT, false, true);   // B = state / U image (MN-major)
+            constexpr uint32_t idS = idesc_fp16(128, VT, true, true);    // A = Kd^T (MN-major)
+            constexpr uint32_t idXY = idesc_fp16(128, 64, false, false); // B = Kd^T read K-major (N = tokens)
+            bool ok = true;
+            auto product_a1 = [&](int j) {  // D_j = A1_j img(E)  (img(S_0) for j = 0)
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_f16(tD(j), desc_kmajor(smem_u32(stage(j) + C::sA1), 128, kk), desc_mnmajor(sE, D, kk), idB,
+                            kk > 0);
+            };
+            auto product_xy = [&](int j) {  // XY_j = A1_j Kd_{j-1}^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_f16(tXY, desc_kmajor(smem_u32(stage(j) + C::sA1), 128, kk),
+                            desc_kmajor(smem_u32(stage(j - 1) + C::sKdT), 64, kk), idXY, kk > 0);
+                mma_commit(&xy_full);
+            };
+            if (!mbar_wait(&full_bar[0], 0) || !mbar_wait(&s_ready, 0)) ok = false;
+            if (ok) {
+                tc_fence_after();
+                product_a1(0);
+                mma_commit(&d_full[0]);
+                if (nck > 1) {
+                    if (!mbar_wait(&full_bar[1 % NSTAGE], 0)) {
+                        ok = false;
+                    } else {
+                        tc_fence_after();
+                        product_xy(1);
+                    }
+                }
+            }
+            for (int c = 0; c < nck && ok; ++c) {
+                const bool next = c + 1 < nck;
+                // E_c is ready: its image (for D_{c+1}) and Tensor Memory (for
+                // the state update)
+                if (!mbar_wait(&s_ready, (c + 1) & 1) ||
+                    (next && c + 1 >= 3 && !mbar_wait(&d_free[(c + 1) % 3], ((c - 2) / 3) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (next) product_a1(c + 1);
+                if (!mbar_wait(&u_ready, c & 1) || (next && !mbar_wait(&xy_ready, c & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (next) {  // the chain: D_{c+1} += XY_{c+1} U_c
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) mma_f16_ta(tD(c + 1), tXa + 8 * kk, desc_mnmajor(sU(c), 64, kk), idB, 1);
+                    mma_commit(&d_full[(c + 1) % 3]);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(tS, desc_mnmajor(smem_u32(stage(c) + C::sKdT), 64, kk), desc_mnmajor(sU(c), 64, kk), idS,
+                            1);
+                mma_commit(&s_full);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_f16(tD(c), desc_kmajor(smem_u32(stage(c) + C::sP), 128, kk), desc_mnmajor(sU(c), 64, kk), idB,
+                            1);
+                mma_commit(&o_full[c % 3]);
+                if (c + 2 < nck) {
+                    if (!mbar_wait(&full_bar[(c + 2) % NSTAGE], ((c + 2) / NSTAGE) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    product_xy(c + 2);
+                }
+                mma_commit(&empty_bar[c % NSTAGE]);
+            }
+            if (!ok) set_timeout_la(p);
+            mma_commit(&drain);
+            if (!mbar_wait(&drain, 0)) set_timeout_la(p);
+        }
+    } else if (warp >= 8 && warp < 16) {
+        // ------------------------- state epilogue: E_c = eGL_c S_c (rows = key channels)
+        const int q = warp & 3, g = (warp - 8) >> 2;  // lane quarter, 32-column group
+        const int row = 32 * q + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const size_t sblk = (static_cast<size_t>(n) * p.HV + hv) * D * D;  // this (sequence, head) block
+        const bool plain = !p.state_vmajor && !p.state_bf16;           // fp32 [K][V]
+        const int col0 = v0 + 32 * g;
+        uint8_t *img = sm + C::oE;
+        auto write_img = [&](const uint32_t (&r)[32]) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint4 v;
+                v.x = pack_h2(__uint_as_float(r[8 * cc + 0]), __uint_as_float(r[8 * cc + 1]));
+                v.y = pack_h2(__uint_as_float(r[8 * cc + 2]), __uint_as_float(r[8 * cc + 3]));
+                v.z = pack_h2(__uint_as_float(r[8 * cc + 4]), __uint_as_float(r[8 * cc + 5]));
+                v.w = pack_h2(__uint_as_float(r[8 * cc + 6]), __uint_as_float(r[8 * cc + 7]));
+                *reinterpret_cast<uint4 *>(img + swz(row, 4 * g + cc)) = v;
+            }
+        };
+        uint32_t r[32];
+        if (p.h0 && plain) {
+            const float *h0 = static_cast<const float *>(p.h0) + sblk + static_cast<size_t>(row) * D + col0;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(h0 + e);
+                r[e] = __float_as_uint(x.x); r[e + 1] = __float_as_uint(x.y);
+                r[e + 2] = __float_as_uint(x.z); r[e + 3] = __float_as_uint(x.w);
+            }
+        } else {  // zero, bf16 or V-major: element by element (lanes = consecutive rows)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                r[e] = __float_as_uint(
+                    p.h0 ? state_ld(p.h0, sblk + state_off(row, col0 + e, D, D, p.state_vmajor), p.state_bf16) : 0.f);
+        }
+        write_img(r);  // img(S_0) for D_0
+        fence_proxy_async();
+        mbar_arrive(&s_ready);
+        bool ok = true;
+        for (int c = 0; c < nck; ++c) {
+            // S_c is in Tensor Memory (chunk 0: in registers) and the image is
+            // free: after D_0's product, later after the state update (which
+            // the tensor pipe runs after D_c's first product)
+            if ((c == 0 ? !warp_wait(&d_full[0], 0) : !warp_wait(&s_full, (c - 1) & 1)) ||
+                !warp_wait(&full_bar[c % NSTAGE], (c / NSTAGE) & 1)) {
+                set_timeout_la(p);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (c > 0) {
+                tmem_ld32(tS + lane_base + 32 * g, r);
+                tmem_ld_wait();
+            }
+            const float egl = reinterpret_cast<const float *>(sm + C::oEGL + (c % NSTAGE) * D * 4)[row];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * egl);
+            write_img(r);
+            tmem_st32(tS + lane_base + 32 * g, r);
+            tmem_st_wait();
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(&s_ready);
+        }
+        if (ok && nck > 0 && !warp_wait(&s_full, (nck - 1) & 1)) {
+            set_timeout_la(p);
+            ok = false;
+        }
+        tc_fence_after();
+        if (ok && p.hT) {
+            if (nck > 0) {  // S_nck (with no chunk, S_0 is still in registers)
+                tmem_ld32(tS + lane_base + 32 * g, r);
+                tmem_ld_wait();
+            }
+            if (plain) {
+                float *hT = static_cast<float *>(p.hT) + sblk + static_cast<size_t>(row) * D + col0;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(hT + e) = make_float4(
+                        __uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                        __uint_as_float(r[e + 3]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    state_st(p.hT, sblk + state_off(row, col0 + e, D, D, p.state_vmajor), __uint_as_float(r[e]),
+                             p.state_bf16);
+            }
+        }
+    } else if (warp >= 16) {
+        // ------------------- XY epilogue: fp32 accumulator -> fp16 A operand in TMEM
+        const int q = warp & 3, g = (warp - 16) >> 2;  // lane quarter, 32 of the 64 token columns
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        for (int k = 0; k + 1 < nck; ++k) {  // XY of chunk k + 1
+            if (!warp_wait(&xy_full, k & 1)) {
+                set_timeout_la(p);
+                break;
+            }
+            tc_fence_after();
+            uint32_t r[32], h[16];
+            tmem_ld32(tXY + lane_base + 32 * g, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) h[i] = pack_h2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            tmem_st16(tXa + lane_base + 16 * g, h);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&xy_ready);
+        }
+    } else if (warp == 4 || warp == 5) {
+        // ----------------------------------------- output epilogue (tokens 0-63)
+        const int q = warp & 3;  // 0 or 1
+        const int t = 32 * q + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const int64_t seq_start = cu_at(p, n), seq_end = cu_at(p, n + 1);
+        for (int c = 0; c < nck; ++c) {
+            if (!warp_wait(&o_full[c % 3], (c / 3) & 1)) {
+                set_timeout_la(p);
+                break;
+            }
+            tc_fence_after();
+            const int64_t tok = seq_start + static_cast<int64_t>(c) * kChunk + t;
+            const bool valid = tok < seq_end;
+            bf16 *orow = p.o + tok * p.so_t + static_cast<int64_t>(hv) * p.so_h + v0;
+#pragma unroll 1
+            for (int j = 0; j < VT / 32; ++j) {
+                uint32_t r[32];
+                tmem_ld32(tD(c) + lane_base + 32 * j, r);
+                tmem_ld_wait();
+                if (valid) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        // output at the inputs' dtype (plain round-to-nearest)
+                        auto pk = [&](int e) {
+                            const float a = __uint_as_float(r[8 * cc + e]) * p.scale;
+                            const float b = __uint_as_float(r[8 * cc + e + 1]) * p.scale;
+                            return p.in_f16 ? pack_f16_rn(a, b) : pack_bf2(a, b);
+                        };
+                        reinterpret_cast<uint4 *>(orow + 32 * j)[cc] = make_uint4(pk(0), pk(2), pk(4), pk(6));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&d_free[c % 3]);
+        }
+    } else {
+        // ----------------------------------- U epilogue (D rows 64-127 = Wt S)
+        const int q = warp & 3;  // 2 or 3
+        const int t = 32 * (q - 2) + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        const int g = warp < 4 ? 0 : 1;  // 32-column group
+        for (int c = 0; c < nck; ++c) {
+            if (!warp_wait(&d_full[c % 3], (c / 3) & 1) || !warp_wait(&full_bar[c % NSTAGE], (c / NSTAGE) & 1)) {
+                set_timeout_la(p);
+                break;
+            }
+            tc_fence_after();
+            const uint8_t *ut = stage(c) + C::sUt;
+            uint8_t *dst = sm + C::oU + (c & 1) * 8192;
+            uint32_t r[32];
+            tmem_ld32(tD(c) + lane_base + 32 * g, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(ut + swz(t, 4 * g + cc));
+                const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+                uint32_t ow[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 a = unpack_h2(uw[e]);
+                    ow[e] = pack_h2(a.x - __uint_as_float(r[8 * cc + 2 * e]), a.y - __uint_as_float(r[8 * cc + 2 * e + 1]));
+                }
+                *reinterpret_cast<uint4 *>(dst + swz(t, 4 * g + cc)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(&u_ready);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_slot, C::kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_state_la(const Params &p, cudaStream_t s) {
+    auto kern = gdn2_tc_state_la_kernel;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LaCfg::kSmem);
+    if (e != cudaSuccess) return e;
+    const long long ctas = static_cast<long long>(p.N) * p.HV * 2;
+    if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+    if (ctas > 0) kern<<<static_cast<unsigned>(ctas), kLaThreads, LaCfg::kSmem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn2

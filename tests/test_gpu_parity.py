@@ -267,3 +267,22 @@ def test_host_runner_matches_device_call(cuda_lib, groups):
     o_ref, h_ref = run_oracle(d)
     assert rel_max(o_h.float().numpy(), o_ref) <= TOL
     assert rel_max(h_h.numpy(), h_ref) <= TOL
+
+
+@pytest.mark.parametrize("lookahead", ["1", "0"])
+def test_state_kernels_64_column_tiles(cuda_lib, monkeypatch, lookahead):
+    """Both state kernels of the 64-column tile (few (sequence, head) pairs):
+    the one-chunk lookahead kernel (default) and the plain one; ragged
+    sequences from empty to several stage wraps, decay stress, initial state."""
+    monkeypatch.setenv("GDN2_STATE_LOOKAHEAD", lookahead)
+    wl = inputs.small("vt64_%s" % lookahead, [0, 1, 64, 65, 200, 900], H=2, HV=4, K=128, V=128, g_max=2.0,
+                      beta_max=2.0, h0_std=0.05, seed=95)
+    d = inputs.generate(wl)
+    o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                                       initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
+    dd = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in d.items()}
+    o, hT = cuda_lib.chunk_gdn2_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["w"], scale=dd["scale"],
+                                    initial_state=dd["h0"], cu_seqlens=dd["cu_seqlens"], state_segments=1)
+    torch.cuda.synchronize()
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
