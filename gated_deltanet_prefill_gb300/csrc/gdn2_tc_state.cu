@@ -7,9 +7,12 @@
 // with the intra kernel's record (gdn2_record.cuh):
 //   MMA1  D1 = [Qe ; Wt] x S_fp16          (M=128, N=VT, K=D)
 //   epi   U  = Ut - (Wt S)  -> fp16 smem   (rows 64-127 of D1)
-//   MMA2  D1[0:64] += P x U                (M=128, K=64; rows 64-127 dead)
 //   MMA3  S  += Kd^T x U                   (M=128, K=64), S pre-scaled by eGL
+//   MMA2  D1[0:64] += P x U                (M=128, K=64; rows 64-127 dead)
 //   epi   o = scale * D1[0:64] -> bf16 global
+// (the state update is issued first: it is on the chunk chain, the output
+// product is not).  For 64-column tiles of the sequential pass the
+// lookahead kernel (gdn2_tc_state_la.cu) is used instead.
 // which is the FlashRT page's WY chain (chunk_h then output_o) fused into one
 // pass, with burn-gdn2's "in-loop output phase".
 //
