@@ -159,6 +159,13 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
         if (lane == 0) {
             constexpr uint32_t id1 = idesc_fp16(128, VT, false, true);
             constexpr uint32_t id3 = idesc_fp16(128, VT, true, true);
+            // descriptors are linear in the address (below 256 KB): a k-step
+            // adds a constant to the base descriptor
+            auto kmaj = [](uint32_t rows, int kk) -> uint64_t {
+                return ((kk >> 2) * rows * 128u + (kk & 3) * 32u) >> 4;
+            };
+            auto mnmaj = [](int kk) -> uint64_t { return static_cast<uint64_t>(kk) * (2048u >> 4); };
+            const uint64_t dS = desc_mnmajor(sS, D, 0), dU = desc_mnmajor(sU, 64, 0);
             for (int i = 0; i < nck; ++i) {
                 const int s = i % NSTAGE, b = i & 1;
                 if (!mbar_wait(&full_bar[s], (i / NSTAGE) & 1) || !mbar_wait(&s_ready, i & 1) ||
@@ -168,9 +175,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                 }
                 tc_fence_after();
                 const uint32_t st = smem_u32(sm + s * C::kStage);
+                const uint64_t dA1 = desc_kmajor(st + C::sA1, 128, 0), dKd = desc_mnmajor(st + C::sKdT, 64, 0),
+                               dP = desc_kmajor(st + C::sP, 128, 0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_f16(tD1[b], desc_kmajor(st + C::sA1, 128, kk), desc_mnmajor(sS, D, kk), id1, kk > 0);
+                    mma_f16(tD1[b], dA1 + kmaj(128, kk), dS + mnmaj(kk), id1, kk > 0);
                 mma_commit(&d1_full[b]);
                 if (!mbar_wait(&u_ready, i & 1)) {
                     set_timeout(p);
@@ -180,12 +189,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                 // the state update first: the S epilogue (the chain) starts
                 // while the output product P U still runs
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(tS, desc_mnmajor(st + C::sKdT, 64, kk), desc_mnmajor(sU, 64, kk), id3, 1);
+                for (int kk = 0; kk < 4; ++kk) mma_f16(tS, dKd + mnmaj(kk), dU + mnmaj(kk), id3, 1);
                 mma_commit(&s_full);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(tD1[b], desc_kmajor(st + C::sP, 128, kk), desc_mnmajor(sU, 64, kk), id1, 1);
+                for (int kk = 0; kk < 4; ++kk) mma_f16(tD1[b], dP + kmaj(128, kk), dU + mnmaj(kk), id1, 1);
                 mma_commit(&o_full[b]);
                 mma_commit(&empty_bar[s]);
             }

@@ -144,17 +144,23 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
             constexpr uint32_t idS = idesc_fp16(128, VT, true, true);    // A = Kd^T (MN-major)
             constexpr uint32_t idXY = idesc_fp16(128, 64, false, false); // B = Kd^T read K-major (N = tokens)
             bool ok = true;
+            // descriptors are linear in the address (below 256 KB): a k-step
+            // adds a constant to the base descriptor
+            auto kmaj = [](uint32_t rows, int kk) -> uint64_t {
+                return ((kk >> 2) * rows * 128u + (kk & 3) * 32u) >> 4;
+            };
+            auto mnmaj = [](int kk) -> uint64_t { return static_cast<uint64_t>(kk) * (2048u >> 4); };
+            const uint64_t dE = desc_mnmajor(sE, D, 0);
             auto product_a1 = [&](int j) {  // D_j = A1_j img(E)  (img(S_0) for j = 0)
+                const uint64_t dA = desc_kmajor(smem_u32(stage(j) + C::sA1), 128, 0);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_f16(tD(j), desc_kmajor(smem_u32(stage(j) + C::sA1), 128, kk), desc_mnmajor(sE, D, kk), idB,
-                            kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk) mma_f16(tD(j), dA + kmaj(128, kk), dE + mnmaj(kk), idB, kk > 0);
             };
             auto product_xy = [&](int j) {  // XY_j = A1_j Kd_{j-1}^T
+                const uint64_t dA = desc_kmajor(smem_u32(stage(j) + C::sA1), 128, 0);
+                const uint64_t dK = desc_kmajor(smem_u32(stage(j - 1) + C::sKdT), 64, 0);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_f16(tXY, desc_kmajor(smem_u32(stage(j) + C::sA1), 128, kk),
-                            desc_kmajor(smem_u32(stage(j - 1) + C::sKdT), 64, kk), idXY, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk) mma_f16(tXY, dA + kmaj(128, kk), dK + kmaj(64, kk), idXY, kk > 0);
                 mma_commit(&xy_full);
             };
             if (!mbar_wait(&full_bar[0], 0) || !mbar_wait(&s_ready, 0)) ok = false;
@@ -187,20 +193,19 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
                     break;
                 }
                 tc_fence_after();
+                const uint64_t dU = desc_mnmajor(sU(c), 64, 0);
                 if (next) {  // the chain: D_{c+1} += XY_{c+1} U_c
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) mma_f16_ta(tD(c + 1), tXa + 8 * kk, desc_mnmajor(sU(c), 64, kk), idB, 1);
+                    for (int kk = 0; kk < 4; ++kk) mma_f16_ta(tD(c + 1), tXa + 8 * kk, dU + mnmaj(kk), idB, 1);
                     mma_commit(&d_full[(c + 1) % 3]);
                 }
+                const uint64_t dK = desc_mnmajor(smem_u32(stage(c) + C::sKdT), 64, 0);
+                const uint64_t dP = desc_kmajor(smem_u32(stage(c) + C::sP), 128, 0);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(tS, desc_mnmajor(smem_u32(stage(c) + C::sKdT), 64, kk), desc_mnmajor(sU(c), 64, kk), idS,
-                            1);
+                for (int kk = 0; kk < 4; ++kk) mma_f16(tS, dK + mnmaj(kk), dU + mnmaj(kk), idS, 1);
                 mma_commit(&s_full);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_f16(tD(c), desc_kmajor(smem_u32(stage(c) + C::sP), 128, kk), desc_mnmajor(sU(c), 64, kk), idB,
-                            1);
+                for (int kk = 0; kk < 4; ++kk) mma_f16(tD(c), dP + kmaj(128, kk), dU + mnmaj(kk), idB, 1);
                 mma_commit(&o_full[c % 3]);
                 if (c + 2 < nck) {
                     if (!mbar_wait(&full_bar[(c + 2) % NSTAGE], ((c + 2) / NSTAGE) & 1)) {
