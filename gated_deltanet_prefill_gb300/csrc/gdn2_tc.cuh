@@ -57,15 +57,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 // Wait for the phase with the given parity to complete; gives up after
-// kWaitLimitNs of wall time and returns false (the caller records the
-// timeout and unwinds instead of hanging).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// limit_ns of wall time and returns false (the caller records the timeout
+// and unwinds instead of hanging).
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_ns(bar, parity, kWaitLimitNs);
 }
 
 // The same wait taken by a whole warp, with a warp-uniform result, so that the

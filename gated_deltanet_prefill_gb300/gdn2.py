@@ -29,7 +29,7 @@ _DTYPE_CODE = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16, torch.float
 EXPORTS = ("gdn2_workspace_bytes", "gdn2_dims_init", "gdn2_check_args", "gdn2_chunk_fwd",
            "gdn2_chunk_fwd_staged", "gdn2_num_stages", "gdn2_stage_name", "gdn2_launch_count",
            "gdn2_device_status", "gdn2_chunk_fwd_noalloc", "gdn2_recurrent_workspace_bytes",
-           "gdn2_recurrent_fwd", "gdn2_status_string", "gdn2_version")
+           "gdn2_recurrent_fwd", "gdn2_selftest_wait_timeout", "gdn2_status_string", "gdn2_version")
 
 
 class Gdn2Error(RuntimeError):
@@ -98,6 +98,8 @@ def load(path: Optional[str] = None):
     lib.gdn2_recurrent_fwd.restype = ctypes.c_int
     lib.gdn2_device_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
     lib.gdn2_device_status.restype = ctypes.c_int
+    lib.gdn2_selftest_wait_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
+    lib.gdn2_selftest_wait_timeout.restype = ctypes.c_int
     lib.gdn2_status_string.argtypes = [ctypes.c_int]
     lib.gdn2_status_string.restype = ctypes.c_char_p
     lib.gdn2_version.argtypes = []
@@ -285,6 +287,16 @@ def device_status(workspace, stream=None) -> int:
     if st != GDN2_OK:
         raise Gdn2Error(st, "gdn2_device_status")
     return int(s.value)
+
+
+def selftest_wait_timeout(workspace, limit_ns=1_000_000, stream=None) -> int:
+    """Run the bounded-wait self-test (``gdn2_selftest_wait_timeout``) on
+    ``workspace``; returns the call's status (the timeout itself is then read
+    with ``device_status``)."""
+    if stream is None and workspace.is_cuda:
+        stream = torch.cuda.current_stream(workspace.device).cuda_stream
+    return int(load().gdn2_selftest_wait_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                                 int(limit_ns), stream))
 
 
 def stage_names(dims: Dims):

@@ -307,6 +307,22 @@ GDN2_API gdn2_status gdn2_chunk_fwd_noalloc(const void *q, const void *k, const 
                                             const void *initial_state, const void *cu_seqlens, void *out,
                                             void *final_state, const gdn2_dims *dims, void *stream);
 
+/*
+ * Self-test of the device-side failure detection.  Every wait in the
+ * tensor-core kernels is bounded in wall time; a wait that runs out records
+ * GDN2_ERR_TIMEOUT in the workspace status word and the kernel returns, so
+ * the CUDA context stays usable.  This call launches one small kernel that
+ * waits, through the same bounded wait, on a barrier that nothing completes,
+ * for limit_ns nanoseconds (1 000 .. 100 000 000), then records the timeout.
+ * Afterwards gdn2_device_status(workspace) reports GDN2_ERR_TIMEOUT.
+ *   workspace        device buffer of at least 64 bytes (its status words are
+ *                    overwritten); workspace_bytes its size
+ * Returns GDN2_ERR_NULL / GDN2_ERR_WORKSPACE / GDN2_ERR_SHAPE (limit out of
+ * range) / GDN2_ERR_ARCH before any launch, else GDN2_OK once enqueued.
+ */
+GDN2_API gdn2_status gdn2_selftest_wait_timeout(void *workspace, size_t workspace_bytes, uint64_t limit_ns,
+                                                void *stream);
+
 /* Static, human-readable text for a status code.  Host-only. */
 GDN2_API const char *gdn2_status_string(int status);
 

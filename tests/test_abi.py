@@ -210,3 +210,15 @@ def test_state_segments_host_logic(lib):
     assert gdn2.launch_count(many) == 3
     short = _dims(lib, T=1024, N=1, H=2, HV=2, K=128, V=128)    # 16 chunks: too short to split
     assert gdn2.launch_count(short) == 3
+
+
+def test_selftest_wait_timeout_argument_checks(lib):
+    """The bounded-wait self-test validates its arguments before any launch;
+    without a device a valid call reports ERR_ARCH."""
+    ws = ctypes.c_void_p(BASE)
+    assert lib.gdn2_selftest_wait_timeout(None, 64, 1_000_000, None) == 1      # ERR_NULL
+    assert lib.gdn2_selftest_wait_timeout(ws, 32, 1_000_000, None) == 5        # ERR_WORKSPACE
+    assert lib.gdn2_selftest_wait_timeout(ws, 64, 10, None) == 2               # limit below 1 us
+    assert lib.gdn2_selftest_wait_timeout(ws, 64, 10**9, None) == 2            # limit above 100 ms
+    if not torch.cuda.is_available():
+        assert lib.gdn2_selftest_wait_timeout(ws, 64, 1_000_000, None) == 6    # ERR_ARCH
