@@ -399,49 +399,55 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         }
         // outputs packed two channels per 32-bit word as they are produced
         uint32_t wLk[4], wLq[4], wkr[4], wX1[4], wQe[4], wKd[4], wr0[4], wr2[4], wr3[4];
-        auto cmp = [](const float4 &v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; };
         const float4 z4f = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int x2 = 0; x2 < 4; ++x2) {
-            // per-channel tables for channels cb + 4 (x2 / 2) .. + 3 (16-byte loads)
-            const int c4 = cb + 4 * (x2 / 2);
-            const float4 vB = I > 0 ? *reinterpret_cast<const float4 *>(gE + (I - 1) * D + c4) : z4f;
-            const float4 vE = *reinterpret_cast<const float4 *>(gE + I * D + c4);
-            const float4 vL = *reinterpret_cast<const float4 *>(gE + 3 * D + c4);
-            const float4 vG = *reinterpret_cast<const float4 *>(tGB + I * D + c4);
-            const float4 vI = *reinterpret_cast<const float4 *>(tI + I * D + c4);
-            const float4 v2 = *reinterpret_cast<const float4 *>(t2 + (I & 1) * D + c4);
-            const float4 v3 = *reinterpret_cast<const float4 *>(t2 + D + c4);
-            float lk[2], lq[2], kr[2], x1[2], qe[2], kd[2], r0[2], r2[2], r3[2];
+        for (int hh = 0; hh < 2; ++hh) {
+            // per-channel tables for channels cb + 4 hh .. + 3: one 16-byte load
+            // each, shared by the four channels
+            const int c4 = cb + 4 * hh;
+            const float4 vB4 = I > 0 ? *reinterpret_cast<const float4 *>(gE + (I - 1) * D + c4) : z4f;
+            const float4 vE4 = *reinterpret_cast<const float4 *>(gE + I * D + c4);
+            const float4 vL4 = *reinterpret_cast<const float4 *>(gE + 3 * D + c4);
+            const float4 vG4 = *reinterpret_cast<const float4 *>(tGB + I * D + c4);
+            const float4 vI4 = *reinterpret_cast<const float4 *>(tI + I * D + c4);
+            const float4 v24 = *reinterpret_cast<const float4 *>(t2 + (I & 1) * D + c4);
+            const float4 v34 = *reinterpret_cast<const float4 *>(t2 + D + c4);
+            const float vB[4] = {vB4.x, vB4.y, vB4.z, vB4.w}, vE[4] = {vE4.x, vE4.y, vE4.z, vE4.w};
+            const float vL[4] = {vL4.x, vL4.y, vL4.z, vL4.w}, vG[4] = {vG4.x, vG4.y, vG4.z, vG4.w};
+            const float vI[4] = {vI4.x, vI4.y, vI4.z, vI4.w}, v2[4] = {v24.x, v24.y, v24.z, v24.w};
+            const float v3[4] = {v34.x, v34.y, v34.z, v34.w};
+            float lk[4], lq[4], kr[4], x1[4], qe[4], kd[4], r0[4], r2[4], r3[4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int x = 2 * x2 + e;
-                const int ce = x & 3;  // component in the 16-byte table loads
+            for (int ce = 0; ce < 4; ++ce) {
+                const int x = 4 * hh + ce;
                 const float gt = Gr[8 * j + x];
-                const float F = ex2(gt - cmp(vB, ce));                // e^{G_t - G_{B_I}}
-                const float eR = ex2(cmp(vE, ce) - gt);               // e^{G_{E_I} - G_t}
-                const float eL = ex2(cmp(vL, ce) - gt);               // e^{G_L - G_t}
-                const float eGB = cmp(vG, ce);                        // e^{G_{B_I}}
+                const float F = ex2(gt - vB[ce]);                // e^{G_t - G_{B_I}}
+                const float eR = ex2(vE[ce] - gt);               // e^{G_{E_I} - G_t}
+                const float eL = ex2(vL[ce] - gt);               // e^{G_L - G_t}
                 const float kx = kk[x] * kscale;
-                lk[e] = bb[x] * kx * F;
-                lq[e] = qq[x] * qscale * F;
-                kr[e] = kx * eR;
-                x1[e] = lk[e] * eGB;
-                qe[e] = lq[e] * eGB;
-                kd[e] = kx * eL;
-                r0[e] = kr[e] * cmp(vI, ce);                          // row of R_I
-                r2[e] = kr[e] * cmp(v2, ce);                          // row of R_{I+2}, I <= 1
-                r3[e] = r2[e] * cmp(v3, ce);                          // row of R_3, I = 0
+                lk[ce] = bb[x] * kx * F;
+                lq[ce] = qq[x] * qscale * F;
+                kr[ce] = kx * eR;
+                x1[ce] = lk[ce] * vG[ce];                        // * e^{G_{B_I}}
+                qe[ce] = lq[ce] * vG[ce];
+                kd[ce] = kx * eL;
+                r0[ce] = kr[ce] * vI[ce];                        // row of R_I
+                r2[ce] = kr[ce] * v2[ce];                        // row of R_{I+2}, I <= 1
+                r3[ce] = r2[ce] * v3[ce];                        // row of R_3, I = 0
             }
-            wLk[x2] = pack_bf2(lk[0], lk[1]);
-            wLq[x2] = pack_bf2(lq[0], lq[1]);
-            wkr[x2] = pack_bf2(kr[0], kr[1]);
-            wr0[x2] = pack_bf2(r0[0], r0[1]);
-            wr2[x2] = pack_bf2(r2[0], r2[1]);
-            wr3[x2] = pack_bf2(r3[0], r3[1]);
-            wX1[x2] = pack_h2(x1[0], x1[1]);
-            wQe[x2] = pack_h2(qe[0], qe[1]);
-            wKd[x2] = pack_h2(kd[0], kd[1]);
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int x2 = 2 * hh + e2, a = 2 * e2;
+                wLk[x2] = pack_bf2(lk[a], lk[a + 1]);
+                wLq[x2] = pack_bf2(lq[a], lq[a + 1]);
+                wkr[x2] = pack_bf2(kr[a], kr[a + 1]);
+                wr0[x2] = pack_bf2(r0[a], r0[a + 1]);
+                wr2[x2] = pack_bf2(r2[a], r2[a + 1]);
+                wr3[x2] = pack_bf2(r3[a], r3[a + 1]);
+                wX1[x2] = pack_h2(x1[a], x1[a + 1]);
+                wQe[x2] = pack_h2(qe[a], qe[a + 1]);
+                wKd[x2] = pack_h2(kd[a], kd[a + 1]);
+            }
         }
         auto u4 = [](const uint32_t (&w)[4]) { return make_uint4(w[0], w[1], w[2], w[3]); };
         const int kb = cb / 64, chunk = (cb % 64) / 8;
