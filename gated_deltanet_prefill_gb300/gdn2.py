@@ -289,6 +289,119 @@ def device_status(workspace, stream=None) -> int:
     return int(s.value)
 
 
+class _SlicedRunner:
+    """HostRunner for few sequences: every sequence is cut in time into
+    ``slices`` pieces of whole 64-token chunks (the last piece takes the
+    remainder).  Piece j of all sequences is packed into a device staging
+    buffer (two, alternating), run as one forward whose initial state is
+    piece j - 1's final state (two state buffers, alternating), and its output
+    rows are copied back into their places in the pinned host output."""
+
+    def __init__(self, host, impl, use_qk_l2norm, output_final_state, slices):
+        self.host, self.impl, self.l2, self.S = host, impl, use_qk_l2norm, slices
+        T, HV, V = host["v"].shape
+        K = host["q"].shape[2]
+        cu = [int(x) for x in host["cu_seqlens"].tolist()]
+        self.N = N = len(cu) - 1
+        sdt = host["h0"].dtype if host.get("h0") is not None else torch.float32
+        self.keys = [k for k in ("q", "k", "v", "g", "beta", "w") if torch.is_tensor(host.get(k))]
+        rows = max(self._plan(cu)[1])
+        self.stage = [{k: torch.empty((max(rows, 1),) + tuple(host[k].shape[1:]), dtype=host[k].dtype,
+                                      device="cuda") for k in self.keys} for _ in range(2)]
+        self.out_stage = [torch.empty((max(rows, 1), HV, V), dtype=host["q"].dtype, device="cuda")
+                          for _ in range(2)]
+        self.state = [torch.empty((N, HV, K, V), dtype=sdt, device="cuda") for _ in range(2)]
+        self.h0 = torch.empty_like(host["h0"], device="cuda") if torch.is_tensor(host.get("h0")) else None
+        self.out_host = torch.empty((T, HV, V), dtype=host["q"].dtype).pin_memory()
+        self.fs_host = torch.empty((N, HV, K, V), dtype=sdt).pin_memory() if output_final_state else None
+        cu_dt = host["cu_seqlens"].dtype
+        self.cu_host = [torch.empty(N + 1, dtype=cu_dt).pin_memory() for _ in range(slices)]
+        self.cu_dev = [torch.empty(N + 1, dtype=cu_dt, device="cuda") for _ in range(slices)]
+        self.cu_ev = [None] * slices
+        dims = make_dims(self.stage[0]["q"], self.stage[0]["k"], self.stage[0]["v"], self.stage[0].get("g"),
+                         self.stage[0].get("beta"), self.stage[0].get("w"), self.out_stage[0],
+                         self.cu_dev[0], use_qk_l2norm, impl, False, sdt)
+        self.ws = torch.empty(max(workspace_bytes(dims), 256), dtype=torch.uint8, device="cuda")
+        self.streams = [torch.cuda.Stream() for _ in range(3)]
+        self.h2d_bytes = sum(v.numel() * v.element_size() for v in host.values() if torch.is_tensor(v))
+        self.d2h_bytes = self.out_host.numel() * self.out_host.element_size() + (
+            0 if self.fs_host is None else self.fs_host.numel() * self.fs_host.element_size())
+
+    def _plan(self, cu):
+        """Token bounds of every piece: b[n][j] = offset of piece j in sequence
+        n; returns (b, rows of each piece)."""
+        S = self.S
+        b = []
+        for n in range(self.N):
+            L = cu[n + 1] - cu[n]
+            b.append([64 * ((L * j) // (64 * S)) for j in range(S)] + [L])
+        rows = [sum(b[n][j + 1] - b[n][j] for n in range(self.N)) for j in range(S)]
+        return b, rows
+
+    def __call__(self):
+        s_in, s_cmp, s_out = self.streams
+        caller = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(caller)
+        for st in self.streams:
+            st.wait_event(start)
+        h = self.host
+        cu = [int(x) for x in h["cu_seqlens"].tolist()]
+        b, _ = self._plan(cu)
+        ev_c, ev_o = [None] * self.S, [None] * self.S
+        if self.h0 is not None:
+            with torch.cuda.stream(s_in):
+                self.h0.copy_(h["h0"], non_blocking=True)
+        for j in range(self.S):
+            buf = j % 2
+            # piece j's cu_seqlens (host arithmetic into a pinned buffer whose
+            # previous copy to the device must be done)
+            if self.cu_ev[j] is not None:
+                self.cu_ev[j].synchronize()
+            offs = [0]
+            for n in range(self.N):
+                offs.append(offs[-1] + b[n][j + 1] - b[n][j])
+            self.cu_host[j].copy_(torch.tensor(offs, dtype=self.cu_host[j].dtype))
+            with torch.cuda.stream(s_in):
+                if j >= 2:
+                    s_in.wait_event(ev_c[j - 2])  # the staging buffer was read by forward j - 2
+                for n in range(self.N):
+                    a, e = cu[n] + b[n][j], cu[n] + b[n][j + 1]
+                    if e > a:
+                        for k in self.keys:
+                            self.stage[buf][k][offs[n]:offs[n + 1]].copy_(h[k][a:e], non_blocking=True)
+                self.cu_dev[j].copy_(self.cu_host[j], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+                self.cu_ev[j] = ev_in
+            s_cmp.wait_event(ev_in)
+            if j >= 2:
+                s_cmp.wait_event(ev_o[j - 2])  # the output staging was copied out
+            with torch.cuda.stream(s_cmp):
+                rows = offs[-1]
+                st = self.stage[buf]
+                sl = lambda k: st[k][:rows] if k in st else None
+                init = self.h0 if j == 0 else self.state[(j - 1) % 2]
+                chunk_gdn2_fwd(sl("q"), sl("k"), sl("v"), sl("g"), sl("beta"), sl("w"), scale=h.get("scale"),
+                               initial_state=init, cu_seqlens=self.cu_dev[j], use_qk_l2norm=self.l2,
+                               out=self.out_stage[buf][:rows], final_state=self.state[j % 2], workspace=self.ws,
+                               impl=self.impl, stream=s_cmp.cuda_stream)
+                ev_c[j] = torch.cuda.Event()
+                ev_c[j].record(s_cmp)
+            s_out.wait_event(ev_c[j])
+            with torch.cuda.stream(s_out):
+                for n in range(self.N):
+                    a, e = cu[n] + b[n][j], cu[n] + b[n][j + 1]
+                    if e > a:
+                        self.out_host[a:e].copy_(self.out_stage[buf][offs[n]:offs[n + 1]], non_blocking=True)
+                if j == self.S - 1 and self.fs_host is not None:
+                    self.fs_host.copy_(self.state[j % 2], non_blocking=True)
+                ev_o[j] = torch.cuda.Event()
+                ev_o[j].record(s_out)
+        caller.wait_event(ev_o[-1])
+        return self.out_host, self.fs_host
+
+
 def selftest_wait_timeout(workspace, limit_ns=1_000_000, stream=None) -> int:
     """Run the bounded-wait self-test (``gdn2_selftest_wait_timeout``) on
     ``workspace``; returns the call's status (the timeout itself is then read
@@ -312,15 +425,29 @@ def launch_count(dims: Dims) -> int:
 class HostRunner:
     """End-to-end call from HOST buffers: pinned host inputs are copied to
     preallocated device buffers, the forward runs, and the output and final
-    state are copied back into pinned host buffers.  The sequences are taken
-    in contiguous groups (at most ``groups``, balanced by tokens): the
-    host-to-device copy of group i + 1, the forward of group i and the
-    device-to-host copy of group i - 1 run on three streams at once, so the
-    call is bounded by the host link rather than by the kernels.  The caller's
-    stream waits for the last copy.  Device buffers and the workspace are
-    allocated once (torch) and reused."""
+    state are copied back into pinned host buffers.  The work is cut into
+    pieces whose host-to-device copy, forward and device-to-host copy run on
+    three streams at once (piece i + 1 in, piece i computed, piece i - 1
+    out), so the call is bounded by the host link rather than by the kernels.
+    The caller's stream waits for the last copy.  Device buffers and the
+    workspace are allocated once (torch) and reused.
 
-    def __init__(self, host: dict, impl="tc", use_qk_l2norm=False, output_final_state=True, groups=4):
+    Pieces: with at most ``max_sliced_seqs`` sequences (each piece takes
+    one copy per sequence and tensor) every sequence is cut in time into
+    ``slices`` pieces of whole 64-token chunks, each forward starting from
+    the previous piece's final state (_SlicedRunner); with more sequences,
+    or slices <= 1, contiguous sequence groups (at most ``groups``, balanced
+    by tokens)."""
+
+    def __new__(cls, host: dict, impl="tc", use_qk_l2norm=False, output_final_state=True, groups=4,
+                slices=8, max_sliced_seqs=8):
+        n_seq = host["cu_seqlens"].numel() - 1
+        if cls is HostRunner and slices and slices > 1 and 0 < n_seq <= max_sliced_seqs:
+            return _SlicedRunner(host, impl, use_qk_l2norm, output_final_state, slices)
+        return super().__new__(cls)
+
+    def __init__(self, host: dict, impl="tc", use_qk_l2norm=False, output_final_state=True, groups=4,
+                 slices=8, max_sliced_seqs=8):
         self.host = host
         self.impl = impl
         self.l2 = use_qk_l2norm

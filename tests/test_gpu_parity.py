@@ -249,21 +249,26 @@ def test_full_size_sampled(cuda_lib, impl, index):
     assert eo <= TOL and eh <= TOL, "%s/%s: o err %.3e, state err %.3e" % (wl.name, impl, eo, eh)
 
 
-@pytest.mark.parametrize("groups", [1, 3])
-def test_host_runner_matches_device_call(cuda_lib, groups):
-    """HostRunner (pinned host buffers, sequence groups pipelined over three
-    streams) returns what the device call returns, and matches the oracle."""
-    wl = inputs.small("host", [100, 1, 0, 64, 250, 33], H=2, HV=4, K=128, V=128, g_max=1.0, beta_max=2.0,
+@pytest.mark.parametrize("groups,slices", [(1, 0), (3, 0), (4, 4), (4, 8)])
+def test_host_runner_matches_device_call(cuda_lib, groups, slices):
+    """HostRunner (pinned host buffers, pieces pipelined over three streams)
+    matches the oracle.  Sequence groups (slices = 0) return exactly what one
+    device call returns; time slices (every sequence cut into pieces of whole
+    chunks, the state carried from piece to piece) differ from it by rounding
+    only."""
+    wl = inputs.small("host", [100, 1, 0, 64, 250, 33, 700], H=2, HV=4, K=128, V=128, g_max=1.0, beta_max=2.0,
                       h0_std=0.05, seed=38)
     d = inputs.generate(wl)
     host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in d.items()}
-    runner = cuda_lib.HostRunner(host, groups=groups)
+    runner = cuda_lib.HostRunner(host, groups=groups, slices=slices)
+    assert (type(runner).__name__ == "_SlicedRunner") == (slices > 0)
     for _ in range(2):  # twice in a row: buffers are reused
         o_h, h_h = runner()
     torch.cuda.synchronize()
     o_d, h_d = run_gpu(cuda_lib, to_dev(d), "tc")
-    assert rel_max(o_h.float().numpy(), o_d.float().cpu().numpy()) <= 1e-6
-    assert rel_max(h_h.numpy(), h_d.cpu().numpy()) <= 1e-6
+    tol_dev = 1e-6 if slices == 0 else TOL
+    assert rel_max(o_h.float().numpy(), o_d.float().cpu().numpy()) <= tol_dev
+    assert rel_max(h_h.numpy(), h_d.cpu().numpy()) <= tol_dev
     o_ref, h_ref = run_oracle(d)
     assert rel_max(o_h.float().numpy(), o_ref) <= TOL
     assert rel_max(h_h.numpy(), h_ref) <= TOL
