@@ -67,7 +67,9 @@ def parse():
 
 
 # ---------------------------------------------------------------------------
-# byte accounting (per launch), see DESIGN.md "Roofline accounting"
+# byte accounting (per launch): the algorithmic bytes a stage must move, each
+# of its inputs read once and each output written once; the roofline's
+# `achieved` is these bytes over the stage's CUDA-event time
 # ---------------------------------------------------------------------------
 def n_chunks(wl):
     return sum((L + 63) // 64 for L in wl.lens)
