@@ -249,7 +249,9 @@ GDN2_API size_t gdn2_recurrent_workspace_bytes(const gdn2_dims *dims);
  * overlap is GDN2_ERR_ALIAS).  dims->impl is ignored.  Each token costs a
  * pass over the state held on chip; the state is read and written once per
  * call, so the call suits few tokens per sequence (gdn2_chunk_fwd is the
- * prefill path).  Two launches: a cu_seqlens check, then one CTA per
+ * prefill path; measured on a GB300 with 128 sequences and 32 heads of 128
+ * channels, the chunked call is the faster one from about 20 tokens per
+ * sequence on).  Two launches: a cu_seqlens check, then one CTA per
  * (sequence, value head, 32 value columns).
  */
 GDN2_API gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void *v, const void *g,
