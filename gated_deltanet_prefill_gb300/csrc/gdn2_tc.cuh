@@ -70,6 +70,30 @@ __device__ __forceinline__ bool mbar_wait_ns(uint64_t *bar, uint32_t parity, uin
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return mbar_wait_ns(bar, parity, kWaitLimitNs);
 }
+// The same bounded wait with a suspend-time hint: a thread whose phase is not
+// complete is parked by the hardware (for at most hint_ns per try) until the
+// phase completes, instead of polling.  Which waits gain from it is measured
+// per kernel and per role.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_parked(uint64_t *bar, uint32_t parity) {
+    constexpr uint32_t kHintNs = 20000;
+    if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity, kHintNs)) return true;
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+}
 
 // The same wait taken by a whole warp, with a warp-uniform result, so that the
 // warp-collective tcgen05 loads and stores that follow never diverge.

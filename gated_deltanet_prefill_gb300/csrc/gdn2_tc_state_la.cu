@@ -17,8 +17,9 @@
 //   epi U_c  = Ut_c - D_c[64:128]          fp16 image (two buffers)
 //   Me  S    = E_c + Kd_c^T U_c            S_{c+1}, fp32 in TMEM
 //   Md  D_c[0:64] += P_c U_c               output -> scale -> global
-// Tensor pipe order per chunk c: Ma_{c+1}; once U_c is ready Mc_{c+1} (the
-// chain), Me_c, Md_c; then Mb_{c+2}.  Accumulators D are triple-buffered so
+// Tensor pipe order per chunk c, once E_c, U_c and XY_{c+1} are ready: Ma_{c+1},
+// Mc_{c+1} (the chain), Me_c, Md_c as one burst of 20 instructions; the stage
+// of chunk c is released; then Mb_{c+2}.  Accumulators D are triple-buffered so
 // that an output epilogue never delays the next chunk's first product.
 //
 // Warps (24): 0 bulk-copy producer, 1 MMA issuer (and TMEM owner), 2-3 and
@@ -139,6 +140,11 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
         }
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
+        // Its waits park the thread (the other roles poll), and it waits for
+        // all of a chunk's inputs before issuing: MMAs issued in short bursts
+        // pay the tensor pipe's fill latency per burst.  On two sequences of
+        // 16384 tokens with 32 value heads: 0.465 -> 0.438 ms (parked waits)
+        // -> 0.425 ms (one burst, stage released before the XY product).
         if (lane == 0 && nck > 0) {
             constexpr uint32_t idB = idesc_fp16(128, VT, false, true);   // B = state / U image (MN-major)
             constexpr uint32_t idS = idesc_fp16(128, VT, true, true);    // A = Kd^T (MN-major)
@@ -163,13 +169,13 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
                 for (int kk = 0; kk < D / 16; ++kk) mma_f16(tXY, dA + kmaj(128, kk), dK + kmaj(64, kk), idXY, kk > 0);
                 mma_commit(&xy_full);
             };
-            if (!mbar_wait(&full_bar[0], 0) || !mbar_wait(&s_ready, 0)) ok = false;
+            if (!mbar_wait_parked(&full_bar[0], 0) || !mbar_wait_parked(&s_ready, 0)) ok = false;
             if (ok) {
                 tc_fence_after();
                 product_a1(0);
                 mma_commit(&d_full[0]);
                 if (nck > 1) {
-                    if (!mbar_wait(&full_bar[1 % NSTAGE], 0)) {
+                    if (!mbar_wait_parked(&full_bar[1 % NSTAGE], 0)) {
                         ok = false;
                     } else {
                         tc_fence_after();
@@ -181,18 +187,17 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
                 const bool next = c + 1 < nck;
                 // E_c is ready: its image (for D_{c+1}) and Tensor Memory (for
                 // the state update)
-                if (!mbar_wait(&s_ready, (c + 1) & 1) ||
-                    (next && c + 1 >= 3 && !mbar_wait(&d_free[(c + 1) % 3], ((c - 2) / 3) & 1))) {
+                if (!mbar_wait_parked(&s_ready, (c + 1) & 1) ||
+                    (next && c + 1 >= 3 && !mbar_wait_parked(&d_free[(c + 1) % 3], ((c - 2) / 3) & 1))) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait_parked(&u_ready, c & 1) || (next && !mbar_wait_parked(&xy_ready, c & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (next) product_a1(c + 1);
-                if (!mbar_wait(&u_ready, c & 1) || (next && !mbar_wait(&xy_ready, c & 1))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
                 const uint64_t dU = desc_mnmajor(sU(c), 64, 0);
                 if (next) {  // the chain: D_{c+1} += XY_{c+1} U_c
 #pragma unroll
@@ -207,19 +212,19 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) mma_f16(tD(c), dP + kmaj(128, kk), dU + mnmaj(kk), idB, 1);
                 mma_commit(&o_full[c % 3]);
+                mma_commit(&empty_bar[c % NSTAGE]);
                 if (c + 2 < nck) {
-                    if (!mbar_wait(&full_bar[(c + 2) % NSTAGE], ((c + 2) / NSTAGE) & 1)) {
+                    if (!mbar_wait_parked(&full_bar[(c + 2) % NSTAGE], ((c + 2) / NSTAGE) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     product_xy(c + 2);
                 }
-                mma_commit(&empty_bar[c % NSTAGE]);
             }
             if (!ok) set_timeout_la(p);
             mma_commit(&drain);
-            if (!mbar_wait(&drain, 0)) set_timeout_la(p);
+            if (!mbar_wait_parked(&drain, 0)) set_timeout_la(p);
         }
     } else if (warp >= 8 && warp < 16) {
         // ------------------------- state epilogue: E_c = eGL_c S_c (rows = key channels)
