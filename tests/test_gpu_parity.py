@@ -278,9 +278,10 @@ def test_host_runner_matches_device_call(cuda_lib, groups, slices):
 def test_state_kernels_64_column_tiles(cuda_lib, monkeypatch, lookahead):
     """Both state kernels of the 64-column tile (few (sequence, head) pairs):
     the one-chunk lookahead kernel (default) and the plain one; ragged
-    sequences from empty to several stage wraps, decay stress, initial state."""
+    sequences of 0 to 15 chunks (every count up to one past the three record
+    stages, then several wraps), decay stress, initial state."""
     monkeypatch.setenv("GDN2_STATE_LOOKAHEAD", lookahead)
-    wl = inputs.small("vt64_%s" % lookahead, [0, 1, 64, 65, 200, 900], H=2, HV=4, K=128, V=128, g_max=2.0,
+    wl = inputs.small("vt64_%s" % lookahead, [0, 1, 64, 65, 129, 192, 200, 900], H=2, HV=4, K=128, V=128, g_max=2.0,
                       beta_max=2.0, h0_std=0.05, seed=95)
     d = inputs.generate(wl)
     o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
