@@ -140,6 +140,7 @@ cudaError_t launch_simt_output(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_intra(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_state(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_state_la(const Params &p, cudaStream_t s);
+cudaError_t launch_tc_state_la128(const Params &p, cudaStream_t s);
 cudaError_t launch_tc_scan_combine(const Params &p, cudaStream_t s);
 // Segments per sequence of the chunk-parallel state pass for `d` (1 = none).
 int scan_segments(const gdn2_dims &d);

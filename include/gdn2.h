@@ -191,10 +191,11 @@ GDN2_API gdn2_status gdn2_check_args(const void *q, const void *k, const void *v
  * the host at each call (no device state).  Where the driver rejects a layout
  * (for example a zero head stride) it copies those rows one by one instead;
  * the environment variable GDN2_ROW_COPIES=1 forces that path (diagnostics).
- * When few (sequence, head) pairs make the state pass use 64-column V tiles,
- * it runs a kernel with a one-chunk lookahead; GDN2_STATE_LOOKAHEAD=0
- * selects the plain state kernel instead (diagnostics; same results up to
- * rounding).
+ * The sequential state pass runs kernels with a one-chunk lookahead (one for
+ * 64-column V tiles, used when few (sequence, head) pairs leave SMs idle, one
+ * for 128-column tiles); GDN2_STATE_LOOKAHEAD=0 selects the plain state
+ * kernel for both, =64 for the 128-column tiles only (diagnostics; same
+ * results up to rounding).
  */
 GDN2_API gdn2_status gdn2_chunk_fwd(const void *q, const void *k, const void *v, const void *g,
                            const void *beta, const void *w, float scale,

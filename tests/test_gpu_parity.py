@@ -294,6 +294,28 @@ def test_state_kernels_64_column_tiles(cuda_lib, monkeypatch, lookahead):
     assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
 
 
+@pytest.mark.parametrize("lookahead", ["1", "64"])
+def test_state_kernels_128_column_tiles(cuda_lib, monkeypatch, lookahead):
+    """Both state kernels of the 128-column tile (more (sequence, head) pairs
+    than half the SMs): the lookahead kernel (default) and the plain one
+    (GDN2_STATE_LOOKAHEAD=64); ragged sequences of 0 to 15 chunks, grouped
+    value heads, decay stress, initial state."""
+    monkeypatch.setenv("GDN2_STATE_LOOKAHEAD", lookahead)
+    lens = [0, 1, 64, 65, 129, 192, 200, 900, 333, 64]
+    wl = inputs.small("vt128_%s" % lookahead, lens, H=4, HV=8, K=128, V=128, g_max=2.0, beta_max=2.0,
+                      h0_std=0.05, seed=96)
+    assert 2 * len(lens) * 8 > 152  # the host picks 128-column tiles
+    d = inputs.generate(wl)
+    o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                                       initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
+    dd = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in d.items()}
+    o, hT = cuda_lib.chunk_gdn2_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["w"], scale=dd["scale"],
+                                    initial_state=dd["h0"], cu_seqlens=dd["cu_seqlens"], state_segments=1)
+    torch.cuda.synchronize()
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
+
+
 def test_many_short_sequences(cuda_lib):
     """2,500 ragged sequences of 0-130 tokens (more than the chunk map's 1024
     threads: its scans and its longest-first counting sort loop), grouped
