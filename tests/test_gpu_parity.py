@@ -294,24 +294,39 @@ def test_state_kernels_64_column_tiles(cuda_lib, monkeypatch, lookahead):
     assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
 
 
-@pytest.mark.parametrize("lookahead", ["1", "64"])
-def test_state_kernels_128_column_tiles(cuda_lib, monkeypatch, lookahead):
+@pytest.mark.parametrize("lookahead,variant", [("1", False), ("64", False), ("1", True)])
+def test_state_kernels_128_column_tiles(cuda_lib, monkeypatch, lookahead, variant):
     """Both state kernels of the 128-column tile (more (sequence, head) pairs
     than half the SMs): the lookahead kernel (default) and the plain one
     (GDN2_STATE_LOOKAHEAD=64); ragged sequences of 0 to 15 chunks, grouped
-    value heads, decay stress, initial state."""
+    value heads, decay stress, initial state.  The variant case runs the
+    lookahead kernel on fp16 inputs, fp16 g, a bf16 V-major state, the fused
+    q/k L2 norm and no w gate."""
     monkeypatch.setenv("GDN2_STATE_LOOKAHEAD", lookahead)
     lens = [0, 1, 64, 65, 129, 192, 200, 900, 333, 64]
-    wl = inputs.small("vt128_%s" % lookahead, lens, H=4, HV=8, K=128, V=128, g_max=2.0, beta_max=2.0,
-                      h0_std=0.05, seed=96)
+    wl = inputs.small("vt128_%s_%d" % (lookahead, variant), lens, H=4, HV=8, K=128, V=128, g_max=2.0,
+                      beta_max=2.0, h0_std=0.05, seed=96)
     assert 2 * len(lens) * 8 > 152  # the host picks 128-column tiles
     d = inputs.generate(wl)
+    kw = {}
+    if variant:
+        d["w"] = None
+        for k in ("q", "k", "v", "beta"):
+            d[k] = d[k].float().to(torch.float16)
+        d["g"] = d["g"].to(torch.float16)
+        d["h0"] = d["h0"].to(torch.bfloat16)
+        kw = dict(use_qk_l2norm=True, state_v_major=True, state_dtype=torch.bfloat16)
     o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
-                                       initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
+                                       initial_state=d["h0"], cu_seqlens=d["cu_seqlens"],
+                                       use_qk_l2norm=variant)
     dd = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in d.items()}
+    h0 = dd["h0"].transpose(-1, -2).contiguous() if variant else dd["h0"]
     o, hT = cuda_lib.chunk_gdn2_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["w"], scale=dd["scale"],
-                                    initial_state=dd["h0"], cu_seqlens=dd["cu_seqlens"], state_segments=1)
+                                    initial_state=h0, cu_seqlens=dd["cu_seqlens"], state_segments=1, **kw)
     torch.cuda.synchronize()
+    hT = hT.float()
+    if variant:
+        hT = hT.transpose(-1, -2)
     assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
     assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
 
