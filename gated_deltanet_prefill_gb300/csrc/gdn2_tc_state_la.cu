@@ -19,9 +19,9 @@
 //   epi U_c  = Ut_c - D_c[64:128]          fp16 image (two buffers)
 //   Me  S    = E_c + Kd_c^T U_c            S_{c+1}, fp32 in TMEM
 //   Md  D_c[0:64] += P_c U_c               output -> scale -> global
-// Tensor pipe order per chunk c, once E_c, U_c and XY_{c+1} are ready: Ma_{c+1},
-// Mc_{c+1} (the chain), Me_c, Md_c as one burst of 20 instructions; the stage
-// of chunk c is released; then Mb_{c+2}.  Accumulators D are triple-buffered so
+// Tensor pipe order per chunk c: Ma_{c+1} once E_c is ready; once U_c and
+// XY_{c+1} are, Mc_{c+1} (the chain), Me_c, Md_c in one burst; the stage of
+// chunk c is released; then Mb_{c+2}.  Accumulators D are triple-buffered so
 // that an output epilogue never delays the next chunk's first product.
 //
 // Warps (24): 0 bulk-copy producer, 1 MMA issuer (and TMEM owner), 2-3 and
@@ -142,11 +142,13 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
         }
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
-        // Its waits park the thread (the other roles poll), and it waits for
-        // all of a chunk's inputs before issuing: MMAs issued in short bursts
-        // pay the tensor pipe's fill latency per burst.  On two sequences of
-        // 16384 tokens with 32 value heads: 0.465 -> 0.438 ms (parked waits)
-        // -> 0.425 ms (one burst, stage released before the XY product).
+        // Its waits park the thread (the other roles poll), and the chunk's
+        // dependent instructions go out in as few bursts as the inputs allow:
+        // MMAs issued in short bursts pay the tensor pipe's fill latency per
+        // burst.  On two sequences of 16384 tokens with 32 value heads: 0.465
+        // -> 0.438 ms (parked waits) -> 0.424 ms (the stage released before
+        // the XY product, Mc/Me/Md in one burst) -> 0.421 ms (Ma issued as
+        // soon as E_c is ready).
         if (lane == 0 && nck > 0) {
             constexpr uint32_t idB = idesc_fp16(128, VT, false, true);   // B = state / U image (MN-major)
             constexpr uint32_t idS = idesc_fp16(128, VT, true, true);    // A = Kd^T (MN-major)
@@ -189,17 +191,18 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
                 const bool next = c + 1 < nck;
                 // E_c is ready: its image (for D_{c+1}) and Tensor Memory (for
                 // the state update)
-                if (!mbar_wait_parked(&s_ready, (c + 1) & 1) ||
-                    (next && c + 1 >= 3 && !mbar_wait_parked(&d_free[(c + 1) % 3], ((c - 2) / 3) & 1))) {
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait_parked(&u_ready, c & 1) || (next && !mbar_wait_parked(&xy_ready, c & 1))) {
+                if ((next && c + 1 >= 3 && !mbar_wait_parked(&d_free[(c + 1) % 3], ((c - 2) / 3) & 1)) ||
+                    !mbar_wait_parked(&s_ready, (c + 1) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (next) product_a1(c + 1);
+                if ((next && !mbar_wait_parked(&xy_ready, c & 1)) || !mbar_wait_parked(&u_ready, c & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
                 const uint64_t dU = desc_mnmajor(sU(c), 64, 0);
                 if (next) {  // the chain: D_{c+1} += XY_{c+1} U_c
 #pragma unroll
@@ -554,7 +557,8 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
         // product goes out as soon as E_c is ready, ahead of the wait for U_c:
         // at 128 columns the U epilogue is the longer chain (long workload,
         // 4 x 32768 tokens: state stage 1.158 -> 1.113 ms, against 1.184 ms
-        // for the plain kernel).
+        // for the plain kernel).  Each pair of waits takes first the barrier
+        // that usually completes first (1.115 -> 1.102 ms).
         if (lane == 0 && nck > 0) {
             constexpr uint32_t idB = idesc_fp16(128, 128, false, true);   // B = state / U image (MN-major)
             constexpr uint32_t idS = idesc_fp16(128, 128, true, true);    // A = Kd^T (MN-major)
@@ -596,14 +600,14 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
                 const bool next = c + 1 < nck;
                 // E_c (image in stage c, and Tensor Memory), U_c and XY_{c+1}
                 // are ready, and D_{c+1}'s buffer is free
-                if (!mbar_wait_parked(&s_ready, (c + 1) & 1) ||
-                    (next && c + 1 >= 2 && !mbar_wait_parked(&d_free[(c + 1) & 1], ((c - 1) >> 1) & 1))) {
+                if ((next && c + 1 >= 2 && !mbar_wait_parked(&d_free[(c + 1) & 1], ((c - 1) >> 1) & 1)) ||
+                    !mbar_wait_parked(&s_ready, (c + 1) & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 if (next) product_a1(c + 1, smem_u32(stage(c) + C::sA1));
-                if (!mbar_wait_parked(&u_ready, c & 1) || (next && !mbar_wait_parked(&xy_ready, c & 1))) {
+                if ((next && !mbar_wait_parked(&xy_ready, c & 1)) || !mbar_wait_parked(&u_ready, c & 1)) {
                     ok = false;
                     break;
                 }
