@@ -348,21 +348,40 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     // w v for this thread's chunks, stored to its operand image after the
     // barrier below (it overwrites the raw rows)
     uint4 wX2[NJ];
+    // raw rows are 256 bytes apart and an eight-lane group holds rows t and
+    // t + 4: rows with bit 2 of t set read each pair of chunks in the other
+    // order, so the two rows of a group hit different banks
+    const bool rsw = (t >> 2) & 1;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        const int cb = 8 * (seg + 4 * j);
-        float vv[8], ww[8];
-        unpack8_in(live ? *reinterpret_cast<const uint4 *>(raw_v + (t * D + cb) * 2) : z4, vv, F16);
-        unpack8_in(live && p.has_w ? *reinterpret_cast<const uint4 *>(raw_w + (t * D + cb) * 2) : z4, ww, F16);
+    for (int j = 0; j < NJ; j += 2) {
+        uint4 rv[2], rw[2];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) ww[x] = (p.has_w || !live) ? ww[x] * vv[x] : vv[x];
-        wX2[j] = pack8_h(ww);
+        for (int h = 0; h < 2; ++h) {
+            const int cb = 8 * (seg + 4 * (j + (h ^ static_cast<int>(rsw))));
+            rv[h] = live ? *reinterpret_cast<const uint4 *>(raw_v + (t * D + cb) * 2) : z4;
+            rw[h] = live && p.has_w ? *reinterpret_cast<const uint4 *>(raw_w + (t * D + cb) * 2) : z4;
+        }
+        auto sel = [](bool c, const uint4 &x, const uint4 &y) {
+            return make_uint4(c ? x.x : y.x, c ? x.y : y.y, c ? x.z : y.z, c ? x.w : y.w);
+        };
+        const uint4 v0 = sel(rsw, rv[1], rv[0]), v1 = sel(rsw, rv[0], rv[1]);
+        const uint4 w0 = sel(rsw, rw[1], rw[0]), w1 = sel(rsw, rw[0], rw[1]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float vv[8], ww[8];
+            unpack8_in(h ? v1 : v0, vv, F16);
+            unpack8_in(h ? w1 : w0, ww, F16);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) ww[x] = (p.has_w || !live) ? ww[x] * vv[x] : vv[x];
+            wX2[j + h] = pack8_h(ww);
+        }
     }
     float Gr[8 * NJ];
-    // G rows are 512 bytes apart, so the same channels of a warp's eight rows
-    // share banks; odd rows load each chunk's two halves in the other order,
-    // which spreads every load instruction over all 32 banks
-    const int gsw = (t & 1) ? 4 : 0;
+    // G rows are 512 bytes apart, so the same channels of different rows share
+    // banks.  A 16-byte load is served eight lanes at a time, and those lanes
+    // hold rows t and t + 4: rows with bit 2 of t set load each chunk's two
+    // halves in the other order, so every eight-lane group covers all 32 banks
+    const int gsw = ((t >> 2) & 1) ? 4 : 0;
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
         const int cb = 8 * (seg + 4 * j);
