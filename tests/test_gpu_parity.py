@@ -86,6 +86,33 @@ def test_missing_gates(cuda_lib, impl):
 
 
 @pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("case", ["linear_attention", "no_write", "scalar_gated_delta"])
+def test_degenerate_gates(cuda_lib, impl, case):
+    """Gates present but degenerate, where the method reduces to a simpler one
+    (the oracle pins check the same reductions on the host): g = 0, beta = 0,
+    w = 1 is cumulative linear attention (A = 0, T = I); w = 0 writes nothing,
+    so the output reads the decayed and erased initial state; g and beta
+    constant over the channels with w = beta is the scalar gated delta rule."""
+    wl = inputs.small("degen_" + case, [0, 1, 63, 64, 200], H=2, HV=4, K=128, V=128, g_max=0.5, beta_max=1.0,
+                      h0_std=0.05, seed=41)
+    d = inputs.generate(wl)
+    if case == "linear_attention":
+        d["g"] = torch.zeros_like(d["g"])
+        d["beta"] = torch.zeros_like(d["beta"])
+        d["w"] = torch.ones_like(d["w"])
+    elif case == "no_write":
+        d["w"] = torch.zeros_like(d["w"])
+    else:
+        d["g"] = d["g"][..., :1].expand_as(d["g"]).contiguous()
+        d["beta"] = d["beta"][..., :1].expand_as(d["beta"]).contiguous()
+        d["w"] = d["beta"].clone()
+    o_ref, h_ref = run_oracle(d)
+    o, hT = run_gpu(cuda_lib, to_dev(d), impl)
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
+
+
+@pytest.mark.parametrize("impl", IMPLS)
 def test_l2norm_in_kernel(cuda_lib, impl):
     wl = inputs.small("l2", [150], H=2, HV=2, K=128, V=128, seed=34)
     d = inputs.generate(wl)
