@@ -147,6 +147,7 @@ WsLayout workspace_layout(const gdn2_dims &d) {
     } else {
         off = (off + 1023) & ~static_cast<size_t>(1023);  // records are 1 KB aligned
         L.rec = take(NC * d.HV * tc_record_bytes(d.K));
+        L.exact_list = take(NC * d.HV * 4);
         const size_t P = static_cast<size_t>(scan_segments(d));
         if (P > 1) {
             const size_t units = static_cast<size_t>(d.N) * (P - 1) * d.HV;
@@ -182,6 +183,7 @@ const char *gdn2_status_string(int status) {
         case GDN2_ERR_IMPL: return "unknown implementation selector";
         case GDN2_ERR_TIMEOUT: return "a tensor-core kernel timed out waiting on its own pipeline (outputs invalid)";
         case GDN2_ERR_NOALLOC_LIMIT: return "problem needs more scratch than the allocation-free entry point holds (GDN2_NOALLOC_SCRATCH_BYTES)";
+        case GDN2_ERR_RANGE: return "a value passed the range of the fp16 intermediates and was clipped (outputs invalid)";
         default: return "unknown status";
     }
 }
@@ -353,6 +355,7 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     p.hbuf = reinterpret_cast<bf16 *>(ws + L.hbuf);
     p.vnew = reinterpret_cast<bf16 *>(ws + L.vnew);
     p.rec = reinterpret_cast<uint8_t *>(ws + L.rec);
+    p.exact_list = reinterpret_cast<int *>(ws + L.exact_list);
     // State-kernel V tile: V columns of S evolve independently, so splitting V
     // is exact.  Two 64-column tiles per (sequence, head) when the untiled
     // grid would leave more than half of the SMs idle.
@@ -454,8 +457,8 @@ int32_t gdn2_launch_count(const gdn2_dims *d) {
     if (!d || !shape_ok(*d)) return 0;
     if (d->N == 0) return 1;
     const int64_t ncmax = nc_max(*d);
-    if (d->impl != GDN2_IMPL_SIMT)  // map, intra, state (+ transitions and combine when segmented)
-        return 1 + (ncmax > 0 ? 1 : 0) + 1 + (scan_segments(*d) > 1 ? 2 : 0);
+    if (d->impl != GDN2_IMPL_SIMT)  // map, intra (two passes), state (+ transitions and combine when segmented)
+        return 1 + (ncmax > 0 ? 2 : 0) + 1 + (scan_segments(*d) > 1 ? 2 : 0);
     int n = 1;                                          // chunk map
     n += (d->use_qk_l2norm && d->T_tot > 0) ? 1 : 0;    // q/k L2 norm
     n += ncmax > 0 ? 1 : 0;                             // cumsum
@@ -485,13 +488,15 @@ gdn2_status gdn2_chunk_fwd_staged(const void *q, const void *k, const void *v, c
 gdn2_status gdn2_device_status(const void *workspace, void *stream, int32_t *status) {
     if (!workspace || !status) return GDN2_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int32_t host[3] = {0, 0, 0};  // the status words sit at offset 0 of the workspace
+    // the status words sit at offset 0 of the workspace: [0] cu_seqlens,
+    // [1] chunk count, [2] wait timeout, [3] 16-bit range
+    int32_t host[4] = {0, 0, 0, 0};
     if (cudaMemcpyAsync(host, workspace, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return GDN2_ERR_CUDA;
     }
-    *status = host[0] != GDN2_OK ? host[0] : host[2];
+    *status = host[0] != GDN2_OK ? host[0] : host[2] != GDN2_OK ? host[2] : host[3];
     return GDN2_OK;
 }
 

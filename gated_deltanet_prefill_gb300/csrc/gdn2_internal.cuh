@@ -43,7 +43,8 @@ struct Params {
     int state_vmajor, state_bf16;
     int NCmax;                  // upper bound on the chunk count: T_tot/64 + N
     // ---- workspace ----
-    int *status;                // [0] cu_seqlens status, [1] chunk count NC, [2] wait timeout
+    int *status;                // [0] cu_seqlens status, [1] chunk count NC, [2] wait timeout,
+                                // [3] 16-bit range, [4] length of exact_list
     int *chunk_seq;             // [NCmax]  sequence of chunk c, -1 past NC
     int *chunk_len;             // [NCmax]  tokens in chunk c (1..64)
     int64_t *chunk_start;       // [NCmax]  first token of chunk c
@@ -55,6 +56,7 @@ struct Params {
     bf16 *hbuf;                 // [NCmax, HV, K, V] state entering each chunk (bf16)
     bf16 *vnew;                 // [T_tot, HV, V]  u_t (v_new) per token
     uint8_t *rec;               // [NCmax, HV] records of the tensor-core path
+    int *exact_list;            // [NCmax * HV] items (c * HV + hv) for the intra kernel's exact pass
     int vtile;                  // V columns per state CTA (tensor-core path)
     // chunk-parallel state pass (tensor-core path, K = V = 128): each sequence's
     // chunks in sc_P segments.  sc_mode 0: one sequential pass (sc_P = 1);
@@ -79,7 +81,8 @@ struct Params {
 
 // Workspace layout (byte offsets), a function of the problem only.
 struct WsLayout {
-    size_t status, chunk_seq, chunk_len, chunk_start, seq_first, seq_order, G, qn, kn, Wt, Ut, hbuf, vnew, rec, sc_tr, sc_si;
+    size_t status, chunk_seq, chunk_len, chunk_start, seq_first, seq_order, G, qn, kn, Wt, Ut, hbuf, vnew, rec,
+        exact_list, sc_tr, sc_si;
     size_t total;
 };
 
@@ -124,6 +127,13 @@ __device__ __forceinline__ void state_st(void *base, size_t i, float x, bool is_
         static_cast<bf16 *>(base)[i] = __float2bfloat16_rn(x);
     else
         static_cast<float *>(base)[i] = x;
+}
+
+// Status word 3 of the workspace: a kernel converted a value past the range of
+// its 16-bit intermediates (the conversion clipped it); gdn2_device_status
+// reports GDN2_ERR_RANGE.
+__device__ __forceinline__ void report_range(int *status, bool clipped) {
+    if (clipped) atomicExch(status + 3, static_cast<int>(GDN2_ERR_RANGE));
 }
 
 __device__ __forceinline__ int64_t cu_at(const Params &p, int i) {

@@ -20,7 +20,8 @@ std::mutex g_mu;
 void *g_scratch[kMaxDevices] = {};
 
 // Device address of the scratch on `dev` (the current device), looked up once
-// per device; nullptr if the lookup fails.
+// per device; nullptr if the lookup fails.  The address belongs to the context
+// current at the lookup (it does not survive cudaDeviceReset).
 void *scratch_address(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -36,6 +37,16 @@ void *scratch_address(int dev) {
     return g_scratch[dev];
 }
 
+// The scratch of the current device after the architecture check: the image
+// holds sm_103a code only, so on another device the lookup itself would fail
+// with a CUDA error instead of GDN2_ERR_ARCH.
+gdn2_status current_scratch(void **ws) {
+    int dev = 0;
+    if (!gdn2::device_is_sm103(&dev)) return GDN2_ERR_ARCH;
+    *ws = scratch_address(dev);
+    return *ws ? GDN2_OK : GDN2_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" gdn2_status gdn2_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *g,
@@ -45,13 +56,17 @@ extern "C" gdn2_status gdn2_chunk_fwd_noalloc(const void *q, const void *k, cons
     if (!dims) return GDN2_ERR_NULL;
     if (gdn2_workspace_bytes(dims) > static_cast<size_t>(GDN2_NOALLOC_SCRATCH_BYTES))
         return GDN2_ERR_NOALLOC_LIMIT;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return GDN2_ERR_ARCH;
-    }
-    void *ws = scratch_address(dev);
-    if (!ws) return GDN2_ERR_CUDA;
+    void *ws = nullptr;
+    const gdn2_status st = current_scratch(&ws);
+    if (st != GDN2_OK) return st;
     return gdn2_chunk_fwd(q, k, v, g, beta, w, scale, initial_state, cu_seqlens, out, final_state, dims, ws,
                           static_cast<size_t>(GDN2_NOALLOC_SCRATCH_BYTES), stream);
+}
+
+extern "C" gdn2_status gdn2_noalloc_device_status(void *stream, int32_t *status) {
+    if (!status) return GDN2_ERR_NULL;
+    void *ws = nullptr;
+    const gdn2_status st = current_scratch(&ws);
+    if (st != GDN2_OK) return st;
+    return gdn2_device_status(ws, stream, status);
 }

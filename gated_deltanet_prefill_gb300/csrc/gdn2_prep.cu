@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(kMapThreads) gdn2_chunk_map_kernel(Params p) {
     if (tid == 0) {
         s_bad = 0;
         p.status[2] = GDN2_OK;
+        p.status[3] = GDN2_OK;
+        p.status[4] = 0;
     }
     __syncthreads();
     for (int n = tid; n < p.N; n += kMapThreads)

@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(256) gdn2_recurrent_check_kernel(RecParams p) 
         bad = rec_cu(p, 0) != 0 || rec_cu(p, p.N) != p.T_tot;
         p.status[1] = 0;
         p.status[2] = 0;
+        p.status[3] = 0;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < p.N; i += blockDim.x)

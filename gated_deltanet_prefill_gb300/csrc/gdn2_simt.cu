@@ -15,8 +15,9 @@
 //   S_C  = diag(e^{G_L}) S0 + (k * e^{G_L - G})^T U         (L = last row)
 // Decay factors e^{G_t - G_s} are split through 16-token sub-chunk references
 // (burn-gdn2 README, "Numerical stability"): for column sub-chunk J with last
-// row E_J, e^{G_t-G_s} = e^{G_t-G_{E_J}} * e^{G_{E_J}-G_s}; the right factor is
-// <= 1, the left one is <= 1 below sub-chunk J and at most e^{15 max|g|} inside it.
+// row E_J and rows t below sub-chunk J, e^{G_t-G_s} = e^{G_t-G_{E_J}} *
+// e^{G_{E_J}-G_s}, both factors <= 1.  Pairs inside one sub-chunk take
+// e^{G_t-G_s} <= 1 directly, so no factor exceeds 1 for any g <= 0.
 #include "gdn2_internal.cuh"
 
 namespace gdn2 {
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(kIntraThreads) gdn2_simt_intra_kernel(Params p
         for (int i = tid; i < 64 * D; i += kIntraThreads) {
             const int r = i / D, ch = i % D;
             float x = 0.f;
-            if (r >= J * kSub && r < len)
+            if (r > e && r < len)
                 x = Bs[r * LD + ch] * Ks[r * LD + ch] * __expf(Gs[r * LD + ch] - Gs[e * LD + ch]);
             Ls[r * LD + ch] = x;
         }
@@ -87,8 +88,15 @@ __global__ void __launch_bounds__(kIntraThreads) gdn2_simt_intra_kernel(Params p
             const int t = i / kSub, s = J * kSub + i % kSub;
             if (s < t && t < len) {
                 float acc = 0.f;
+                if (t > e) {
 #pragma unroll 8
-                for (int ch = 0; ch < D; ++ch) acc += Ls[t * LD + ch] * Rs[s * LD + ch];
+                    for (int ch = 0; ch < D; ++ch) acc += Ls[t * LD + ch] * Rs[s * LD + ch];
+                } else {  // same sub-chunk: the decay of each pair directly
+#pragma unroll 8
+                    for (int ch = 0; ch < D; ++ch)
+                        acc += Bs[t * LD + ch] * Ks[t * LD + ch] * Ks[s * LD + ch] *
+                               __expf(Gs[t * LD + ch] - Gs[s * LD + ch]);
+                }
                 As[t * 65 + s] = acc;
             }
         }
@@ -235,6 +243,19 @@ __global__ void __launch_bounds__(kOutThreads) gdn2_simt_output_kernel(Params p)
     }
     for (int i = tid; i < 64 * 65; i += kOutThreads) Ps[i] = 0.f;
     __syncthreads();
+    // pairs inside one sub-chunk (s <= t): the decay of each pair directly,
+    // from the raw k rows
+    for (int i = tid; i < 64 * kSub; i += kOutThreads) {
+        const int t = i / kSub, s = (t / kSub) * kSub + i % kSub;
+        if (s <= t && t < len) {
+            float acc = 0.f;
+#pragma unroll 8
+            for (int ch = 0; ch < D; ++ch)
+                acc += Qs[t * LD + ch] * Rs[s * LD + ch] * __expf(Gs[t * LD + ch] - Gs[s * LD + ch]);
+            Ps[t * 65 + s] = acc;
+        }
+    }
+    __syncthreads();
     for (int i = tid; i < 64 * D; i += kOutThreads) {
         const int r = i / D, ch = i % D;
         const int e = sub_end(r, len);
@@ -246,13 +267,13 @@ __global__ void __launch_bounds__(kOutThreads) gdn2_simt_output_kernel(Params p)
         for (int i = tid; i < 64 * D; i += kOutThreads) {
             const int r = i / D, ch = i % D;
             float x = 0.f;
-            if (r >= J * kSub && r < len) x = Qs[r * LD + ch] * __expf(Gs[r * LD + ch] - Gs[e * LD + ch]);
+            if (r > e && r < len) x = Qs[r * LD + ch] * __expf(Gs[r * LD + ch] - Gs[e * LD + ch]);
             Ls[r * LD + ch] = x;
         }
         __syncthreads();
         for (int i = tid; i < 64 * kSub; i += kOutThreads) {
             const int t = i / kSub, s = J * kSub + i % kSub;
-            if (s <= t && t < len) {
+            if (t > e && t < len) {  // rows below sub-chunk J
                 float acc = 0.f;
 #pragma unroll 8
                 for (int ch = 0; ch < D; ++ch) acc += Ls[t * LD + ch] * Rs[s * LD + ch];

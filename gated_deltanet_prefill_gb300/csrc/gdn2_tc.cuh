@@ -294,8 +294,8 @@ __host__ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
 }
 
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero): used on
-// log2(e)-prescaled decay exponents, which are <= 0 except for the documented
-// sub-chunk factor.
+// log2(e)-prescaled decay exponents, which are <= 0 except for the diagonal
+// sub-chunk factors, which the intra kernel keeps below 2^92.
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -308,6 +308,24 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     uint32_t r;  // a -> low half; out-of-range finite values saturate to +-65504
     asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
     return r;
+}
+// The same conversion, tracking in m the largest fp16 magnitude written (two
+// 16-bit lanes, sign bits cleared; unsigned order of those bit patterns is the
+// order of the magnitudes).  A lane at 0x7bff (65504, where the conversion
+// saturates) or above (inf, NaN) means a value was clipped: the kernel then
+// reports GDN2_ERR_RANGE in the device status instead of returning it silently.
+__device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t pack_h2m(float a, float b, uint32_t &m) {
+    const uint32_t r = pack_h2(a, b);
+    m = umax16x2(m, r & 0x7fff7fffu);
+    return r;
+}
+__device__ __forceinline__ bool half_clipped(uint32_t m) {
+    return (m & 0xffffu) >= 0x7bffu || (m >> 16) >= 0x7bffu;
 }
 // a -> low half, IEEE round-to-nearest (overflow gives inf, as a cast would)
 __device__ __forceinline__ uint32_t pack_f16_rn(float a, float b) {
@@ -326,6 +344,10 @@ __device__ __forceinline__ float2 unpack_bf2(uint32_t x) {
 }
 __device__ __forceinline__ uint4 pack8_h(const float (&f)[8]) {
     return make_uint4(pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
+}
+__device__ __forceinline__ uint4 pack8_hm(const float (&f)[8], uint32_t &m) {
+    return make_uint4(pack_h2m(f[0], f[1], m), pack_h2m(f[2], f[3], m), pack_h2m(f[4], f[5], m),
+                      pack_h2m(f[6], f[7], m));
 }
 __device__ __forceinline__ uint4 pack8_bf(const float (&f)[8]) {
     return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));

@@ -19,6 +19,11 @@
 //        eR_s = e^{G_{E_J} - G_s} <= 1, m_{I,J} = e^{G_{B_I} - G_{E_J}}
 //     (m <= 1 for J < I; m = e^{+decay of sub-chunk I} for J = I).  Every m is
 //     a product of the per-sub-chunk decays ge_J = e^{G_{E_J} - G_{E_{J-1}}}.
+//     m for J = I stays below 2^92 (63.8 nats of decay in the sub-chunk); a
+//     key channel that decays faster gets m = 0 there, and its terms of the
+//     diagonal 16 x 16 blocks come from the exact path (e^{G_t - G_s} <= 1 per
+//     pair), which a second launch of this kernel runs over the items the
+//     first one lists.  So no factor exceeds its range for any g <= 0.
 //  3. tcgen05 (bf16): [beta k F ; q F] (M=128) x [R_0; R_1; R_2; R_3]^T, one
 //     N = 160 product, where R_I = k eR m_{I,.} holds the 16(I+1) tokens of row
 //     blocks <= I; the rows of block I against R_I give A (strictly lower) and
@@ -28,6 +33,8 @@
 //     lower triangular matrix, [[Ta, 0], [Aba, Tb]]^{-1} -> -Tb Aba Ta).
 //  5. tcgen05 (fp16): [Wt | Ut] = T x [beta k e^G | w v]  (M=128, N=2D, K=64).
 //  6. write Qe, Kd^T, P, Wt, Ut (fp16) and eGL (fp32) as shared-memory images.
+// Every fp16 conversion tracks the largest magnitude it wrote; one that
+// clipped (past 65504) sets GDN2_ERR_RANGE in the device status.
 //
 // Thread (t, seg = tid % 4) owns token row t and the 8-channel chunks seg,
 // seg + 4, seg + 8, ...: the four segments of a row fall in different
@@ -46,6 +53,12 @@ using namespace tc;
 
 constexpr int kIntraThreads = 256;
 constexpr int kLD = 68;  // row stride (floats) of the fp32 solver matrices
+// Largest decay (log2 units, 92 = 63.8 nats) of one key channel inside one
+// 16-token sub-chunk for which the factorised diagonal block stays exact: its
+// factors F_t >= 2^-92 and m = 2^92 stay normal in bf16 / fp32.  A channel
+// that decays faster is taken out of the diagonal block's product and added
+// back by the exact path (e^{G_t - G_s} per pair, fp32).
+constexpr float kWideLog2 = 92.f;
 
 template <int D>
 struct IntraCfg {
@@ -74,12 +87,16 @@ struct IntraCfg {
     static constexpr uint32_t kBWU = (2 * D / 64) * 8192;
     // per-channel tables (log2-scaled G): gE[4][D] = G'_{E_J}, tGB[4][D] =
     // e^{G_{B_I}}, tI[4][D] = e^{G_{B_I} - G_{E_I}}, t2[2][D] = e^{G_{E_{I+1}} -
-    // G_{E_I}}; the scan totals use the same area before the tables exist
+    // G_{E_I}}, t3[D] = e^{G_{E_3} - G_{E_2}}; the scan totals use the same
+    // area before the tables exist
     static constexpr uint32_t oTab = oBWU + kBWU;
-    static constexpr uint32_t kTab = 14 * D * 4;
-    // mbarriers (MMA, g copies, v/w copies) and the TMEM slot
+    static constexpr uint32_t kTab = 15 * D * 4;
+    // mbarriers (MMA, g copies, v/w copies) and the TMEM slot; then the
+    // staged item's exact-diagonal flag and the rows' k scales (exact path)
     static constexpr uint32_t oBar = oTab + kTab;
-    static constexpr uint32_t kSmem = oBar + 32 + 1024;         // + alignment slack
+    static constexpr uint32_t oFlag = oBar + 32;
+    static constexpr uint32_t oKs = oBar + 64;                  // [64] fp32
+    static constexpr uint32_t kSmem = oKs + 256 + 1024;         // + alignment slack
     static constexpr uint32_t kTmemCols = 256;
     static_assert(oTimg >= oY + 4096, "solver buffers overlap the T image");
     static_assert(oG + 64 * D * 4 <= oTimg, "G scratch must not overlap the T image");
@@ -91,9 +108,153 @@ struct IntraCfg {
 
 __device__ __forceinline__ uint4 ldg16(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
 
-// F16: q, k, v, beta, w are fp16 (else bf16); a template parameter so that the
-// operand-image loop carries no dtype branch
+// Exact diagonal blocks for the wide-decay channels of one item (thread
+// (t, seg); called by the whole CTA at the start of the item).  For the rows
+// s of t's sub-chunk I (s <= t), the sums over the channels that decay by more
+// than kWideLog2 inside sub-chunk I of beta_t k_t k_s e^{G_t - G_s} (A, s < t)
+// and q_t k_s e^{G_t - G_s} (P), with e^{G_t - G_s} <= 1 taken per pair in
+// fp32.  They go to the record's Ut area as fp32 [64 t][16] (A, then P);
+// exact_diag_apply adds them to the product's diagonal blocks, and Ut itself
+// is written later.  Gs: the item's G' rows; gE: G' at the sub-chunks' last
+// rows; ks: scratch for each row's k scale.  Separate functions, off the
+// per-item path, so that path keeps its own register allocation.
 template <int D, bool F16>
+__device__ __noinline__ void exact_diag_sums(const Params &p, const float *Gs, const float *gE, float *ks,
+                                             uint8_t *rec, const bf16 *kp, const bf16 *qp, const bf16 *bp,
+                                             int64_t start, int h, int t, int seg, bool live) {
+    constexpr int NJ = D / 32;
+    const int I = t / 16;
+    float kscale = 1.f, qscale = 1.f;
+    if (p.l2norm) {  // the row's scales, as the operand images take them
+        float sk = 0.f, sq = 0.f;
+        if (live) {
+#pragma unroll 1
+            for (int j = 0; j < NJ; ++j) {
+                float a[8], b[8];
+                unpack8_in(ldg16(kp + 8 * (seg + 4 * j)), a, F16);
+                unpack8_in(ldg16(qp + 8 * (seg + 4 * j)), b, F16);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    sk += a[x] * a[x];
+                    sq += b[x] * b[x];
+                }
+            }
+        }
+        sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+        sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+        kscale = 1.f / fmaxf(sqrtf(sk), 1e-12f);
+        qscale = 1.f / fmaxf(sqrtf(sq), 1e-12f);
+    }
+    if (seg == 0) ks[t] = kscale;
+    __syncthreads();
+    float cA[16], cP[16];
+#pragma unroll
+    for (int si = 0; si < 16; ++si) cA[si] = cP[si] = 0.f;
+    if (live) {
+#pragma unroll 1
+        for (int j = 0; j < NJ; ++j) {
+            const int cb = 8 * (seg + 4 * j);
+            uint32_t wm = 0;  // wide channels of this 8-channel chunk
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const float b = I > 0 ? gE[(I - 1) * D + cb + x] : 0.f;
+                if (b - gE[I * D + cb + x] > kWideLog2) wm |= 1u << x;
+            }
+            if (!wm) continue;
+            float kt[8], qt[8], bt[8], gt[8];
+            unpack8_in(ldg16(kp + cb), kt, F16);
+            unpack8_in(ldg16(qp + cb), qt, F16);
+            if (p.has_beta) unpack8_in(ldg16(bp + cb), bt, F16);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                kt[x] *= kscale;
+                qt[x] *= qscale;
+                bt[x] = (p.has_beta ? bt[x] : 1.f) * kt[x];
+                gt[x] = Gs[t * D + cb + x];
+            }
+#pragma unroll 1
+            for (int si = 0; si < 16; ++si) {
+                const int s = 16 * I + si;
+                if (s > t) break;
+                float kv[8];
+                unpack8_in(ldg16(p.k + (start + s) * p.sk_t + static_cast<int64_t>(h) * p.sk_h + cb), kv, F16);
+                const float sc = ks[s];
+                float a = 0.f, q = 0.f;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    if (!((wm >> x) & 1u)) continue;
+                    const float kw = kv[x] * sc * ex2(gt[x] - Gs[s * D + cb + x]);
+                    a += bt[x] * kw;
+                    q += qt[x] * kw;
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {  // register arrays take constant indices
+                    if (u == si) {
+                        cA[u] += s < t ? a : 0.f;
+                        cP[u] += q;
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {  // the four segments of the row hold partial sums
+        cA[u] += __shfl_xor_sync(0xffffffffu, cA[u], 1);
+        cA[u] += __shfl_xor_sync(0xffffffffu, cA[u], 2);
+        cP[u] += __shfl_xor_sync(0xffffffffu, cP[u], 1);
+        cP[u] += __shfl_xor_sync(0xffffffffu, cP[u], 2);
+    }
+    float4 a4 = make_float4(cA[0], cA[1], cA[2], cA[3]), p4 = make_float4(cP[0], cP[1], cP[2], cP[3]);
+    if (seg == 1) {
+        a4 = make_float4(cA[4], cA[5], cA[6], cA[7]);
+        p4 = make_float4(cP[4], cP[5], cP[6], cP[7]);
+    } else if (seg == 2) {
+        a4 = make_float4(cA[8], cA[9], cA[10], cA[11]);
+        p4 = make_float4(cP[8], cP[9], cP[10], cP[11]);
+    } else if (seg == 3) {
+        a4 = make_float4(cA[12], cA[13], cA[14], cA[15]);
+        p4 = make_float4(cP[12], cP[13], cP[14], cP[15]);
+    }
+    float *corr = reinterpret_cast<float *>(rec + Rec<D>::Ut);
+    *reinterpret_cast<float4 *>(corr + t * 16 + 4 * seg) = a4;
+    *reinterpret_cast<float4 *>(corr + 64 * 16 + t * 16 + 4 * seg) = p4;
+}
+
+// Adds the exact path's sums (exact_diag_sums) to the four diagonal 16 x 16
+// blocks of A (fp32, shared memory, row stride kLD; s < t) and of P (the
+// record's fp16 image; s <= t), once the A/P epilogue has written both.
+// Thread (block, row, 4-column group); called by the whole CTA.
+template <int D>
+__device__ __noinline__ void exact_diag_apply(float *Af, uint8_t *rec, int tid) {
+    const int I = tid / 64, r = (tid / 4) % 16, q4 = tid % 4;
+    const int tt = 16 * I + r, s0 = 16 * I + 4 * q4;
+    const float *corr = reinterpret_cast<const float *>(rec + Rec<D>::Ut) + tt * 16 + 4 * q4;
+    const float4 ca = *reinterpret_cast<const float4 *>(corr);
+    const float4 cp = *reinterpret_cast<const float4 *>(corr + 64 * 16);
+    const float a4[4] = {ca.x, ca.y, ca.z, ca.w}, p4[4] = {cp.x, cp.y, cp.z, cp.w};
+    float *arow = Af + tt * kLD + s0;
+    uint2 *prow = reinterpret_cast<uint2 *>(rec + Rec<D>::P + swz(tt, s0 / 8) + (s0 % 8) * 2);
+    const uint2 ph = *prow;
+    float2 pa = unpack_h2(ph.x), pb = unpack_h2(ph.y);
+    float pv[4] = {pa.x, pa.y, pb.x, pb.y};
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        if (s0 + x < tt) arow[x] += a4[x];
+        if (s0 + x <= tt) pv[x] += p4[x];
+    }
+    *prow = make_uint2(pack_h2(pv[0], pv[1]), pack_h2(pv[2], pv[3]));
+}
+
+// F16: q, k, v, beta, w are fp16 (else bf16); a template parameter so that the
+// operand-image loop carries no dtype branch.  EXACT = false: the pass over
+// every (chunk, value head) item; an item with a wide-decay channel gets its
+// record without that channel's diagonal terms and is appended to the exact
+// list.  EXACT = true: the second launch, over the listed items only, with the
+// exact path; it rewrites their records.  Two instantiations keep the exact
+// path's code out of the first pass.
+template <int D, bool F16, bool EXACT>
 __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const __grid_constant__ Params p) {
     using C = IntraCfg<D>;
     constexpr int NJ = D / 32;         // 8-channel chunks per thread
@@ -111,7 +272,14 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     const int seg = tid % 4;
     const int t = 8 * warp + (((lane >> 2) & 1) << 2) + (lane >> 3);
     const int I = t / 16;
-    const int total = p.status[0] == GDN2_OK ? p.status[1] * p.HV : 0;  // (chunk, value head) items
+    // The exact pass is launched as a programmatic dependent of the first one
+    // (it may start while the first pass drains); it waits here until the
+    // first pass has completed and its exact list is visible.
+    if (EXACT) asm volatile("griddepcontrol.wait;" ::: "memory");
+    else asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // (chunk, value head) items: all of them, or the exact list
+    const int total = p.status[0] != GDN2_OK ? 0 : EXACT ? p.status[4] : p.status[1] * p.HV;
+    if (static_cast<int>(blockIdx.x) >= total) return;  // before any barrier or TMEM allocation
 
     if (tid == 0) {
         mbar_init(&bar_mma, 1);
@@ -130,16 +298,18 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     // (warp 7), its v and w rows into the B operand area once the W/U product
     // has read it (warp 2); both land during the W/U product and epilogue.
     // k, q and beta are read by every thread during the operand images.
-    int c = 0, hv = 0, len = 1, h = 0;
+    int c = 0, hv = 0, len = 1, h = 0, item = 0;
     int nc = 0, nhv = 0, nlen = 1;
-    int64_t nstart = 0;
+    int64_t nstart = 0, start = 0;
     bool live = false;
     const bf16 *kp = nullptr, *qp = nullptr, *bp = nullptr;
     const uint4 z4 = make_uint4(0, 0, 0, 0);
     uint4 nk = z4, nq = z4, nb = z4;
+    int nitem = 0;  // item index c * HV + hv of the staged item
     auto meta = [&](int it) {
-        nc = it / p.HV;
-        nhv = it - nc * p.HV;
+        nitem = EXACT ? p.exact_list[it] : it;
+        nc = nitem / p.HV;
+        nhv = nitem - nc * p.HV;
         nstart = p.chunk_start[nc];
         nlen = p.chunk_len[nc];
     };
@@ -194,7 +364,9 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     auto adopt = [&]() {  // the staged item becomes the current one
         c = nc;
         hv = nhv;
+        item = nitem;
         len = nlen;
+        start = nstart;
         h = hv / p.group;
         live = t < len;
         const int64_t tok = nstart + (live ? t : 0);
@@ -213,7 +385,11 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     float *tGB = gE + 4 * D;                              // e^{G_{B_I}}
     float *tI = tGB + 4 * D;                              // e^{G_{B_I} - G_{E_I}}
     float *t2 = tI + 4 * D;                               // e^{G_{E_{I+1}} - G_{E_I}}, I = 0, 1
+    float *t3 = t2 + 2 * D;                               // e^{G_{E_3} - G_{E_2}}
+    volatile uint32_t *exact_flag = reinterpret_cast<volatile uint32_t *>(sm + C::oFlag);
+    float *ks_row = reinterpret_cast<float *>(sm + C::oKs);  // k scale of each row (exact path)
     uint32_t gph = 0, vph = 0;  // parities of the g and v/w staging barriers
+    uint32_t hmax = 0;           // largest magnitude converted to fp16 (range check)
     const bool aux = (warp & 2) != 0;
     auto scan_tables = [&](int ilen, uint8_t *irec) {
         const int lt = 32 * ((warp & 1) + 2 * (warp >> 2)) + lane;  // 0 .. 127
@@ -273,20 +449,28 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
                 }
             }
         }
+        if (lt == 0) *exact_flag = 0u;
         named_sync(1, 128);
         if (lt < D) {
             float e[4];
 #pragma unroll
             for (int J = 0; J < 4; ++J) e[J] = Gs[min(16 * J + 15, ilen - 1) * D + lt];
+            bool wide = false;
 #pragma unroll
             for (int J = 0; J < 4; ++J) {
                 const float b = J > 0 ? e[J - 1] : 0.f;
                 gE[J * D + lt] = e[J];
                 tGB[J * D + lt] = ex2(b);
-                tI[J * D + lt] = ex2(b - e[J]);
+                // a channel that decays by more than kWideLog2 inside sub-chunk
+                // J takes its diagonal block from the exact path (m = 0 here)
+                const bool wj = b - e[J] > kWideLog2;
+                tI[J * D + lt] = wj ? 0.f : ex2(b - e[J]);
+                wide |= wj;
             }
+            if (wide) *exact_flag = 1u;
             t2[lt] = ex2(e[1] - e[0]);
             t2[D + lt] = ex2(e[2] - e[1]);
+            t3[lt] = ex2(e[3] - e[2]);
             reinterpret_cast<float *>(irec + Rec<D>::eGL)[lt] = ex2(e[3]);
         }
     };
@@ -309,6 +493,12 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     for (int it = blockIdx.x; it < total; it += gridDim.x) {
     adopt();
     uint8_t *rec = rec_of(c, hv);
+    // some key channel decays past the factorised range inside a sub-chunk of
+    // this item: its diagonal blocks take the exact path (CTA-uniform)
+    const bool exact = *exact_flag != 0u;
+    const uint32_t hmax_in = hmax;
+    if (!EXACT && exact && tid == 0) p.exact_list[atomicAdd(p.status + 4, 1)] = item;
+    if (EXACT && exact) exact_diag_sums<D, F16>(p, Gs, gE, ks_row, rec, kp, qp, bp, start, h, t, seg, live);
 
     // ---- 1. cumsum (g is in the G scratch) ----------------------------------------
     nk = nq = nb = z4;
@@ -342,7 +532,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         qscale = 1.f / fmaxf(sqrtf(sq), 1e-12f);
     }
     // G' prefix sums and tables are ready (computed during the previous item's
-    // W/U epilogue, or before the loop); raw v and w are in the B operand area
+    // W/U epilogue, or before the loop).
+    // raw v and w are in the B operand area
     if (!mbar_wait(&bar_vw, vph)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
     vph ^= 1u;
     // w v for this thread's chunks, stored to its operand image after the
@@ -373,7 +564,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
             unpack8_in(h ? w1 : w0, ww, F16);
 #pragma unroll
             for (int x = 0; x < 8; ++x) ww[x] = (p.has_w || !live) ? ww[x] * vv[x] : vv[x];
-            wX2[j + h] = pack8_h(ww);
+            wX2[j + h] = pack8_hm(ww, hmax);
         }
     }
     float Gr[8 * NJ];
@@ -426,13 +617,13 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
             const int c4 = cb + 4 * hh;
             const float4 vB4 = I > 0 ? *reinterpret_cast<const float4 *>(gE + (I - 1) * D + c4) : z4f;
             const float4 vE4 = *reinterpret_cast<const float4 *>(gE + I * D + c4);
-            const float4 vL4 = *reinterpret_cast<const float4 *>(gE + 3 * D + c4);
+            const float4 v44 = *reinterpret_cast<const float4 *>(t3 + c4);
             const float4 vG4 = *reinterpret_cast<const float4 *>(tGB + I * D + c4);
             const float4 vI4 = *reinterpret_cast<const float4 *>(tI + I * D + c4);
             const float4 v24 = *reinterpret_cast<const float4 *>(t2 + (I & 1) * D + c4);
             const float4 v34 = *reinterpret_cast<const float4 *>(t2 + D + c4);
             const float vB[4] = {vB4.x, vB4.y, vB4.z, vB4.w}, vE[4] = {vE4.x, vE4.y, vE4.z, vE4.w};
-            const float vL[4] = {vL4.x, vL4.y, vL4.z, vL4.w}, vG[4] = {vG4.x, vG4.y, vG4.z, vG4.w};
+            const float v4[4] = {v44.x, v44.y, v44.z, v44.w}, vG[4] = {vG4.x, vG4.y, vG4.z, vG4.w};
             const float vI[4] = {vI4.x, vI4.y, vI4.z, vI4.w}, v2[4] = {v24.x, v24.y, v24.z, v24.w};
             const float v3[4] = {v34.x, v34.y, v34.z, v34.w};
             float lk[4], lq[4], kr[4], x1[4], qe[4], kd[4], r0[4], r2[4], r3[4];
@@ -442,7 +633,12 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
                 const float gt = Gr[8 * j + x];
                 const float F = ex2(gt - vB[ce]);                // e^{G_t - G_{B_I}}
                 const float eR = ex2(vE[ce] - gt);               // e^{G_{E_I} - G_t}
-                const float eL = ex2(vL[ce] - gt);               // e^{G_L - G_t}
+                // e^{G_L - G_t} = eR e^{G_L - G_{E_I}}, the second factor a
+                // product of the sub-chunk decays after sub-chunk I (L = E_3)
+                float fL = I == 3 ? 1.f : v4[ce];
+                if (I <= 1) fL *= v2[ce];
+                if (I == 0) fL *= v3[ce];
+                const float eL = eR * fL;
                 const float kx = kk[x] * kscale;
                 lk[ce] = bb[x] * kx * F;
                 lq[ce] = qq[x] * qscale * F;
@@ -463,9 +659,9 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
                 wr0[x2] = pack_bf2(r0[a], r0[a + 1]);
                 wr2[x2] = pack_bf2(r2[a], r2[a + 1]);
                 wr3[x2] = pack_bf2(r3[a], r3[a + 1]);
-                wX1[x2] = pack_h2(x1[a], x1[a + 1]);
-                wQe[x2] = pack_h2(qe[a], qe[a + 1]);
-                wKd[x2] = pack_h2(kd[a], kd[a + 1]);
+                wX1[x2] = pack_h2m(x1[a], x1[a + 1], hmax);
+                wQe[x2] = pack_h2m(qe[a], qe[a + 1], hmax);
+                wKd[x2] = pack_h2m(kd[a], kd[a + 1], hmax);
             }
         }
         auto u4 = [](const uint32_t (&w)[4]) { return make_uint4(w[0], w[1], w[2], w[3]); };
@@ -538,7 +734,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
                             const int s = s0 + 8 * half + x;
                             f[x] = s <= tt ? __uint_as_float(v[8 * half + x]) : 0.f;
                         }
-                        *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, s0 / 8 + half)) = pack8_h(f);
+                        *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, s0 / 8 + half)) = pack8_hm(f, hmax);
                     }
                 }
             }
@@ -554,6 +750,11 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
             for (int chunk = 2 * (Ir + 1); chunk < 8; ++chunk)
                 *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, chunk)) = make_uint4(0, 0, 0, 0);
         }
+    }
+    if (EXACT && exact) {  // the exact path's sums join the diagonal blocks of A and P
+        __syncthreads();
+        exact_diag_apply<D>(Af, rec, tid);
+        __syncthreads();
     }
     const bool has_next = it + static_cast<int>(gridDim.x) < total;
     if (has_next) meta(it + static_cast<int>(gridDim.x));
@@ -664,16 +865,20 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         *reinterpret_cast<float2 *>(Tf + (33 + i0) * kLD + j0) = make_float2(z10, z11);
     }
     __syncthreads();
-    // T -> fp16 K-major image [64 t][64 s]; zeros above the diagonal
+    // T -> fp16 K-major image [64 t][64 s]; zeros above the diagonal.  An
+    // eight-lane group takes chunks 0-3 of row 2m and 4-7 of row 2m + 1 (or
+    // the other halves): fp32 rows kLD = 68 floats apart start 4 banks apart,
+    // so its 16-byte loads cover all 32 banks, and so do its swizzled stores.
     for (int e = tid; e < 64 * 8; e += kIntraThreads) {
-        const int tt = e / 8, chunk = e % 8;
+        const int l = e % 16, hb = (l / 4) & 1;
+        const int tt = 2 * (e / 16) + hb, chunk = (l % 4) + 4 * (hb ^ (l / 8));
         const float4 lo = *reinterpret_cast<const float4 *>(Tf + tt * kLD + 8 * chunk);
         const float4 hi = *reinterpret_cast<const float4 *>(Tf + tt * kLD + 8 * chunk + 4);
         const float tv8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
         float f[8];
 #pragma unroll
         for (int x = 0; x < 8; ++x) f[x] = 8 * chunk + x <= tt ? tv8[x] : 0.f;
-        *reinterpret_cast<uint4 *>(sm + C::oTimg + swz(tt, chunk)) = pack8_h(f);
+        *reinterpret_cast<uint4 *>(sm + C::oTimg + swz(tt, chunk)) = pack8_hm(f, hmax);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -711,20 +916,24 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const uint32_t *w = v + 8 * cc;
-                const uint4 o = make_uint4(pack_h2(__uint_as_float(w[0]), __uint_as_float(w[1])),
-                                           pack_h2(__uint_as_float(w[2]), __uint_as_float(w[3])),
-                                           pack_h2(__uint_as_float(w[4]), __uint_as_float(w[5])),
-                                           pack_h2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+                const uint4 o = make_uint4(pack_h2m(__uint_as_float(w[0]), __uint_as_float(w[1]), hmax),
+                                           pack_h2m(__uint_as_float(w[2]), __uint_as_float(w[3]), hmax),
+                                           pack_h2m(__uint_as_float(w[4]), __uint_as_float(w[5]), hmax),
+                                           pack_h2m(__uint_as_float(w[6]), __uint_as_float(w[7]), hmax));
                 uint8_t *dst = is_u ? rec + Rec<D>::Ut + kb * 8192 + swz(tt, c0 + cc)
                                     : rec + Rec<D>::A1 + kb * 16384 + swz(64 + tt, c0 + cc);
                 *reinterpret_cast<uint4 *>(dst) = o;
             }
         }
     }
+    // the first pass's record of a listed item is rewritten by the exact pass:
+    // its values do not count for the range check
+    if (!EXACT && exact) hmax = hmax_in;
     tc_fence_before();
     __syncthreads();  // the item's shared memory and TMEM are free for the next one
     tc_fence_after();
     }  // items
+    report_range(p.status, half_clipped(hmax));
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -734,20 +943,47 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     }
 }
 
-template <int D, bool F16>
-cudaError_t launch_intra(const Params &p, cudaStream_t s) {
+template <int D, bool F16, bool EXACT>
+cudaError_t launch_intra_pass(const Params &p, cudaStream_t s) {
     using C = IntraCfg<D>;
-    auto kern = gdn2_tc_intra_kernel<D, F16>;
+    auto kern = gdn2_tc_intra_kernel<D, F16, EXACT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return cudaGetLastError();
-    const long long items = static_cast<long long>(p.NCmax) * p.HV;  // upper bound; the kernel reads NC
+    const long long items = static_cast<long long>(p.NCmax) * p.HV;  // upper bound; the kernel reads the count
     const int grid = static_cast<int>(items < 2ll * sms ? items : 2ll * sms);
-    if (grid > 0) kern<<<grid, kIntraThreads, C::kSmem, s>>>(p);
+    if (grid <= 0) return cudaGetLastError();
+    if (!EXACT) {
+        kern<<<grid, kIntraThreads, C::kSmem, s>>>(p);
+        return cudaGetLastError();
+    }
+    // the exact pass: a programmatic dependent launch, so that its launch
+    // overlaps the first pass's tail (it waits for the first pass in-kernel)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kIntraThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// Both passes: every item, then the exact pass over the items the first one
+// listed (its CTAs return at once when the list is empty).
+template <int D, bool F16>
+cudaError_t launch_intra(const Params &p, cudaStream_t s) {
+    const cudaError_t e = launch_intra_pass<D, F16, false>(p, s);
+    if (e != cudaSuccess) return e;
+    return launch_intra_pass<D, F16, true>(p, s);
 }
 
 }  // namespace

@@ -201,6 +201,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
         }
     } else if (warp >= 8) {
         // ------------------------------------- state epilogue (S rows = key channels)
+        uint32_t hmax = 0;  // largest magnitude converted to fp16 (range check)
         const int q = warp & 3;
         const int row = 32 * q + lane;
         const int grp = (warp - 8) >> 2;  // 32-column group of this warp
@@ -269,10 +270,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         uint4 v;
-                        v.x = pack_h2(__uint_as_float(r[8 * cc + 0]), __uint_as_float(r[8 * cc + 1]));
-                        v.y = pack_h2(__uint_as_float(r[8 * cc + 2]), __uint_as_float(r[8 * cc + 3]));
-                        v.z = pack_h2(__uint_as_float(r[8 * cc + 4]), __uint_as_float(r[8 * cc + 5]));
-                        v.w = pack_h2(__uint_as_float(r[8 * cc + 6]), __uint_as_float(r[8 * cc + 7]));
+                        v.x = pack_h2m(__uint_as_float(r[8 * cc + 0]), __uint_as_float(r[8 * cc + 1]), hmax);
+                        v.y = pack_h2m(__uint_as_float(r[8 * cc + 2]), __uint_as_float(r[8 * cc + 3]), hmax);
+                        v.z = pack_h2m(__uint_as_float(r[8 * cc + 4]), __uint_as_float(r[8 * cc + 5]), hmax);
+                        v.w = pack_h2m(__uint_as_float(r[8 * cc + 6]), __uint_as_float(r[8 * cc + 7]), hmax);
                         *reinterpret_cast<uint4 *>(dst + swz(row, c0 + cc)) = v;
                     }
 #pragma unroll
@@ -323,6 +324,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                 }
             }
         }
+        report_range(p.status, half_clipped(hmax));
     } else if (warp == 4 || warp == 5) {
         // ----------------------------------------- output epilogue (tokens 0-63)
         const int q = warp & 3;  // 0 or 1
@@ -368,6 +370,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
         }
     } else if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
         // ----------------------------------- U epilogue (D1 rows 64-127 = Wt S)
+        uint32_t hmax = 0;  // largest magnitude converted to fp16 (range check)
         const int q = warp & 3;  // 2 or 3
         const int t = 32 * (q - 2) + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -395,8 +398,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 a = unpack_h2(uw[e]);
-                        ow[e] = pack_h2(a.x - __uint_as_float(r[8 * cc + 2 * e]),
-                                        a.y - __uint_as_float(r[8 * cc + 2 * e + 1]));
+                        ow[e] = pack_h2m(a.x - __uint_as_float(r[8 * cc + 2 * e]),
+                                        a.y - __uint_as_float(r[8 * cc + 2 * e + 1]), hmax);
                     }
                     *reinterpret_cast<uint4 *>(sm + C::oU + blk * 8192 + swz(t, c0 + cc)) =
                         make_uint4(ow[0], ow[1], ow[2], ow[3]);
@@ -406,6 +409,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             tc_fence_before();
             mbar_arrive(&u_ready);
         }
+        report_range(p.status, half_clipped(hmax));
     }
     tc_fence_before();
     __syncthreads();

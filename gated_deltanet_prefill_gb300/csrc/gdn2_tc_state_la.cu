@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
         }
     } else if (warp >= 8 && warp < 16) {
         // ------------------------- state epilogue: E_c = eGL_c S_c (rows = key channels)
+        uint32_t hmax = 0;  // largest magnitude converted to fp16 (range check)
         const int q = warp & 3, g = (warp - 8) >> 2;  // lane quarter, 32-column group
         const int row = 32 * q + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -244,10 +245,10 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint4 v;
-                v.x = pack_h2(__uint_as_float(r[8 * cc + 0]), __uint_as_float(r[8 * cc + 1]));
-                v.y = pack_h2(__uint_as_float(r[8 * cc + 2]), __uint_as_float(r[8 * cc + 3]));
-                v.z = pack_h2(__uint_as_float(r[8 * cc + 4]), __uint_as_float(r[8 * cc + 5]));
-                v.w = pack_h2(__uint_as_float(r[8 * cc + 6]), __uint_as_float(r[8 * cc + 7]));
+                v.x = pack_h2m(__uint_as_float(r[8 * cc + 0]), __uint_as_float(r[8 * cc + 1]), hmax);
+                v.y = pack_h2m(__uint_as_float(r[8 * cc + 2]), __uint_as_float(r[8 * cc + 3]), hmax);
+                v.z = pack_h2m(__uint_as_float(r[8 * cc + 4]), __uint_as_float(r[8 * cc + 5]), hmax);
+                v.w = pack_h2m(__uint_as_float(r[8 * cc + 6]), __uint_as_float(r[8 * cc + 7]), hmax);
                 *reinterpret_cast<uint4 *>(img + swz(row, 4 * g + cc)) = v;
             }
         };
@@ -319,8 +320,10 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
                              p.state_bf16);
             }
         }
+        report_range(p.status, half_clipped(hmax));
     } else if (warp >= 16) {
         // ------------------- XY epilogue: fp32 accumulator -> fp16 A operand in TMEM
+        uint32_t hmax = 0;  // largest magnitude converted to fp16 (range check)
         const int q = warp & 3, g = (warp - 16) >> 2;  // lane quarter, 32 of the 64 token columns
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         for (int k = 0; k + 1 < nck; ++k) {  // XY of chunk k + 1
@@ -333,12 +336,13 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
             tmem_ld32(tXY + lane_base + 32 * g, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) h[i] = pack_h2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            for (int i = 0; i < 16; ++i) h[i] = pack_h2m(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), hmax);
             tmem_st16(tXa + lane_base + 16 * g, h);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&xy_ready);
         }
+        report_range(p.status, half_clipped(hmax));
     } else if (warp == 4 || warp == 5) {
         // ----------------------------------------- output epilogue (tokens 0-63)
         const int q = warp & 3;  // 0 or 1
@@ -377,6 +381,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
         }
     } else {
         // ----------------------------------- U epilogue (D rows 64-127 = Wt S)
+        uint32_t hmax = 0;  // largest magnitude converted to fp16 (range check)
         const int q = warp & 3;  // 2 or 3
         const int t = 32 * (q - 2) + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -400,7 +405,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 a = unpack_h2(uw[e]);
-                    ow[e] = pack_h2(a.x - __uint_as_float(r[8 * cc + 2 * e]), a.y - __uint_as_float(r[8 * cc + 2 * e + 1]));
+                    ow[e] = pack_h2m(a.x - __uint_as_float(r[8 * cc + 2 * e]), a.y - __uint_as_float(r[8 * cc + 2 * e + 1]), hmax);
                 }
                 *reinterpret_cast<uint4 *>(dst + swz(t, 4 * g + cc)) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
             }
@@ -408,6 +413,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
             tc_fence_before();
             mbar_arrive(&u_ready);
         }
+        report_range(p.status, half_clipped(hmax));
     }
     tc_fence_before();
     __syncthreads();
@@ -643,6 +649,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
         }
     } else if (warp >= 8 && warp < 16) {
         // ------------------------- state epilogue: E_c = eGL_c S_c (rows = key channels)
+        uint32_t hmax = 0;  // largest magnitude converted to fp16 (range check)
         const int q = warp & 3, g2 = (warp - 8) >> 2;  // lane quarter, 64-column half
         const int row = 32 * q + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -654,10 +661,10 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint4 v;
-                v.x = pack_h2(__uint_as_float(r[8 * cc + 0]), __uint_as_float(r[8 * cc + 1]));
-                v.y = pack_h2(__uint_as_float(r[8 * cc + 2]), __uint_as_float(r[8 * cc + 3]));
-                v.z = pack_h2(__uint_as_float(r[8 * cc + 4]), __uint_as_float(r[8 * cc + 5]));
-                v.w = pack_h2(__uint_as_float(r[8 * cc + 6]), __uint_as_float(r[8 * cc + 7]));
+                v.x = pack_h2m(__uint_as_float(r[8 * cc + 0]), __uint_as_float(r[8 * cc + 1]), hmax);
+                v.y = pack_h2m(__uint_as_float(r[8 * cc + 2]), __uint_as_float(r[8 * cc + 3]), hmax);
+                v.z = pack_h2m(__uint_as_float(r[8 * cc + 4]), __uint_as_float(r[8 * cc + 5]), hmax);
+                v.w = pack_h2m(__uint_as_float(r[8 * cc + 6]), __uint_as_float(r[8 * cc + 7]), hmax);
                 *reinterpret_cast<uint4 *>(blk + swz(row, 4 * (gcol & 1) + cc)) = v;
             }
         };
@@ -748,8 +755,10 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
                 }
             }
         }
+        report_range(p.status, half_clipped(hmax));
     } else if (warp >= 16) {
         // ------------------- XY epilogue: fp32 accumulator -> fp16 A operand in TMEM
+        uint32_t hmax = 0;  // largest magnitude converted to fp16 (range check)
         const int q = warp & 3, g = (warp - 16) >> 2;  // lane quarter, 32 of the 64 token columns
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         for (int k = 0; k + 1 < nck; ++k) {  // XY of chunk k + 1
@@ -762,12 +771,13 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
             tmem_ld32(tXY + lane_base + 32 * g, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) h[i] = pack_h2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            for (int i = 0; i < 16; ++i) h[i] = pack_h2m(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), hmax);
             tmem_st16(tXa + lane_base + 16 * g, h);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&xy_ready);
         }
+        report_range(p.status, half_clipped(hmax));
     } else if (warp == 4 || warp == 5) {
         // ----------------------------------------- output epilogue (tokens 0-63)
         const int q = warp & 3;  // 0 or 1
@@ -806,6 +816,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
         }
     } else {
         // ------------------- U epilogue (D rows 64-127 = Wt S): U = Ut - Wt S in place
+        uint32_t hmax = 0;  // largest magnitude converted to fp16 (range check)
         const int q = warp & 3;  // 2 or 3
         const int t = 32 * (q - 2) + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
@@ -831,8 +842,8 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 a = unpack_h2(uw[e]);
-                        ow[e] = pack_h2(a.x - __uint_as_float(r[8 * cc + 2 * e]),
-                                        a.y - __uint_as_float(r[8 * cc + 2 * e + 1]));
+                        ow[e] = pack_h2m(a.x - __uint_as_float(r[8 * cc + 2 * e]),
+                                        a.y - __uint_as_float(r[8 * cc + 2 * e + 1]), hmax);
                     }
                     *at = make_uint4(ow[0], ow[1], ow[2], ow[3]);
                 }
@@ -841,6 +852,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
             tc_fence_before();
             mbar_arrive(&u_ready);
         }
+        report_range(p.status, half_clipped(hmax));
     }
     tc_fence_before();
     __syncthreads();

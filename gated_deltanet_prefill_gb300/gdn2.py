@@ -20,7 +20,7 @@ GDN2_OK = 0
 STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_STRIDE", 4: "ERR_ALIAS",
                 5: "ERR_WORKSPACE", 6: "ERR_ARCH", 7: "ERR_LAUNCH", 8: "ERR_DTYPE",
                 9: "ERR_CU_SEQLENS", 10: "ERR_CUDA", 11: "ERR_IMPL", 12: "ERR_TIMEOUT",
-                13: "ERR_NOALLOC_LIMIT"}
+                13: "ERR_NOALLOC_LIMIT", 14: "ERR_RANGE"}
 NOALLOC_SCRATCH_BYTES = 64 << 20
 IMPL = {"tc": 0, "simt": 1}
 DTYPE_BF16, DTYPE_F16, DTYPE_F32 = 0, 1, 2
@@ -28,7 +28,8 @@ _DTYPE_CODE = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16, torch.float
 
 EXPORTS = ("gdn2_workspace_bytes", "gdn2_dims_init", "gdn2_check_args", "gdn2_chunk_fwd",
            "gdn2_chunk_fwd_staged", "gdn2_num_stages", "gdn2_stage_name", "gdn2_launch_count",
-           "gdn2_device_status", "gdn2_chunk_fwd_noalloc", "gdn2_recurrent_workspace_bytes",
+           "gdn2_device_status", "gdn2_chunk_fwd_noalloc", "gdn2_noalloc_device_status",
+           "gdn2_recurrent_workspace_bytes",
            "gdn2_recurrent_fwd", "gdn2_selftest_wait_timeout", "gdn2_status_string", "gdn2_version")
 
 
@@ -91,6 +92,8 @@ def load(path: Optional[str] = None):
     lib.gdn2_chunk_fwd_noalloc.argtypes = [vp] * 6 + [ctypes.c_float, vp, vp, vp, vp,
                                                       ctypes.POINTER(Dims), vp]
     lib.gdn2_chunk_fwd_noalloc.restype = ctypes.c_int
+    lib.gdn2_noalloc_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.gdn2_noalloc_device_status.restype = ctypes.c_int
     lib.gdn2_recurrent_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
     lib.gdn2_recurrent_workspace_bytes.restype = sz
     lib.gdn2_recurrent_fwd.argtypes = [vp] * 6 + [ctypes.c_float, vp, vp, vp, vp,
@@ -165,6 +168,19 @@ def workspace_bytes(dims: Dims) -> int:
     return int(load().gdn2_workspace_bytes(ctypes.byref(dims)))
 
 
+def _check_inputs(q, k, v, cu_seqlens, initial_state):
+    """The checks every wrapper makes before marshalling: packed input with
+    cu_seqlens, CUDA tensors, and a contiguous initial state (the C ABI takes
+    the state without strides)."""
+    if cu_seqlens is None:
+        raise ValueError("cu_seqlens is required (packed input only)")
+    for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens", cu_seqlens), ("initial_state", initial_state)):
+        if t is not None and not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+    if initial_state is not None and not initial_state.is_contiguous():
+        raise ValueError("initial_state must be contiguous [N, HV, K, V]")
+
+
 def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=None,
                    cu_seqlens=None, output_final_state=True, use_qk_l2norm=False, out=None,
                    final_state=None, workspace=None, impl="tc", stream=None, stage_events=None,
@@ -177,11 +193,7 @@ def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state
     final_state [N, HV, K, V] fp32 or None).
     """
     lib = load()
-    if cu_seqlens is None:
-        raise ValueError("cu_seqlens is required (packed input only)")
-    for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens", cu_seqlens)):
-        if not t.is_cuda:
-            raise ValueError("%s must be a CUDA tensor" % name)
+    _check_inputs(q, k, v, cu_seqlens, initial_state)
     T, H, K = q.shape
     HV, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
@@ -190,8 +202,6 @@ def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state
     sdt = _state_dtype(initial_state, final_state, state_dtype)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, HV, K, V), dtype=sdt, device=q.device)
-    if initial_state is not None and not initial_state.is_contiguous():
-        raise ValueError("initial_state must be contiguous [N, HV, K, V] fp32")
     dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, impl, state_v_major, sdt)
     dims.state_segments = int(state_segments)  # 0: chosen by the library
     nbytes = workspace_bytes(dims)
@@ -219,8 +229,10 @@ def chunk_gdn2_fwd_noalloc(q, k, v, g=None, beta=None, w=None, scale=None, initi
     """The forward through ``gdn2_chunk_fwd_noalloc``: no workspace argument;
     the library's fixed device scratch (NOALLOC_SCRATCH_BYTES) is used, so
     calls must not overlap on the GPU.  Outputs are allocated here only when
-    the caller does not pass them."""
+    the caller does not pass them; ``noalloc_device_status()`` reads the
+    device-side status of the last call."""
     lib = load()
+    _check_inputs(q, k, v, cu_seqlens, initial_state)
     T, H, K = q.shape
     HV, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
@@ -249,11 +261,7 @@ def recurrent_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_s
     as ``chunk_gdn2_fwd``; ``final_state`` may be ``initial_state`` itself
     (updated in place).  Returns (out, final_state)."""
     lib = load()
-    if cu_seqlens is None:
-        raise ValueError("cu_seqlens is required (packed input only)")
-    for name, t in (("q", q), ("k", k), ("v", v), ("cu_seqlens", cu_seqlens)):
-        if not t.is_cuda:
-            raise ValueError("%s must be a CUDA tensor" % name)
+    _check_inputs(q, k, v, cu_seqlens, initial_state)
     T, H, K = q.shape
     HV, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
@@ -262,8 +270,6 @@ def recurrent_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_s
     sdt = _state_dtype(initial_state, final_state, state_dtype)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, HV, K, V), dtype=sdt, device=q.device)
-    if initial_state is not None and not initial_state.is_contiguous():
-        raise ValueError("initial_state must be contiguous [N, HV, K, V] fp32")
     dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, "tc", state_v_major, sdt)
     if workspace is None:
         workspace = torch.empty(256, dtype=torch.uint8, device=q.device)
@@ -276,6 +282,18 @@ def recurrent_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_s
     if st != GDN2_OK:
         raise Gdn2Error(st, "gdn2_recurrent_fwd")
     return out, final_state
+
+
+def noalloc_device_status(device=None, stream=None) -> int:
+    """Device-side status of the last ``chunk_gdn2_fwd_noalloc`` call on the
+    current device (syncs the stream)."""
+    if stream is None:
+        stream = torch.cuda.current_stream(device).cuda_stream
+    s = ctypes.c_int32(-1)
+    st = load().gdn2_noalloc_device_status(stream, ctypes.byref(s))
+    if st != GDN2_OK:
+        raise Gdn2Error(st, "gdn2_noalloc_device_status")
+    return int(s.value)
 
 
 def device_status(workspace, stream=None) -> int:

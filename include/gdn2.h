@@ -61,8 +61,11 @@ typedef enum gdn2_status {
     GDN2_ERR_IMPL = 11,       /* unknown implementation selector                      */
     GDN2_ERR_TIMEOUT = 12,    /* device-side: a kernel gave up waiting on one of its  */
                               /* own pipeline barriers (see gdn2_device_status)       */
-    GDN2_ERR_NOALLOC_LIMIT = 13 /* the problem needs more scratch than                */
+    GDN2_ERR_NOALLOC_LIMIT = 13, /* the problem needs more scratch than               */
                               /* gdn2_chunk_fwd_noalloc holds                         */
+    GDN2_ERR_RANGE = 14       /* device-side: a value passed the range of the fp16    */
+                              /* intermediates and was clipped; outputs are invalid   */
+                              /* (see gdn2_device_status)                             */
 } gdn2_status;
 
 typedef enum gdn2_dtype {
@@ -176,12 +179,16 @@ GDN2_API gdn2_status gdn2_check_args(const void *q, const void *k, const void *v
  *   workspace     device buffer of at least gdn2_workspace_bytes(dims) bytes
  *
  * Chunks are 64 tokens and never span two sequences; an empty sequence
- * returns final_state = initial_state.  Numerics: bf16 tensor-core operands,
- * fp32 accumulation and fp32 carried state; chunk-local decays are applied
- * through 16-token sub-chunk references (burn-gdn2 README, "Numerical
- * stability"), which stays finite while no key channel decays by more than
- * about 80 nats inside one 16-token sub-chunk (|g| <= 5 per token is always
- * inside this range).
+ * returns final_state = initial_state.  Numerics: bf16 tensor-core operands
+ * for the decayed q.k and k.k products, fp16 operands for the chunk
+ * intermediates, fp32 accumulation and fp32 carried state.  Chunk-local decays
+ * are applied through 16-token sub-chunk references (burn-gdn2 README,
+ * "Numerical stability"): every factor across sub-chunks is <= 1, and inside
+ * a sub-chunk a key channel that decays by more than 2^92 (63.8 nats) takes
+ * its decay per token pair exactly, so any g <= 0 is valid.  Values of the
+ * fp16 intermediates (which scale with v, w and the state) must stay below
+ * 65504 in magnitude: a value past that is clipped and the call reports
+ * GDN2_ERR_RANGE through gdn2_device_status (outputs then invalid).
  *
  * Returns GDN2_OK once all kernels are enqueued.  cu_seqlens is checked on
  * the device; a bad cu_seqlens makes every kernel a no-op and is reported by
@@ -264,10 +271,11 @@ GDN2_API gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void
 /*
  * Read the device-side status that the last gdn2_chunk_fwd or
  * gdn2_recurrent_fwd on this workspace wrote into *status: GDN2_OK,
- * GDN2_ERR_CU_SEQLENS, or GDN2_ERR_TIMEOUT (a tensor-core kernel waited more
- * than 2 s on one of its own barriers and unwound; its outputs are then
- * invalid).  This call SYNCHRONISES `stream`.  Returns GDN2_ERR_CUDA if the
- * copy fails.
+ * GDN2_ERR_CU_SEQLENS, GDN2_ERR_TIMEOUT (a tensor-core kernel waited more
+ * than 2 s on one of its own barriers and unwound), or GDN2_ERR_RANGE (an
+ * fp16 intermediate was clipped); with any of the last two the outputs are
+ * invalid.  If several apply, the first in that order is reported.  This call
+ * SYNCHRONISES `stream`.  Returns GDN2_ERR_CUDA if the copy fails.
  */
 GDN2_API gdn2_status gdn2_device_status(const void *workspace, void *stream, int32_t *status);
 
@@ -303,12 +311,28 @@ GDN2_API gdn2_status gdn2_device_status(const void *workspace, void *stream, int
  * Arguments and results are those of gdn2_chunk_fwd.  Returns
  * GDN2_ERR_NOALLOC_LIMIT, before touching the device, when
  * gdn2_workspace_bytes(dims) exceeds GDN2_NOALLOC_SCRATCH_BYTES;
- * GDN2_ERR_CUDA if the device address cannot be looked up.
+ * GDN2_ERR_ARCH, before the address lookup, on a device that is not compute
+ * capability 10.3; GDN2_ERR_CUDA if the device address cannot be looked up.
+ * The looked-up address belongs to the CUDA context current at the first
+ * call; it does not survive cudaDeviceReset of that device (a later call in
+ * a new context would use a stale address), so do not reset a device between
+ * calls.  The device-side status of the last call (cu_seqlens, timeout,
+ * range) is read with gdn2_noalloc_device_status.
  */
 GDN2_API gdn2_status gdn2_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *g,
                                             const void *beta, const void *w, float scale,
                                             const void *initial_state, const void *cu_seqlens, void *out,
                                             void *final_state, const gdn2_dims *dims, void *stream);
+
+/*
+ * gdn2_device_status for gdn2_chunk_fwd_noalloc: reads the status words that
+ * the last gdn2_chunk_fwd_noalloc call on the current device left in the
+ * library's scratch array (that call's caller has no workspace pointer to
+ * pass).  Same results and the same stream SYNCHRONISATION as
+ * gdn2_device_status; GDN2_ERR_ARCH or GDN2_ERR_CUDA as
+ * gdn2_chunk_fwd_noalloc.  Allocates nothing.
+ */
+GDN2_API gdn2_status gdn2_noalloc_device_status(void *stream, int32_t *status);
 
 /*
  * Self-test of the device-side failure detection.  Every wait in the

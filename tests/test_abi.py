@@ -39,9 +39,10 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_strings(lib):
     assert lib.gdn2_version() >> 16 == 1
-    for code in range(12):
+    for code in range(15):  # GDN2_OK .. GDN2_ERR_RANGE
         s = lib.gdn2_status_string(code).decode()
         assert s and s != "unknown status"
+        assert code in gdn2.STATUS_NAMES
     assert lib.gdn2_status_string(999).decode() == "unknown status"
 
 
@@ -201,15 +202,15 @@ def test_state_segments_host_logic(lib):
         assert _check(lib, d, p, ws_bytes=1 << 34) == code, (val, impl, K)
     # few (sequence, head) pairs on long sequences: P >= 3 chosen automatically
     few = _dims(lib, T=4096, N=1, H=16, HV=16, K=128, V=128)
-    assert gdn2.launch_count(few) == 5            # map, intra, transitions, combine, replay
+    assert gdn2.launch_count(few) == 6            # map, intra (2 passes), transitions, combine, replay
     seq = _dims(lib, T=4096, N=1, H=16, HV=16, K=128, V=128)
     seq.state_segments = 1
-    assert gdn2.launch_count(seq) == 3            # map, intra, state
+    assert gdn2.launch_count(seq) == 4            # map, intra (2 passes), state
     assert lib.gdn2_workspace_bytes(ctypes.byref(few)) > lib.gdn2_workspace_bytes(ctypes.byref(seq))
     many = _dims(lib, T=4096, N=2, H=16, HV=16, K=128, V=128)   # 32 pairs: sequential
-    assert gdn2.launch_count(many) == 3
+    assert gdn2.launch_count(many) == 4
     short = _dims(lib, T=1024, N=1, H=2, HV=2, K=128, V=128)    # 16 chunks: too short to split
-    assert gdn2.launch_count(short) == 3
+    assert gdn2.launch_count(short) == 4
 
 
 def test_selftest_wait_timeout_argument_checks(lib):

@@ -1,6 +1,6 @@
 """A seeded random sweep of the chunked forward against the FP64 oracle:
 ragged sequence sets (empty sequences included), D = 64 or 128, grouped value
-heads, absent gates, the fused L2 norm, initial states, fp16 inputs, 16-bit
+heads, decays up to 20 nats per token, absent gates, the fused L2 norm, initial states, fp16 inputs, 16-bit
 g, bf16 and V-major states, and the state pass forced sequential or
 chunk-parallel where the shape allows.  Each case is drawn from its own seed
 and printed on failure.
@@ -36,7 +36,7 @@ def draw(seed):
         lens[int(rng.integers(0, n))] = 0
     if sum(lens) == 0:
         lens[0] = 1
-    case = dict(D=D, H=H, HV=HV, lens=lens, g_max=float(rng.choice([0.05, 0.5, 2.0])),
+    case = dict(D=D, H=H, HV=HV, lens=lens, g_max=float(rng.choice([0.05, 0.5, 2.0, 8.0, 20.0])),
                 beta_max=float(rng.choice([1.0, 2.0])), h0=bool(rng.random() < 0.6),
                 drop=[k for k in ("g", "beta", "w") if rng.random() < 0.15], l2=bool(rng.random() < 0.3),
                 qkv=[torch.bfloat16, torch.float16][int(rng.integers(0, 2))],

@@ -57,7 +57,7 @@ def test_automatic_segments(cuda_lib):
     d = inputs.generate(wl)
     dd = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in d.items()}
     dims = gdn2_mod.make_dims(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["w"], dd["v"], dd["cu_seqlens"])
-    assert gdn2_mod.launch_count(dims) == 5  # map, intra, transitions, combine, replay
+    assert gdn2_mod.launch_count(dims) == 6  # map, intra (2 passes), transitions, combine, replay
     o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
                                        initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
     o, hT = run(cuda_lib, d, 0)
