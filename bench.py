@@ -58,6 +58,13 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other D=128 workloads (2-4) in the line's `configs` object")
+    ap.add_argument("--config-steps", type=int, default=20)
+    ap.add_argument("--config-cpu-seconds", type=float, default=4.0)
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="keep only the workload's first SEQS sequences (a smaller case of the same "
+                         "shape, for profiler captures); 0 = all")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 500 if args.op == "decode" else 30
@@ -342,25 +349,35 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args):
+def gpu_numa_cpus(dev):
+    """Host CPUs local to CUDA device `dev` (from sysfs), or None."""
     import torch
-    import torch.distributed as dist
-    from gated_deltanet_prefill_gb300 import build as gbuild
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (getattr(pr, "pci_domain_id", 0), pr.pci_bus_id, pr.pci_device_id)
+        txt = open("/sys/bus/pci/devices/%s/local_cpulist" % bus).read().strip()
+    except Exception:
+        return None
+    cpus = set()
+    for part in txt.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    return cpus or None
+
+
+def measure(wl, args, K, warmup, seed_rank=0, world=1, clocks_dev=None):
+    """Time K steps of one workload exactly as the headline is timed: inputs
+    resident in HBM, >= 3 warm-up steps, CUDA events on the launching stream,
+    a 512 MB L2 flush between steps (outside the per-step events) when the
+    inputs are under 1 GB.  Returns the timing record and the live buffers."""
+    import torch
     from gated_deltanet_prefill_gb300 import dist as gdist
     from gated_deltanet_prefill_gb300 import gdn2, inputs
 
-    rank, world, local = gdist.rank_world()
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl")
-    if rank == 0 or world == 1:
-        gbuild.build()
-    if world > 1:
-        dist.barrier()
-    gdn2.load()
-
-    wl = inputs.workload(args.workload)
-    wl_r = inputs.with_seed(wl, gdist.rank_seed(wl.seed, rank))  # each rank: its own batch
+    wl_r = inputs.with_seed(wl, gdist.rank_seed(wl.seed, seed_rank))  # each rank: its own batch
     d = inputs.generate(wl_r, device="cuda")
     T, HV, V = wl.T_tot, wl.HV, wl.V
     out = torch.empty((T, HV, V), dtype=torch.bfloat16, device="cuda")
@@ -376,11 +393,9 @@ def run_ours(args):
                             initial_state=d["h0"], cu_seqlens=d["cu_seqlens"], out=out, final_state=fs,
                             workspace=ws, impl=args.kernels, stage_events=evs)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize()
-
-    K = args.steps
     stage_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
     for evs in stage_evs:  # materialise the CUDA events
         for e in evs:
@@ -392,17 +407,23 @@ def run_ours(args):
     fmin = fused_min_bytes(wl, d["h0"] is not None)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda") if fmin < 1e9 else None
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    with Clocks(local) as clk:
-        start.record(stream)
-        for i in range(K):
-            if flush is not None:
-                flush.zero_()
-            step(stage_evs[i])
-        end.record(stream)
-        torch.cuda.synchronize()
+    clk = Clocks(clocks_dev) if clocks_dev is not None else None
+    if clk:
+        clk.__enter__()
+    start.record(stream)
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        step(stage_evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if clk:
+        clk.__exit__()
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     if flush is None:
         ms = gdist.max_over_ranks(start.elapsed_time(end) / K, device="cuda")
@@ -411,22 +432,117 @@ def run_ours(args):
         ms = gdist.max_over_ranks(sum(per_step) / K, device="cuda")
         del flush
     stage_ms = {n: sum(ev[i].elapsed_time(ev[i + 1]) for ev in stage_evs) / K for i, n in enumerate(names)}
-
-    # roofline of the dominant kernel
+    status = gdn2.device_status(ws)
     peak, peak_kind = load_peaks()
     sb = stage_bytes(wl, args.kernels, d["h0"] is not None, True, False)
-    dom = max(stage_ms, key=stage_ms.get)
-    ach = sb[dom] / (stage_ms[dom] * 1e-3) / 1e9
-    roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
-            "traffic": ncu_traffic(dom, args.kernels, wl.name), "kernel": dom,
-            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured"
-            else "fallback 6.8 TB/s"}
     stages = {n: {"ms": stage_ms[n], "algorithmic_bytes": sb.get(n),
                   "gbs": (sb[n] / (stage_ms[n] * 1e-3) / 1e9) if sb.get(n) else None,
                   "frac_of_peak": (sb[n] / (stage_ms[n] * 1e-3) / 1e9 / peak) if sb.get(n) else None,
                   "share": stage_ms[n] / max(sum(stage_ms.values()), 1e-12)} for n in names}
     whole = {"min_bytes": fmin, "achieved_gbs": fmin / (ms * 1e-3) / 1e9,
              "frac": fmin / (ms * 1e-3) / 1e9 / peak}
+    rec = {"ms": ms, "stage_ms": stage_ms, "stages": stages, "whole_op": whole, "sb": sb, "peak": peak,
+           "peak_kind": peak_kind, "fmin": fmin, "dims": dims, "status": status,
+           "clocks": clk.summary() if clk else None}
+    return rec, dict(d=d, out=out, fs=fs, ws=ws)
+
+
+def l2_note(fmin):
+    return ("inputs (%.1f GB) larger than L2 (129 MB); no flush" % (fmin / 1e9) if fmin >= 1e9 else
+            "inputs (%.2f GB) near the L2 size: a 512 MB buffer written between steps, outside the "
+            "per-step events" % (fmin / 1e9))
+
+
+def host_link(torch, h2d_bytes, d2h_bytes, reps=3):
+    """Plain pinned-memory copies on this GPU's host link, the floor an
+    end-to-end step cannot beat: one cudaMemcpyAsync each way of the step's
+    bytes, alone and both directions at once (best of `reps`)."""
+    src = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(h2d_bytes, dtype=torch.uint8, device="cuda")
+    dsrc = torch.empty(d2h_bytes, dtype=torch.uint8, device="cuda")
+    ddst = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn):
+        best = None
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            t = a.elapsed_time(b)
+            best = t if best is None else min(best, t)
+        return best
+
+    def both():
+        cur = torch.cuda.current_stream()
+        s1.wait_stream(cur)
+        s2.wait_stream(cur)
+        with torch.cuda.stream(s1):
+            dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(s2):
+            ddst.copy_(dsrc, non_blocking=True)
+        cur.wait_stream(s1)
+        cur.wait_stream(s2)
+
+    h_ms = timed(lambda: dst.copy_(src, non_blocking=True))
+    d_ms = timed(lambda: ddst.copy_(dsrc, non_blocking=True))
+    b_ms = timed(both)
+    del src, dst, dsrc, ddst
+    return {"h2d_gbs": h2d_bytes / (h_ms * 1e-3) / 1e9, "d2h_gbs": d2h_bytes / (d_ms * 1e-3) / 1e9,
+            "h2d_ms": h_ms, "d2h_ms": d_ms, "both_ms": b_ms,
+            "how": "one pinned cudaMemcpyAsync of the step's bytes each way, alone and both at once "
+                   "(two streams); best of %d" % reps}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from gated_deltanet_prefill_gb300 import build as gbuild
+    from gated_deltanet_prefill_gb300 import dist as gdist
+    from gated_deltanet_prefill_gb300 import gdn2, inputs
+
+    rank, world, local = gdist.rank_world()
+    torch.cuda.set_device(local)
+    # host threads and first-touch host pages near this GPU (pinned buffers of
+    # the end-to-end leg land on the GPU's own NUMA node)
+    near = gpu_numa_cpus(local)
+    numa = None
+    if near:
+        try:
+            os.sched_setaffinity(0, near)
+            numa = "bound to the %d CPUs local to the GPU (sysfs local_cpulist)" % len(near)
+        except Exception:
+            numa = None
+    if world > 1:
+        dist.init_process_group("nccl")
+    if rank == 0 or world == 1:
+        gbuild.build()
+    if world > 1:
+        dist.barrier()
+    gdn2.load()
+
+    wl = inputs.workload(args.workload)
+    if args.seqs > 0 and args.seqs < wl.N:
+        import dataclasses
+        wl = dataclasses.replace(wl, name="%s_first%d" % (wl.name, args.seqs), lens=wl.lens[:args.seqs])
+    T = wl.T_tot
+    K = args.steps
+    rec, buf = measure(wl, args, K, args.warmup, seed_rank=rank, world=world, clocks_dev=local)
+    d, ms, stage_ms, stages, whole = buf["d"], rec["ms"], rec["stage_ms"], rec["stages"], rec["whole_op"]
+    dims, fmin, peak, peak_kind, sb = rec["dims"], rec["fmin"], rec["peak"], rec["peak_kind"], rec["sb"]
+    stream = torch.cuda.current_stream()
+
+    # roofline of the dominant kernel
+    dom = max(stage_ms, key=stage_ms.get)
+    ach = sb[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+            "traffic": ncu_traffic(dom, args.kernels, wl.name), "kernel": dom,
+            "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
+    del buf["out"], buf["fs"], buf["ws"]
 
     # end-to-end from pinned host buffers through the public API
     e2e = None
@@ -449,16 +565,44 @@ def run_ours(args):
         # the mean, minimum and maximum are reported beside it
         per = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.e2e_steps)]
         ems = gdist.max_over_ranks(statistics.median(per), device="cuda")
+        h2d, d2h = runner.h2d_bytes, runner.d2h_bytes
+        del runner, host
+        link = host_link(torch, h2d, d2h)
+        # the step cannot beat the slower copy direction or the device step
+        floor = max(link["h2d_ms"], link["d2h_ms"], ms)
+        link["floor_ms"] = floor
+        link["frac"] = floor / ems
+        link["numa"] = numa or "not bound (no sysfs local_cpulist)"
         e2e = {"value": gdist.aggregate_throughput(T, world, ems), "unit": "tokens/s",
-               "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": ems, "stat": "median of %d steps" % args.e2e_steps, "steps": args.e2e_steps,
                "warmup": 2, "ms_mean": evs[0].elapsed_time(evs[-1]) / args.e2e_steps,
-               "ms_min": min(per), "ms_max": max(per)}
-        del runner, host
+               "ms_min": min(per), "ms_max": max(per), "ms_all": per, "host_link": link}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(d, wl, args.cpu_seconds)
+    del d, buf
+
+    # the other D = 128 workloads, timed the same way (the headline stays on
+    # the long workload)
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = {}
+        for idx in (2, 3, 4):
+            if idx == args.workload:
+                continue
+            wli = inputs.workload(idx)
+            r, b = measure(wli, args, args.config_steps, args.warmup)
+            c = {"workload": wli.name, "ms_per_step": r["ms"], "tokens_per_s": wli.T_tot / (r["ms"] * 1e-3),
+                 "steps": args.config_steps, "warmup": max(3, args.warmup), "l2": l2_note(r["fmin"]),
+                 "stages": {n: {"ms": v["ms"], "frac_of_peak": v["frac_of_peak"]} for n, v in r["stages"].items()},
+                 "whole_op_frac": r["whole_op"]["frac"], "device_status": r["status"],
+                 "cpu_baseline": None if args.no_cpu_baseline else
+                 cpu_baseline(b["d"], wli, args.config_cpu_seconds)}
+            configs[wli.name] = c
+            del b
+            torch.cuda.empty_cache()
 
     if rank == 0:
         line = {"metric": METRIC, "value": gdist.aggregate_throughput(T, world, ms), "unit": "tokens/s",
@@ -470,14 +614,12 @@ def run_ours(args):
                            "K": wl.K, "V": wl.V, "tokens_per_step_per_gpu": T, "kernels": args.kernels,
                            "g": "-U(0,%g)" % wl.g_max, "beta": "U(0,%g)" % wl.beta_max,
                            "initial_state": "N(0,%g)" % wl.h0_std if wl.h0_std else "zero",
-                           "output_final_state": True,
-                           "l2": ("inputs (%.1f GB) larger than L2 (129 MB); no flush" % (fmin / 1e9)
-                                  if fmin >= 1e9 else "inputs (%.2f GB) near the L2 size: a 512 MB buffer written "
-                                  "between steps, outside the per-step events" % (fmin / 1e9)),
+                           "output_final_state": True, "l2": l2_note(fmin),
                            "parallelism": "replicas x%d (independent batches)" % world},
                 "roofline": roof, "stages": stages, "whole_op": whole, "e2e": e2e,
                 "cpu_baseline": cpu, "gpu_launches": gdn2.launch_count(dims) * K,
-                "clocks": clk.summary(), "source_sha": kernel_source_sha()}
+                "device_status": rec["status"], "configs": configs,
+                "clocks": rec["clocks"], "source_sha": kernel_source_sha()}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

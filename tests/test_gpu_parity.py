@@ -2,8 +2,8 @@
 
 Bar (GDN-2 prefill forward): max|o - o_ref| / max|o_ref| <= 1e-2, and the
 same bound on the final state, per compared set of outputs.  Small cases are
-compared element by element; the full-size workloads on sampled
-(sequence, value head) units that the oracle computes one by one, in the
+compared element by element; the full-size workloads on every
+(sequence, value head) unit, which the oracle computes one by one, in the
 launch configuration the benchmark times.
 """
 import numpy as np
@@ -225,18 +225,8 @@ def test_bad_cu_seqlens_reported_on_device(cuda_lib, impl):
 
 
 # ---------------------------------------------------------------------------
-# Full-size workloads: run the whole launch, compare sampled units.
+# Full-size workloads: run the whole launch, compare every unit.
 # ---------------------------------------------------------------------------
-def sample_units(wl, k=3, seed=0):
-    rng = np.random.default_rng(seed)
-    lens = np.array(wl.lens)
-    n_long = int(np.argmax(lens))
-    units = {(n_long, wl.HV - 1), (0, 0)}
-    while len(units) < k + 2:
-        units.add((int(rng.integers(wl.N)), int(rng.integers(wl.HV))))
-    return sorted(units)
-
-
 def unit_problem(d, wl, n, hv):
     """Inputs of one (sequence, value head) unit as a stand-alone problem."""
     cu = d["cu_seqlens"].tolist()
@@ -249,31 +239,55 @@ def unit_problem(d, wl, n, hv):
                 cu_seqlens=[0, b - a], scale=d["scale"]), (a, b)
 
 
-@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("index", [2, 3, 4, 5])
-def test_full_size_sampled(cuda_lib, impl, index):
-    wl = inputs.workload(index)
-    d = inputs.generate(wl, device="cuda")
-    o, hT = run_gpu(cuda_lib, d, impl)
+def test_full_size_every_unit(cuda_lib, index):
+    """Each D = 128 workload at full size, in the launch configuration the
+    benchmark times, through both GPU paths; every (sequence, value head)
+    unit's output rows and final state against the FP64 oracle (one oracle
+    call per unit, units in parallel).  The bar is the global one,
+    max|x - x_ref| / max|x_ref| <= 1e-2 over all units; the achieved errors
+    are printed, and the worst units on failure."""
+    import os
     from concurrent.futures import ThreadPoolExecutor
 
-    units = sample_units(wl)
+    wl = inputs.workload(index)
+    d = inputs.generate(wl, device="cuda")
+    outs = {}
+    for impl in IMPLS:
+        o, hT = run_gpu(cuda_lib, d, impl)
+        outs[impl] = (o.float().cpu().numpy(), hT.float().cpu().numpy())
+        del o, hT
+    units = [(n, hv) for n in range(wl.N) for hv in range(wl.HV)]
 
     def one(u):
         n, hv = u
         pd, (a, b) = unit_problem(d, wl, n, hv)
-        o_ref, h_ref = run_oracle(pd)
-        return u, (a, b), o_ref[:, 0], h_ref[0, 0]
+        o_ref, h_ref = oracle.gdn2_forward(pd["q"], pd["k"], pd["v"], pd["g"], pd["beta"], pd["w"],
+                                           scale=pd["scale"], initial_state=pd["h0"],
+                                           cu_seqlens=pd["cu_seqlens"], threads=1)
+        res = {"ref": (float(np.abs(o_ref).max(initial=0.0)), float(np.abs(h_ref).max()))}
+        for impl, (o, hT) in outs.items():
+            res[impl] = (float(np.abs(o[a:b, hv] - o_ref[:, 0]).max(initial=0.0)),
+                         float(np.abs(hT[n, hv] - h_ref[0, 0]).max()))
+        return u, res
 
-    with ThreadPoolExecutor(4) as ex:
-        res = list(ex.map(one, units))
-    o_cat, r_cat, h_cat, hr_cat = [], [], [], []
-    for (n, hv), (a, b), o_ref, h_ref in res:
-        o_cat.append(o[a:b, hv].float().cpu().numpy()); r_cat.append(o_ref)
-        h_cat.append(hT[n, hv].cpu().numpy()); hr_cat.append(h_ref)
-    eo = rel_max(np.concatenate(o_cat), np.concatenate(r_cat))
-    eh = rel_max(np.stack(h_cat), np.stack(hr_cat))
-    assert eo <= TOL and eh <= TOL, "%s/%s: o err %.3e, state err %.3e" % (wl.name, impl, eo, eh)
+    with ThreadPoolExecutor(max(1, min(32, os.cpu_count() or 1))) as ex:
+        per_unit = dict(ex.map(one, units))
+    ref_o = max(r["ref"][0] for r in per_unit.values())
+    ref_h = max(r["ref"][1] for r in per_unit.values())
+    bad = []
+    for impl in IMPLS:
+        eo = max(r[impl][0] for r in per_unit.values()) / ref_o
+        eh = max(r[impl][1] for r in per_unit.values()) / ref_h
+        print("full size %s, %d units, %s: o err %.3e, final-state err %.3e"
+              % (wl.name, len(units), impl, eo, eh))
+        if eo > TOL or eh > TOL:
+            worst = sorted(per_unit.items(), key=lambda kv: -max(kv[1][impl][0] / ref_o, kv[1][impl][1] / ref_h))
+            bad.append("%s: o %.3e state %.3e; worst units %s" % (
+                impl, eo, eh, ["(n=%d, hv=%d): o %.3e state %.3e" % (u[0], u[1], r[impl][0] / ref_o,
+                                                                       r[impl][1] / ref_h)
+                                for u, r in worst[:5]]))
+    assert not bad, "; ".join(bad)
 
 
 @pytest.mark.parametrize("groups,slices", [(1, 0), (3, 0), (4, 4), (4, 8)])
