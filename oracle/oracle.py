@@ -55,7 +55,7 @@ def load_library(path: str):
     f = lib.gdn2_oracle_forward
     dp = ctypes.c_void_p
     f.argtypes = [dp, dp, dp, dp, dp, dp, ctypes.c_double, dp, dp,
-                  ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                   ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, ctypes.c_int,
                   dp, dp, ctypes.c_int]
     f.restype = ctypes.c_int
@@ -88,14 +88,16 @@ def gdn2_forward(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=N
                  cu_seqlens=None, use_qk_l2norm=False, units=None, threads=None, lib=None):
     """Run the oracle.
 
-    q, k: [T, H, K]; v, w: [T, HV, V]; g, beta: [T, HV, K]; initial_state
-    [N, HV, K, V]; cu_seqlens [N + 1].  A leading batch dim of size B on
-    q..w (fixed-length [B, T, ...] input) is folded into T when cu_seqlens is
-    None.  ``units`` is an optional list of (n, hv) pairs to compute; rows of
+    q: [T, H, K]; k: [T, HK, K]; v: [T, HV, V]; with HS = max(H, HV) state
+    heads: g, beta [T, HS, K]; w [T, HS, V]; initial_state [N, HS, K, V];
+    cu_seqlens [N + 1].  HK equals H or HV, and H, HV are equal or one a
+    multiple of the other.  A leading batch dim of size B on q..w
+    (fixed-length [B, T, ...] input) is folded into T when cu_seqlens is
+    None.  ``units`` is an optional list of (n, hs) pairs to compute; rows of
     other units in the returned ``o`` are NaN and their final states NaN.
     ``lib`` selects another compiled copy of the oracle (see load_library).
 
-    Returns (o [T, HV, V], final_state [N, HV, K, V]) as float64 arrays.
+    Returns (o [T, HS, V], final_state [N, HS, K, V]) as float64 arrays.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     g, beta, w, h0 = _f64(g), _f64(beta), _f64(w), _f64(initial_state)
@@ -111,25 +113,27 @@ def gdn2_forward(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=N
         cu_seqlens = cu_seqlens.detach().cpu().numpy()
     cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
     T_tot, H, K = q.shape
+    HK = k.shape[1]
     HV, V = v.shape[1], v.shape[2]
+    HS = max(H, HV)
     N = cu.shape[0] - 1
-    assert k.shape == (T_tot, H, K) and v.shape == (T_tot, HV, V)
-    for x, shp in ((g, (T_tot, HV, K)), (beta, (T_tot, HV, K)), (w, (T_tot, HV, V)),
-                   (h0, (N, HV, K, V))):
+    assert k.shape == (T_tot, HK, K) and v.shape == (T_tot, HV, V)
+    for x, shp in ((g, (T_tot, HS, K)), (beta, (T_tot, HS, K)), (w, (T_tot, HS, V)),
+                   (h0, (N, HS, K, V))):
         assert x is None or x.shape == shp, (None if x is None else x.shape, shp)
-    o = np.full((T_tot, HV, V), np.nan)
-    hT = np.full((N, HV, K, V), np.nan)
+    o = np.full((T_tot, HS, V), np.nan)
+    hT = np.full((N, HS, K, V), np.nan)
     if units is not None:
         u = np.ascontiguousarray(np.asarray(units, dtype=np.int32).reshape(-1, 2))
         n_units = u.shape[0]
     else:
-        u, n_units = None, N * HV
+        u, n_units = None, N * HS
     if threads is None:
         threads = max(1, min(os.cpu_count() or 1, n_units))
     rc = (lib or _load()).gdn2_oracle_forward(
         _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(w),
         0.0 if scale is None else float(scale), _ptr(h0), _ptr(cu),
-        T_tot, N, H, HV, K, V, int(bool(use_qk_l2norm)), _ptr(u), n_units,
+        T_tot, N, H, HK, HV, K, V, int(bool(use_qk_l2norm)), _ptr(u), n_units,
         _ptr(o), _ptr(hT), int(threads))
     if rc != 0:
         raise ValueError("oracle rejected its arguments (code %d)" % rc)

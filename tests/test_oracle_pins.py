@@ -251,6 +251,39 @@ def pin_grouped_heads(fwd):
     assert rel_err(o, o3) > 1e-3, "GVA head map is not distinguishable"
 
 
+def pin_head_counts(fwd):
+    """The FlashInfer docs' head counts: HK equals H or HV, and H, HV are
+    equal or one a multiple of the other; one state per state head hs < HS =
+    max(H, HV), which reads q head hs // (HS / H), k head hs // (HS / HK) and
+    v head hs // (HS / HV).  Each case equals H = HK = HV = HS with q, k, v
+    expanded by those maps; a map taken modulo the head count is
+    distinguishable."""
+    rng = np.random.default_rng(25)
+    T, K, V = 13, 4, 3
+    for H, HK, HV in ((4, 2, 2), (4, 4, 2), (2, 4, 4), (2, 2, 4), (3, 3, 6), (6, 2, 2)):
+        HS = max(H, HV)
+        q = rng.standard_normal((T, H, K))
+        k = rng.standard_normal((T, HK, K))
+        v = rng.standard_normal((T, HV, V))
+        g = -0.5 * rng.random((T, HS, K))
+        beta = rng.random((T, HS, K))
+        w = rng.random((T, HS, V))
+        S0 = rng.standard_normal((1, HS, K, V))
+        o, hT = fwd(q, k, v, g, beta, w, initial_state=S0, scale=0.5)
+        assert o.shape == (T, HS, V) and hT.shape == (1, HS, K, V)
+        iq, ik, iv = (np.arange(HS) // (HS // n) for n in (H, HK, HV))
+        o2, h2 = fwd(q[:, iq], k[:, ik], v[:, iv], g, beta, w, initial_state=S0, scale=0.5)
+        close(o, o2, what="heads %s o" % ((H, HK, HV),))
+        close(hT, h2, what="heads %s state" % ((H, HK, HV),))
+        for n, arr, pos in ((H, q, 0), (HK, k, 1), (HV, v, 2)):
+            if n == HS:
+                continue
+            mod = [q[:, iq], k[:, ik], v[:, iv]]
+            mod[pos] = arr[:, np.arange(HS) % n]
+            o3, _ = fwd(*mod, g, beta, w, initial_state=S0, scale=0.5)
+            assert rel_err(o, o3) > 1e-3, "head map of tensor %d not distinguishable at %s" % (pos, (H, HK, HV))
+
+
 def pin_l2norm(fwd):
     """The fused q/k L2 norm equals pre-normalised input; it is a no-op on
     unit rows."""
@@ -298,7 +331,7 @@ def pin_defaults(fwd):
 
 PINS = [pin_brute_force, pin_scalar_gdn, pin_linear_attention, pin_single_token,
         pin_split_sequence, pin_delta_write, pin_decay_only, pin_packing,
-        pin_grouped_heads, pin_l2norm, pin_channel_permutations, pin_defaults]
+        pin_grouped_heads, pin_head_counts, pin_l2norm, pin_channel_permutations, pin_defaults]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -338,7 +371,9 @@ MUTANTS = {
     "erase_without_beta": ("const double bk = (b ? b[c] : 1.0) * kt[c];", "const double bk = kt[c];"),
     "write_gate_dropped": ("u[j] = (w ? w[j] : 1.0) * vv[j] - u[j];", "u[j] = vv[j] - u[j];"),
     "decay_sign": ("const double a = exp(g[c]);", "const double a = exp(-g[c]);"),
-    "head_map_modulo": ("const int h = hv / (HV / H);", "const int h = hv % H;"),
+    "head_map_modulo": ("const int hq = hs / (HS / H);", "const int hq = hs % H;"),
+    "k_head_map_modulo": ("const int hk = hs / (HS / HK);", "const int hk = hs % HK;"),
+    "v_head_map_modulo": ("const int hvv = hs / (HS / HV);", "const int hvv = hs % HV;"),
     "write_with_q": ("row[j] += kt[c] * u[j];", "row[j] += qt[c] * u[j];"),
     "scale_dropped": ("for (j = 0; j < V; j++) o[j] *= J->scale;", ""),
     "l2_dropped": ("for (i = 0; i < n; i++) y[i] = x[i] / d;", "for (i = 0; i < n; i++) y[i] = x[i];"),
