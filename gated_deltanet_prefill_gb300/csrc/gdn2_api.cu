@@ -87,7 +87,10 @@ bool strides_ok(const void *base, const int64_t *st, size_t esize, int heads, in
 }  // namespace
 
 bool shape_ok(const gdn2_dims &d) {
-    if (d.T_tot < 0 || d.N < 0 || d.H <= 0 || d.HV <= 0 || d.HV % d.H != 0) return false;
+    if (d.T_tot < 0 || d.N < 0 || d.H <= 0 || d.HV <= 0 || d.HK < 0) return false;
+    const int hk = dims_hk(d);
+    if (hk != d.H && hk != d.HV) return false;            // num_k_heads = num_q_heads or num_v_heads
+    if (d.HV % d.H != 0 && d.H % d.HV != 0) return false;  // one a multiple of the other
     if (d.K != d.V || (d.K != 64 && d.K != 128)) return false;
     if (nc_max(d) > (1ll << 30)) return false;
     return true;
@@ -105,7 +108,7 @@ int scan_segments(const gdn2_dims &d) {
     if (d.impl != GDN2_IMPL_TC || d.K != 128 || d.V != 128 || d.N <= 0) return 1;
     if (d.state_segments > 0) return d.state_segments;
     constexpr int64_t kWave = 152;
-    const int64_t units = static_cast<int64_t>(d.N) * d.HV;
+    const int64_t units = static_cast<int64_t>(d.N) * dims_hs(d);
     const int64_t chunks = d.T_tot / (static_cast<int64_t>(kChunk) * d.N);  // mean per sequence
     auto waves = [](int64_t ctas) { return static_cast<double>((ctas + kWave - 1) / kWave); };
     auto pass = [&](int64_t P) {  // one state pass over P segments per (sequence, head)
@@ -128,6 +131,7 @@ WsLayout workspace_layout(const gdn2_dims &d) {
     WsLayout L;
     memset(&L, 0, sizeof(L));
     const size_t T = static_cast<size_t>(d.T_tot), NC = static_cast<size_t>(nc_max(d));
+    const size_t HS = static_cast<size_t>(dims_hs(d)), HK = static_cast<size_t>(dims_hk(d));
     size_t off = 0;
     auto take = [&](size_t bytes) { const size_t o = off; off += align_up(bytes); return o; };
     L.status = take(64);
@@ -137,20 +141,20 @@ WsLayout workspace_layout(const gdn2_dims &d) {
     L.seq_first = take((static_cast<size_t>(d.N) + 1) * 4);
     L.seq_order = take(static_cast<size_t>(d.N) * 4);
     if (d.impl == GDN2_IMPL_SIMT) {
-        L.G = take(T * d.HV * d.K * 4);
+        L.G = take(T * HS * d.K * 4);
         L.qn = take(d.use_qk_l2norm ? T * d.H * d.K * 2 : 0);
-        L.kn = take(d.use_qk_l2norm ? T * d.H * d.K * 2 : 0);
-        L.Wt = take(T * d.HV * d.K * 2);
-        L.Ut = take(T * d.HV * d.V * 2);
-        L.hbuf = take(NC * d.HV * d.K * d.V * 2);
-        L.vnew = take(T * d.HV * d.V * 2);
+        L.kn = take(d.use_qk_l2norm ? T * HK * d.K * 2 : 0);
+        L.Wt = take(T * HS * d.K * 2);
+        L.Ut = take(T * HS * d.V * 2);
+        L.hbuf = take(NC * HS * d.K * d.V * 2);
+        L.vnew = take(T * HS * d.V * 2);
     } else {
         off = (off + 1023) & ~static_cast<size_t>(1023);  // records are 1 KB aligned
-        L.rec = take(NC * d.HV * tc_record_bytes(d.K));
-        L.exact_list = take(NC * d.HV * 4);
+        L.rec = take(NC * HS * tc_record_bytes(d.K));
+        L.exact_list = take(NC * HS * 4);
         const size_t P = static_cast<size_t>(scan_segments(d));
         if (P > 1) {
-            const size_t units = static_cast<size_t>(d.N) * (P - 1) * d.HV;
+            const size_t units = static_cast<size_t>(d.N) * (P - 1) * HS;
             L.sc_tr = take(units * d.K * (d.K + d.V) * 4);
             L.sc_si = take(units * d.K * d.V * 4);
         }
@@ -171,7 +175,7 @@ const char *gdn2_status_string(int status) {
     switch (status) {
         case GDN2_OK: return "ok";
         case GDN2_ERR_NULL: return "a required pointer is NULL";
-        case GDN2_ERR_SHAPE: return "unsupported sizes (need K == V in {64,128}, HV a multiple of H, N >= 0, T_tot >= 0)";
+        case GDN2_ERR_SHAPE: return "unsupported sizes (need K == V in {64,128}, key heads equal to query or value heads, query and value heads equal or one a multiple of the other, N >= 0, T_tot >= 0)";
         case GDN2_ERR_STRIDE: return "bad stride or alignment (innermost stride 1; strides and base pointers multiples of 16 bytes)";
         case GDN2_ERR_ALIAS: return "an output overlaps an input (or final_state overlaps initial_state)";
         case GDN2_ERR_WORKSPACE: return "workspace missing or smaller than gdn2_workspace_bytes()";
@@ -193,11 +197,14 @@ gdn2_status gdn2_dims_init(gdn2_dims *d, int64_t T_tot, int32_t N, int32_t H, in
     if (!d) return GDN2_ERR_NULL;
     memset(d, 0, sizeof(*d));
     d->T_tot = T_tot; d->N = N; d->H = H; d->HV = HV; d->K = K; d->V = V;
+    d->HK = 0;  // key heads = query heads
+    const int64_t HS = H > HV ? H : HV;  // state heads: g, beta, w, out
     d->q_stride[0] = d->k_stride[0] = static_cast<int64_t>(H) * K;
     d->q_stride[1] = d->k_stride[1] = K;
-    d->v_stride[0] = d->w_stride[0] = d->o_stride[0] = static_cast<int64_t>(HV) * V;
+    d->v_stride[0] = static_cast<int64_t>(HV) * V;
+    d->w_stride[0] = d->o_stride[0] = HS * V;
     d->v_stride[1] = d->w_stride[1] = d->o_stride[1] = V;
-    d->g_stride[0] = d->beta_stride[0] = static_cast<int64_t>(HV) * K;
+    d->g_stride[0] = d->beta_stride[0] = HS * K;
     d->g_stride[1] = d->beta_stride[1] = K;
     d->dtype_qkv = GDN2_DTYPE_BF16;
     d->dtype_g = GDN2_DTYPE_F32;
@@ -240,26 +247,27 @@ gdn2_status check_args(const void *q, const void *k, const void *v, const void *
     if (!cu_seqlens || !workspace) return GDN2_ERR_NULL;
     if (d->T_tot > 0 && (!q || !k || !v || !out)) return GDN2_ERR_NULL;
     const int64_t T = d->T_tot;
-    if (!strides_ok(q, d->q_stride, 2, d->H, d->K) || !strides_ok(k, d->k_stride, 2, d->H, d->K) ||
-        !strides_ok(v, d->v_stride, 2, d->HV, d->V) || !strides_ok(w, d->w_stride, 2, d->HV, d->V) ||
-        !strides_ok(beta, d->beta_stride, 2, d->HV, d->K) || !strides_ok(g, d->g_stride, g_es, d->HV, d->K) ||
-        !strides_ok(out, d->o_stride, 2, d->HV, d->V))
+    const int HS = dims_hs(*d), HK = dims_hk(*d);
+    if (!strides_ok(q, d->q_stride, 2, d->H, d->K) || !strides_ok(k, d->k_stride, 2, HK, d->K) ||
+        !strides_ok(v, d->v_stride, 2, d->HV, d->V) || !strides_ok(w, d->w_stride, 2, HS, d->V) ||
+        !strides_ok(beta, d->beta_stride, 2, HS, d->K) || !strides_ok(g, d->g_stride, g_es, HS, d->K) ||
+        !strides_ok(out, d->o_stride, 2, HS, d->V))
         return GDN2_ERR_STRIDE;
     if ((initial_state && reinterpret_cast<uintptr_t>(initial_state) % 16) ||
         (final_state && reinterpret_cast<uintptr_t>(final_state) % 16))
         return GDN2_ERR_STRIDE;
     // out rows must not overlap each other
-    if (T > 0 && (d->o_stride[1] < d->V || d->o_stride[0] < static_cast<int64_t>(d->HV - 1) * d->o_stride[1] + d->V))
+    if (T > 0 && (d->o_stride[1] < d->V || d->o_stride[0] < static_cast<int64_t>(HS - 1) * d->o_stride[1] + d->V))
         return GDN2_ERR_ALIAS;
-    const size_t state_bytes = static_cast<size_t>(d->N) * d->HV * d->K * d->V * s_es;
-    const Range r_out = tensor_range(out, T, d->HV, d->V, d->o_stride, 2);
+    const size_t state_bytes = static_cast<size_t>(d->N) * HS * d->K * d->V * s_es;
+    const Range r_out = tensor_range(out, T, HS, d->V, d->o_stride, 2);
     const Range r_fs = flat_range(final_state, state_bytes);
     // the recurrent call may update the state in place (the same pointer)
     const bool in_place = recurrent && initial_state && initial_state == final_state;
     const Range ins[] = {
-        tensor_range(q, T, d->H, d->K, d->q_stride, 2),     tensor_range(k, T, d->H, d->K, d->k_stride, 2),
-        tensor_range(v, T, d->HV, d->V, d->v_stride, 2),    tensor_range(w, T, d->HV, d->V, d->w_stride, 2),
-        tensor_range(beta, T, d->HV, d->K, d->beta_stride, 2), tensor_range(g, T, d->HV, d->K, d->g_stride, g_es),
+        tensor_range(q, T, d->H, d->K, d->q_stride, 2),     tensor_range(k, T, HK, d->K, d->k_stride, 2),
+        tensor_range(v, T, d->HV, d->V, d->v_stride, 2),    tensor_range(w, T, HS, d->V, d->w_stride, 2),
+        tensor_range(beta, T, HS, d->K, d->beta_stride, 2), tensor_range(g, T, HS, d->K, d->g_stride, g_es),
         flat_range(cu_seqlens, (static_cast<size_t>(d->N) + 1) * (d->cu_seqlens_i64 ? 8 : 4)),
         flat_range(workspace, workspace_bytes)};
     for (const Range &r : ins)
@@ -331,8 +339,9 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     p.o = static_cast<bf16 *>(out);
     p.h0 = initial_state; p.hT = final_state;
     p.cu = cu_seqlens; p.cu64 = d->cu_seqlens_i64 ? 1 : 0;
-    p.T_tot = d->T_tot; p.N = d->N; p.H = d->H; p.HV = d->HV; p.K = d->K; p.V = d->V;
-    p.group = d->HV / d->H;
+    const int HS = dims_hs(*d), HK = dims_hk(*d);
+    p.T_tot = d->T_tot; p.N = d->N; p.H = d->H; p.HK = HK; p.HV = HS; p.K = d->K; p.V = d->V;
+    p.gq = HS / d->H; p.gk = HS / HK; p.gv = HS / d->HV;
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d->K));
     p.has_g = g != nullptr; p.has_beta = beta != nullptr; p.has_w = w != nullptr;
     p.l2norm = d->use_qk_l2norm ? 1 : 0;
@@ -367,7 +376,7 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     if (d->K == 128) {
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-            2ll * d->N * d->HV * p.sc_P <= sms)
+            2ll * d->N * HS * p.sc_P <= sms)
             p.vtile = 64;
     }
     // tensor maps for the intra kernel's g / v / w tiles (GDN2_ROW_COPIES=1
@@ -383,21 +392,22 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
                                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         const int64_t g_es = d->dtype_g == GDN2_DTYPE_F32 ? 4 : 2;
         p.tmap = !force_rows &&
-                 (!p.has_g || encode_rows(&p.tm_g, &p.tm_order_g, g, tg, g_es, d->K, d->HV, d->T_tot, p.sg_t,
+                 (!p.has_g || encode_rows(&p.tm_g, &p.tm_order_g, g, tg, g_es, d->K, HS, d->T_tot, p.sg_t,
                                           p.sg_h)) &&
                  encode_rows(&p.tm_v, &p.tm_order_v, v, t16, 2, d->V, d->HV, d->T_tot, p.sv_t, p.sv_h) &&
-                 (!p.has_w || encode_rows(&p.tm_w, &p.tm_order_w, w, t16, 2, d->V, d->HV, d->T_tot, p.sw_t, p.sw_h));
+                 (!p.has_w || encode_rows(&p.tm_w, &p.tm_order_w, w, t16, 2, d->V, HS, d->T_tot, p.sw_t, p.sw_h));
         p.tpre = p.tmap &&
-                 encode_rows(&p.tm_k, &p.tm_order_k, k, t16, 2, d->K, d->H, d->T_tot, p.sk_t, p.sk_h) &&
+                 encode_rows(&p.tm_k, &p.tm_order_k, k, t16, 2, d->K, HK, d->T_tot, p.sk_t, p.sk_h) &&
                  encode_rows(&p.tm_q, &p.tm_order_q, q, t16, 2, d->K, d->H, d->T_tot, p.sq_t, p.sq_h) &&
                  (!p.has_beta ||
-                  encode_rows(&p.tm_b, &p.tm_order_b, beta, t16, 2, d->K, d->HV, d->T_tot, p.sb_t, p.sb_h));
+                  encode_rows(&p.tm_b, &p.tm_order_b, beta, t16, 2, d->K, HS, d->T_tot, p.sb_t, p.sb_h));
     }
     p.q_in = p.q; p.k_in = p.k;
     p.sq_in_t = p.sq_t; p.sq_in_h = p.sq_h; p.sk_in_t = p.sk_t; p.sk_in_h = p.sk_h;
     if (p.l2norm && d->impl == GDN2_IMPL_SIMT) {  // SIMT kernels read the normalised packed copies
         p.q = p.qn; p.k = p.kn;
-        p.sq_t = p.sk_t = static_cast<int64_t>(p.H) * p.K;
+        p.sq_t = static_cast<int64_t>(p.H) * p.K;
+        p.sk_t = static_cast<int64_t>(p.HK) * p.K;
         p.sq_h = p.sk_h = p.K;
     }
 

@@ -35,7 +35,12 @@ struct Params {
     const void *cu;
     int cu64;
     int64_t T_tot;
-    int N, H, HV, K, V, group;  // group = HV / H
+    // Heads: H query heads, HK key heads, and HV here counts the STATE heads
+    // HS = max(H, value heads) (g, beta, w, the states and the output are per
+    // state head).  State head hv reads q head hv / gq, k head hv / gk and v
+    // head hv / gv (gq = HS / H, gk = HS / HK, gv = HS / value heads).
+    int N, H, HK, HV, K, V;
+    int gq, gk, gv;
     float scale;
     int has_g, has_beta, has_w, l2norm;
     int in_f16;                 // q, k, v, beta, w, out are fp16 (else bf16)
@@ -51,7 +56,7 @@ struct Params {
     int *seq_first;             // [N + 1]  first chunk of sequence n; [N] = NC
     int *seq_order;             // [N]      sequences by chunk count, longest first
     float *G;                   // [T_tot, HV, K]  chunk-local inclusive cumsum of g
-    bf16 *qn, *kn;              // [T_tot, H, K]   L2-normalised q, k (l2norm only)
+    bf16 *qn, *kn;              // [T_tot, H, K], [T_tot, HK, K]  L2-normalised q, k (l2norm only)
     bf16 *Wt, *Ut;              // [T_tot, HV, K], [T_tot, HV, V]  WY pseudo-keys / values
     bf16 *hbuf;                 // [NCmax, HV, K, V] state entering each chunk (bf16)
     bf16 *vnew;                 // [T_tot, HV, V]  u_t (v_new) per token
@@ -98,9 +103,14 @@ gdn2_status check_args(const void *q, const void *k, const void *v, const void *
                        const void *w, const void *initial_state, const void *cu_seqlens, const void *out,
                        const void *final_state, const gdn2_dims *d, const void *workspace,
                        size_t workspace_bytes, bool recurrent);
+// Head counts of a problem: key heads (dims.HK, 0 = H) and state heads
+// HS = max(H, HV), one state per state head.
+inline int dims_hk(const gdn2_dims &d) { return d.HK > 0 ? d.HK : d.H; }
+inline int dims_hs(const gdn2_dims &d) { return d.H > d.HV ? d.H : d.HV; }
 // True if the current device is compute capability 10.3 (its index in *dev).
 bool device_is_sm103(int *dev);
-// Shapes the library supports (K = V in {64, 128}, HV a multiple of H, ...).
+// Shapes the library supports (K = V in {64, 128}, HK equal to H or HV, H and
+// HV equal or one a multiple of the other, ...).
 bool shape_ok(const gdn2_dims &d);
 
 // One element of a 16-bit input (bf16, or fp16 when f16) as fp32.

@@ -131,14 +131,19 @@ __global__ void gdn2_cumsum_kernel(Params p) {
     }
 }
 
-// Row L2 norm of q and k, one warp per (token, head) row, fp32 math, bf16 out.
+// Row L2 norm of q (H heads) and k (HK heads), one warp per (token, head)
+// row (the q rows first, then the k rows), fp32 math, bf16 out.
 __global__ void gdn2_l2norm_kernel(Params p) {
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
+    int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
-    if (row >= p.T_tot * p.H) return;
-    const int64_t t = row / p.H;
-    const int h = static_cast<int>(row % p.H);
-    for (int which = 0; which < 2; ++which) {
+    const int64_t qrows = p.T_tot * p.H;
+    if (row >= qrows + p.T_tot * p.HK) return;
+    const int which = row >= qrows;  // 0: q, 1: k
+    if (which) row -= qrows;
+    const int heads = which ? p.HK : p.H;
+    const int64_t t = row / heads;
+    const int h = static_cast<int>(row % heads);
+    {
         const bf16 *src = which ? p.k_in + t * p.sk_in_t + h * p.sk_in_h : p.q_in + t * p.sq_in_t + h * p.sq_in_h;
         bf16 *dst = (which ? p.kn : p.qn) + row * p.K;
         float x[4];
@@ -163,7 +168,7 @@ cudaError_t launch_chunk_map(const Params &p, cudaStream_t s) {
 
 cudaError_t launch_prep(const Params &p, cudaStream_t s) {
     if (p.l2norm && p.T_tot > 0) {
-        const int64_t rows = p.T_tot * p.H;
+        const int64_t rows = p.T_tot * (p.H + p.HK);
         const int per_block = 8;
         gdn2_l2norm_kernel<<<static_cast<unsigned>((rows + per_block - 1) / per_block), 32 * per_block, 0, s>>>(p);
     }

@@ -34,11 +34,11 @@ struct RecParams {
     const void *cu;
     int cu64;
     int64_t T_tot;
-    int N, HV, group;
+    int N, HV, gq, gk, gv;  // HV: state heads HS; q / k / v head of state head hv: hv / gq, gk, gv
     float scale;
     int has_g, has_beta, has_w, l2norm;
     int in_f16, g_dtype, state_vmajor, state_bf16;
-    int *status;  // [0] cu_seqlens status, [1] 0, [2] 0
+    int *status;  // [0] cu_seqlens status, [1] 0, [2] 0, [3] 0
 };
 
 __device__ __forceinline__ int64_t rec_cu(const RecParams &p, int i) {
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
     if (p.status[0] != GDN2_OK) return;
     const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
     const int n = blockIdx.x, hv = blockIdx.y, j = 32 * blockIdx.z + lane;
-    const int h = hv / p.group;
+    const int hk = hv / p.gk, hq = hv / p.gq, hvv = hv / p.gv;  // key, query and value heads
     const int64_t t0 = rec_cu(p, n), t1 = rec_cu(p, n + 1);
     const size_t sbase = (static_cast<size_t>(n) * p.HV + hv) * K * K;  // [N, HV, K, V], K == V
 
@@ -89,8 +89,8 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
                : GEN ? state_ld(p.h0, sbase + state_off(32 * wp + r, j, K, K, vmajor), sbf16)
                      : static_cast<const float *>(p.h0)[sbase + static_cast<size_t>(32 * wp + r) * K + j];
     for (int64_t t = t0; t < t1; ++t) {
-        float kc = ld16(p.k, t * p.sk_t + static_cast<int64_t>(h) * p.sk_h + tid);
-        float qc = ld16(p.q, t * p.sq_t + static_cast<int64_t>(h) * p.sq_h + tid);
+        float kc = ld16(p.k, t * p.sk_t + static_cast<int64_t>(hk) * p.sk_h + tid);
+        float qc = ld16(p.q, t * p.sq_t + static_cast<int64_t>(hq) * p.sq_h + tid);
         const float bc = p.has_beta ? ld16(p.beta, t * p.sb_t + static_cast<int64_t>(hv) * p.sb_h + tid) : 1.f;
         const float gc = p.has_g ? (GEN ? g_ld(p.g, t * p.sg_t + static_cast<int64_t>(hv) * p.sg_h + tid, gdt)
                                  : p.g[t * p.sg_t + static_cast<int64_t>(hv) * p.sg_h + tid]) : 0.f;
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
             kc *= ik; qc *= iq; qk *= ik * iq;
         }
         s_k[tid] = kc; s_bk[tid] = bc * kc; s_q[tid] = qc; s_eg[tid] = expf(gc);
-        const float vj = ld16(p.v, t * p.sv_t + static_cast<int64_t>(hv) * p.sv_h + j);
+        const float vj = ld16(p.v, t * p.sv_t + static_cast<int64_t>(hvv) * p.sv_h + j);
         const float wj = p.has_w ? ld16(p.w, t * p.sw_t + static_cast<int64_t>(hv) * p.sw_h + j) : 1.f;
         __syncthreads();
         float pr = 0.f, po = 0.f;
@@ -191,8 +191,10 @@ gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void *v, cons
     p.cu64 = d->cu_seqlens_i64 ? 1 : 0;
     p.T_tot = d->T_tot;
     p.N = d->N;
-    p.HV = d->HV;
-    p.group = d->HV / d->H;
+    p.HV = dims_hs(*d);
+    p.gq = p.HV / d->H;
+    p.gk = p.HV / dims_hk(*d);
+    p.gv = p.HV / d->HV;
     p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(d->K));
     p.has_g = g != nullptr;
     p.has_beta = beta != nullptr;
@@ -209,7 +211,7 @@ gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void *v, cons
     gdn2_recurrent_check_kernel<<<1, 256, 0, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return GDN2_ERR_LAUNCH;
     if (d->N > 0) {
-        const dim3 grid(d->N, d->HV, d->V / 32);
+        const dim3 grid(d->N, p.HV, d->V / 32);
         const bool gen = p.in_f16 || p.g_dtype != GDN2_DTYPE_F32 || p.state_vmajor || p.state_bf16;
         if (d->K == 64)
             (gen ? gdn2_recurrent_kernel<64, true> : gdn2_recurrent_kernel<64, false>)<<<grid, 64, 0, s>>>(p);

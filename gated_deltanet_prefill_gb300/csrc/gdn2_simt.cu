@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kIntraThreads) gdn2_simt_intra_kernel(Params p
     if (seq < 0) return;
     const int64_t start = p.chunk_start[c];
     const int len = p.chunk_len[c];
-    const int h = hv / p.group;
+    const int h = hv / p.gk;  // key head
 
     for (int i = tid; i < 64 * D; i += kIntraThreads) {
         const int r = i / D, ch = i % D;
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kIntraThreads) gdn2_simt_intra_kernel(Params p
         if (r < len) {
             const int64_t t = start + r;
             x1 = Bs[r * LD + ch] * Ks[r * LD + ch] * __expf(Gs[r * LD + ch]);
-            const float vv = __bfloat162float(p.v[t * p.sv_t + hv * p.sv_h + ch]);
+            const float vv = __bfloat162float(p.v[t * p.sv_t + static_cast<int64_t>(hv / p.gv) * p.sv_h + ch]);
             const float ww = p.has_w ? __bfloat162float(p.w[t * p.sw_t + hv * p.sw_h + ch]) : 1.f;
             x2 = ww * vv;
         }
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(D) gdn2_simt_state_kernel(Params p) {
 
     if (p.status[0] != GDN2_OK) return;
     const int n = blockIdx.x, hv = blockIdx.y, v0 = blockIdx.z * VT, c = threadIdx.x;
-    const int h = hv / p.group;
+    const int h = hv / p.gk;  // key head
     float S[VT];
     const size_t sbase = ((static_cast<size_t>(n) * p.HV + hv) * D + c) * D + v0;
 #pragma unroll
@@ -232,14 +232,14 @@ __global__ void __launch_bounds__(kOutThreads) gdn2_simt_output_kernel(Params p)
     if (seq < 0) return;
     const int64_t start = p.chunk_start[c];
     const int len = p.chunk_len[c];
-    const int h = hv / p.group;
+    const int h = hv / p.gk, hq = hv / p.gq;  // key and query heads
 
     for (int i = tid; i < 64 * D; i += kOutThreads) {
         const int r = i / D, ch = i % D;
         const int64_t t = start + min(r, len - 1);
         Gs[r * LD + ch] = p.G[(t * p.HV + hv) * D + ch];
         Rs[r * LD + ch] = r < len ? __bfloat162float(p.k[t * p.sk_t + h * p.sk_h + ch]) : 0.f;
-        Qs[r * LD + ch] = r < len ? __bfloat162float(p.q[t * p.sq_t + h * p.sq_h + ch]) : 0.f;
+        Qs[r * LD + ch] = r < len ? __bfloat162float(p.q[t * p.sq_t + hq * p.sq_h + ch]) : 0.f;
     }
     for (int i = tid; i < 64 * 65; i += kOutThreads) Ps[i] = 0.f;
     __syncthreads();

@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         if (p.tmap) {
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bar_vw, 64u * D * 2 * (p.has_w ? 2u : 1u));
-                tile(raw_v, &p.tm_v, p.tm_order_v, nhv, &bar_vw);
+                tile(raw_v, &p.tm_v, p.tm_order_v, nhv / p.gv, &bar_vw);
                 if (p.has_w) tile(raw_w, &p.tm_w, p.tm_order_w, nhv, &bar_vw);
             }
             return;
@@ -356,7 +356,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         __syncwarp();
         for (uint32_t r = lane; r < rows; r += 32) {
             const int64_t tok = nstart + r;
-            bulk_g2s(raw_v + r * D * 2, p.v + tok * p.sv_t + static_cast<int64_t>(nhv) * p.sv_h, D * 2, &bar_vw);
+            bulk_g2s(raw_v + r * D * 2, p.v + tok * p.sv_t + static_cast<int64_t>(nhv / p.gv) * p.sv_h, D * 2,
+                     &bar_vw);
             if (p.has_w)
                 bulk_g2s(raw_w + r * D * 2, p.w + tok * p.sw_t + static_cast<int64_t>(nhv) * p.sw_h, D * 2, &bar_vw);
         }
@@ -367,11 +368,11 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         item = nitem;
         len = nlen;
         start = nstart;
-        h = hv / p.group;
+        h = hv / p.gk;  // key head; the query head is hv / gq
         live = t < len;
         const int64_t tok = nstart + (live ? t : 0);
         kp = p.k + tok * p.sk_t + static_cast<int64_t>(h) * p.sk_h;
-        qp = p.q + tok * p.sq_t + static_cast<int64_t>(h) * p.sq_h;
+        qp = p.q + tok * p.sq_t + static_cast<int64_t>(hv / p.gq) * p.sq_h;
         bp = p.beta + tok * p.sb_t + static_cast<int64_t>(hv) * p.sb_h;
     };
     // G' = G log2(e): every decay factor below is an exact power of two of a
@@ -767,9 +768,9 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     float *Yb = reinterpret_cast<float *>(sm + C::oY);
     if (!aux) named_sync(2, 128);
     if (has_next && p.tpre && warp == 6 && lane == 0) {  // next item's k, q, beta into L2
-        const int t0 = static_cast<int>(nstart), nh = nhv / p.group;
-        tma_prefetch_3d(&p.tm_k, 0, p.tm_order_k ? t0 : nh, p.tm_order_k ? nh : t0);
-        tma_prefetch_3d(&p.tm_q, 0, p.tm_order_q ? t0 : nh, p.tm_order_q ? nh : t0);
+        const int t0 = static_cast<int>(nstart), nk_h = nhv / p.gk, nq_h = nhv / p.gq;
+        tma_prefetch_3d(&p.tm_k, 0, p.tm_order_k ? t0 : nk_h, p.tm_order_k ? nk_h : t0);
+        tma_prefetch_3d(&p.tm_q, 0, p.tm_order_q ? t0 : nq_h, p.tm_order_q ? nq_h : t0);
         if (p.has_beta) tma_prefetch_3d(&p.tm_b, 0, p.tm_order_b ? t0 : nhv, p.tm_order_b ? nhv : t0);
     }
     if (tid < 64) {  // diagonal 16x16 blocks, one thread per (block, column)

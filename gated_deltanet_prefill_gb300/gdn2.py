@@ -50,7 +50,7 @@ class Dims(ctypes.Structure):
                 ("dtype_g", ctypes.c_int32), ("cu_seqlens_i64", ctypes.c_int32),
                 ("use_qk_l2norm", ctypes.c_int32), ("impl", ctypes.c_int32),
                 ("state_v_major", ctypes.c_int32), ("dtype_state", ctypes.c_int32),
-                ("state_segments", ctypes.c_int32)]
+                ("state_segments", ctypes.c_int32), ("HK", ctypes.c_int32)]
 
 
 _lib = None
@@ -137,6 +137,7 @@ def make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm=False, impl="t
     HV, V = v.shape[1], v.shape[2]
     d = Dims()
     d.T_tot, d.N, d.H, d.HV, d.K, d.V = T, cu_seqlens.numel() - 1, H, HV, K, V
+    d.HK = k.shape[1]
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("w", w), ("o", out)):
         s = _strides(t, name)
         getattr(d, name + "_stride")[0], getattr(d, name + "_stride")[1] = s
@@ -168,6 +169,12 @@ def workspace_bytes(dims: Dims) -> int:
     return int(load().gdn2_workspace_bytes(ctypes.byref(dims)))
 
 
+def state_heads(q, v) -> int:
+    """State (and output) heads: max(query heads, value heads) (the FlashInfer
+    docs' num_sab_heads)."""
+    return max(q.shape[1], v.shape[1])
+
+
 def _check_inputs(q, k, v, cu_seqlens, initial_state):
     """The checks every wrapper makes before marshalling: packed input with
     cu_seqlens, CUDA tensors, and a contiguous initial state (the C ABI takes
@@ -178,7 +185,7 @@ def _check_inputs(q, k, v, cu_seqlens, initial_state):
         if t is not None and not t.is_cuda:
             raise ValueError("%s must be a CUDA tensor" % name)
     if initial_state is not None and not initial_state.is_contiguous():
-        raise ValueError("initial_state must be contiguous [N, HV, K, V]")
+        raise ValueError("initial_state must be contiguous [N, HS, K, V]")
 
 
 def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state=None,
@@ -187,21 +194,24 @@ def chunk_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_state
                    state_v_major=False, state_dtype=None, state_segments=0):
     """GDN-2 chunked prefill forward through ``gdn2_chunk_fwd``.
 
-    Packed layout (FlashInfer docs, chunk_gated_delta_rule2): q, k [T, H, K];
-    v, w [T, HV, V]; g, beta [T, HV, K]; initial_state [N, HV, K, V] fp32;
-    cu_seqlens [N + 1] int32/int64.  Returns (out [T, HV, V] bf16,
-    final_state [N, HV, K, V] fp32 or None).
+    Packed layout (FlashInfer docs, chunk_gated_delta_rule2): q [T, H, K],
+    k [T, HK, K], v [T, HV, V] (HK equal to H or HV; H and HV equal or one a
+    multiple of the other); with HS = max(H, HV) state heads: w [T, HS, V],
+    g, beta [T, HS, K], initial_state [N, HS, K, V] fp32; cu_seqlens [N + 1]
+    int32/int64.  Returns (out [T, HS, V] at q's dtype, final_state
+    [N, HS, K, V] or None).
     """
     lib = load()
     _check_inputs(q, k, v, cu_seqlens, initial_state)
     T, H, K = q.shape
-    HV, V = v.shape[1], v.shape[2]
+    V = v.shape[2]
+    HS = state_heads(q, v)
     N = cu_seqlens.numel() - 1
     if out is None:
-        out = torch.empty((T, HV, V), dtype=q.dtype, device=q.device)
+        out = torch.empty((T, HS, V), dtype=q.dtype, device=q.device)
     sdt = _state_dtype(initial_state, final_state, state_dtype)
     if final_state is None and output_final_state:
-        final_state = torch.empty((N, HV, K, V), dtype=sdt, device=q.device)
+        final_state = torch.empty((N, HS, K, V), dtype=sdt, device=q.device)
     dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, impl, state_v_major, sdt)
     dims.state_segments = int(state_segments)  # 0: chosen by the library
     nbytes = workspace_bytes(dims)
@@ -234,13 +244,14 @@ def chunk_gdn2_fwd_noalloc(q, k, v, g=None, beta=None, w=None, scale=None, initi
     lib = load()
     _check_inputs(q, k, v, cu_seqlens, initial_state)
     T, H, K = q.shape
-    HV, V = v.shape[1], v.shape[2]
+    V = v.shape[2]
+    HS = state_heads(q, v)
     N = cu_seqlens.numel() - 1
     if out is None:
-        out = torch.empty((T, HV, V), dtype=q.dtype, device=q.device)
+        out = torch.empty((T, HS, V), dtype=q.dtype, device=q.device)
     sdt = _state_dtype(initial_state, final_state, state_dtype)
     if final_state is None and output_final_state:
-        final_state = torch.empty((N, HV, K, V), dtype=sdt, device=q.device)
+        final_state = torch.empty((N, HS, K, V), dtype=sdt, device=q.device)
     dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, impl, state_v_major, sdt)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
@@ -263,13 +274,14 @@ def recurrent_gdn2_fwd(q, k, v, g=None, beta=None, w=None, scale=None, initial_s
     lib = load()
     _check_inputs(q, k, v, cu_seqlens, initial_state)
     T, H, K = q.shape
-    HV, V = v.shape[1], v.shape[2]
+    V = v.shape[2]
+    HS = state_heads(q, v)
     N = cu_seqlens.numel() - 1
     if out is None:
-        out = torch.empty((T, HV, V), dtype=q.dtype, device=q.device)
+        out = torch.empty((T, HS, V), dtype=q.dtype, device=q.device)
     sdt = _state_dtype(initial_state, final_state, state_dtype)
     if final_state is None and output_final_state:
-        final_state = torch.empty((N, HV, K, V), dtype=sdt, device=q.device)
+        final_state = torch.empty((N, HS, K, V), dtype=sdt, device=q.device)
     dims = make_dims(q, k, v, g, beta, w, out, cu_seqlens, use_qk_l2norm, "tc", state_v_major, sdt)
     if workspace is None:
         workspace = torch.empty(256, dtype=torch.uint8, device=q.device)
@@ -317,7 +329,8 @@ class _SlicedRunner:
 
     def __init__(self, host, impl, use_qk_l2norm, output_final_state, slices):
         self.host, self.impl, self.l2, self.S = host, impl, use_qk_l2norm, slices
-        T, HV, V = host["v"].shape
+        T, _, V = host["v"].shape
+        HV = state_heads(host["q"], host["v"])  # output and state heads
         K = host["q"].shape[2]
         cu = [int(x) for x in host["cu_seqlens"].tolist()]
         self.N = N = len(cu) - 1
@@ -471,7 +484,8 @@ class HostRunner:
         self.l2 = use_qk_l2norm
         self.dev = {k: (torch.empty_like(v, device="cuda") if torch.is_tensor(v) else v)
                     for k, v in host.items()}
-        T, HV, V = host["v"].shape
+        T, _, V = host["v"].shape
+        HV = state_heads(host["q"], host["v"])  # output and state heads
         cu = [int(x) for x in host["cu_seqlens"].tolist()]
         N = len(cu) - 1
         K = host["q"].shape[2]

@@ -4,7 +4,7 @@
  *
  * The operation is the GDN-2 recurrence of the FlashInfer docs page
  * "flashinfer.gdn2_prefill.chunk_gated_delta_rule2" (op description), per
- * sequence n and value head hv, with key head h = hv / (HV / H):
+ * sequence n and state head hs (see gdn2_dims for the head counts):
  *
  *     S_t   = diag(exp(g_t)) S_{t-1}
  *     u_t   = w_t * v_t - (beta_t * k_t)^T S_t
@@ -87,13 +87,22 @@ typedef enum gdn2_impl {
  * to be contiguous").  Strides are in ELEMENTS of that tensor's dtype and,
  * like base pointers, must be multiples of 16 bytes.
  *
- *   q, k          [T_tot, H,  K]   dtype_qkv (bf16 or fp16)
- *   v, w          [T_tot, HV, V]   dtype_qkv
- *   g             [T_tot, HV, K]   dtype_g: fp32, bf16 or fp16 (natural-log decay, <= 0)
- *   beta          [T_tot, HV, K]   dtype_qkv (erase gate, post-sigmoid; [0, 2] allowed)
- *   out           [T_tot, HV, V]   dtype_qkv
- *   initial_state [N, HV, K, V]    dtype_state (fp32 or bf16), contiguous, K-major
- *                                  (row c = key channel); [N, HV, V, K] when
+ * Heads (FlashInfer docs, parameters q, k, v): H query heads, HK key heads
+ * (HK = 0 means H) and HV value heads, where HK equals H or HV and H, HV are
+ * equal or one a multiple of the other.  There is one state per STATE head
+ * hs < HS = max(H, HV) (the docs' num_sab_heads; also the output heads);
+ * state head hs reads query head hs / (HS / H), key head hs / (HS / HK) and
+ * value head hs / (HS / HV), contiguous groups of state heads sharing one.
+ *
+ *   q             [T_tot, H,  K]   dtype_qkv (bf16 or fp16)
+ *   k             [T_tot, HK, K]   dtype_qkv
+ *   v             [T_tot, HV, V]   dtype_qkv
+ *   w             [T_tot, HS, V]   dtype_qkv (write gate)
+ *   g             [T_tot, HS, K]   dtype_g: fp32, bf16 or fp16 (natural-log decay, <= 0)
+ *   beta          [T_tot, HS, K]   dtype_qkv (erase gate, post-sigmoid; [0, 2] allowed)
+ *   out           [T_tot, HS, V]   dtype_qkv
+ *   initial_state [N, HS, K, V]    dtype_state (fp32 or bf16), contiguous, K-major
+ *                                  (row c = key channel); [N, HS, V, K] when
  *                                  state_v_major = 1 (the FlashInfer docs' layout)
  *   final_state   same dtype and layout as initial_state
  *   cu_seqlens    [N + 1]          int32 (or int64 with cu_seqlens_i64 = 1)
@@ -103,7 +112,7 @@ typedef enum gdn2_impl {
  * SIMT implementation supports only the defaults (bf16, fp32 g, fp32 K-major
  * state); other combinations with impl = GDN2_IMPL_SIMT are GDN2_ERR_DTYPE.
  *
- * Supported sizes: K = V in {64, 128}; HV a positive multiple of H; N >= 0;
+ * Supported sizes: K = V in {64, 128}; the head counts above; N >= 0;
  * T_tot >= 0 (T_tot = 0 writes only final_state = initial_state).
  */
 typedef struct gdn2_dims {
@@ -117,9 +126,10 @@ typedef struct gdn2_dims {
     int32_t use_qk_l2norm;  /* 1: divide q, k rows by max(||x||_2, 1e-12) first   */
                             /* (FlashInfer docs: use_qk_l2norm_in_kernel)         */
     int32_t impl;           /* gdn2_impl                                          */
-    int32_t state_v_major;  /* 0: states [N, HV, K, V]; 1: [N, HV, V, K]          */
+    int32_t state_v_major;  /* 0: states [N, HS, K, V]; 1: [N, HS, V, K]          */
     int32_t dtype_state;    /* GDN2_DTYPE_F32 or GDN2_DTYPE_BF16                  */
     int32_t state_segments; /* chunk-parallel state pass; see below               */
+    int32_t HK;             /* key heads; 0 = H (the query heads)                 */
 } gdn2_dims;
 /*
  * state_segments (tensor-core path, K = V = 128): P > 1 splits each
@@ -148,8 +158,10 @@ GDN2_API size_t gdn2_workspace_bytes(const gdn2_dims *dims);
 
 /*
  * Fill `dims` for contiguous tensors of the given sizes (strides = packed
- * row-major), dtype_qkv = bf16, dtype_g = fp32, int32 cu_seqlens, no L2
- * norm, impl = GDN2_IMPL_TC, fp32 K-major states.  Host-only.
+ * row-major), key heads = query heads (HK = 0), dtype_qkv = bf16, dtype_g =
+ * fp32, int32 cu_seqlens, no L2 norm, impl = GDN2_IMPL_TC, fp32 K-major
+ * states.  H is the query (and key) head count, HV the value head count.
+ * Host-only.
  */
 GDN2_API gdn2_status gdn2_dims_init(gdn2_dims *dims, int64_t T_tot, int32_t N, int32_t H, int32_t HV,
                            int32_t K, int32_t V);

@@ -122,6 +122,35 @@ def test_check_args_errors(lib):
     assert _check(lib, d4, p) == 4
 
 
+def test_head_count_rules(lib):
+    """FlashInfer docs, parameters q/k/v: num_k_heads equals num_q_heads or
+    num_v_heads, and the query and value head counts are equal or one a
+    multiple of the other; states, gates and output are per state head,
+    max(H, HV)."""
+    def dims(H, HV, HK=0):
+        d = gdn2.Dims()
+        st = lib.gdn2_dims_init(ctypes.byref(d), 256, 2, H, HV, 64, 64)
+        d.HK = HK
+        return st, d
+
+    ok = [(4, 2, 0), (4, 2, 2), (4, 2, 4), (2, 4, 0), (2, 4, 4), (3, 6, 6), (6, 3, 3), (1, 8, 8), (8, 1, 1)]
+    for H, HV, HK in ok:
+        st, d = dims(H, HV, HK)
+        assert st == 0
+        p = _ptrs(d, 0)
+        assert _check(lib, d, p, ws_bytes=1 << 30) == 0, (H, HV, HK)
+    for H, HV, HK in ((4, 2, 3), (4, 2, 1), (2, 4, 1), (4, 6, 0), (2, 3, 2)):
+        _, d = dims(H, HV, HK)
+        assert _check(lib, d, _ptrs(d, 0), ws_bytes=1 << 30) == 2, (H, HV, HK)
+    # per-state-head tensors are laid out with HS = max(H, HV) heads
+    st, d = dims(4, 2)
+    assert d.v_stride[0] == 2 * 64 and d.w_stride[0] == 4 * 64 and d.o_stride[0] == 4 * 64
+    assert d.g_stride[0] == 4 * 64 and d.beta_stride[0] == 4 * 64 and d.q_stride[0] == 4 * 64
+    # the workspace follows the state heads, not the value heads
+    _, d44 = dims(4, 4)
+    assert lib.gdn2_workspace_bytes(ctypes.byref(d)) == lib.gdn2_workspace_bytes(ctypes.byref(d44))
+
+
 def test_chunk_fwd_rejects_before_launch(lib):
     """gdn2_chunk_fwd returns the argument error without any CUDA call."""
     d = _dims(lib)
