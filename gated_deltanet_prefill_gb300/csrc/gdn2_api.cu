@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
 #include <math.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -294,7 +295,63 @@ bool device_is_sm103(int *dev_out) {
 
 }  // namespace gdn2
 
+namespace gdn2 {
+namespace {
+
+// The state-pass V tile the call uses: two 64-column tiles per (sequence,
+// head) when the untiled grid would leave more than half of the SMs idle.
+int state_vtile(const gdn2_dims &d, int P, int sms) {
+    return d.K == 128 && 2ll * d.N * dims_hs(d) * P <= sms ? 64 : d.K;
+}
+
+// The launch sequence of one call as text (what each launch runs and its grid).
+int describe_plan(const gdn2_dims &d, int sms, char *buf, size_t len) {
+    char tmp[1024];
+    const int HS = dims_hs(d);
+    const long long NCmax = nc_max(d), items = NCmax * HS;
+    int n = snprintf(tmp, sizeof(tmp), "N=%d T_tot=%lld H=%d HK=%d HV=%d (state heads %d) K=V=%d; workspace %zu B; ",
+                     d.N, static_cast<long long>(d.T_tot), d.H, dims_hk(d), d.HV, HS, d.K, workspace_layout(d).total);
+    auto add = [&](const char *fmt, auto... a) {
+        if (n >= 0 && static_cast<size_t>(n) < sizeof(tmp)) n += snprintf(tmp + n, sizeof(tmp) - n, fmt, a...);
+    };
+    add("chunk_map 1x1024");
+    if (d.N > 0 && d.impl == GDN2_IMPL_SIMT) {
+        if (d.use_qk_l2norm && d.T_tot > 0) add("; l2norm %lld warps", static_cast<long long>(d.T_tot) * (d.H + dims_hk(d)));
+        add("; cumsum %lldx%d; simt_intra %lldx%d x256; simt_state %dx%dx%d x%d; simt_output %lldx%d x256",
+            NCmax, HS, NCmax, HS, d.N, HS, d.K / 32, d.K, NCmax, HS);
+    } else if (d.N > 0) {
+        const long long grid = items < 2ll * sms ? items : 2ll * sms;
+        add("; intra first pass %lld x256 (persistent, 2 CTAs/SM)", grid);
+        add("; intra exact pass %lld x256 (programmatic dependent; only with g; runs the listed items)", grid);
+        const int P = scan_segments(d);
+        const int vt = state_vtile(d, P, sms);
+        if (d.K == 64) {
+            add("; state_output gdn2_tc_state_kernel<64> %dx%d", d.N, HS);
+        } else if (P > 1) {
+            add("; chunk-parallel state pass, %d segments: transitions %lld CTAs of 128 columns; combine %dx%dx8; "
+                "replay %lld CTAs of %d columns", P, 2ll * d.N * (P - 1) * HS, d.N, HS, 1ll * d.N * P * HS * (128 / vt), vt);
+        } else {
+            add("; state_output %s %lld CTAs of %d columns", vt == 64 ? "gdn2_tc_state_la_kernel" : "gdn2_tc_state_la128_kernel",
+                1ll * d.N * HS * (128 / vt), vt);
+        }
+    }
+    if (buf && len > 0) {
+        const size_t m = static_cast<size_t>(n) < len - 1 ? static_cast<size_t>(n) : len - 1;
+        memcpy(buf, tmp, m);
+        buf[m] = 0;
+    }
+    return n;
+}
+
+}  // namespace
+}  // namespace gdn2
+
 extern "C" {
+
+int32_t gdn2_launch_plan(const gdn2_dims *d, int32_t sm_count, char *buf, size_t len) {
+    if (!d || !shape_ok(*d)) return 0;
+    return describe_plan(*d, sm_count > 0 ? sm_count : 152, buf, len);
+}
 
 gdn2_status gdn2_check_args(const void *q, const void *k, const void *v, const void *g, const void *beta,
                             const void *w, const void *initial_state, const void *cu_seqlens,
@@ -372,12 +429,17 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     p.sc_mode = 0;
     p.sc_tr = p.sc_P > 1 ? reinterpret_cast<float *>(ws + L.sc_tr) : nullptr;
     p.sc_si = p.sc_P > 1 ? reinterpret_cast<float *>(ws + L.sc_si) : nullptr;
-    p.vtile = d->K;
-    if (d->K == 128) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-            2ll * d->N * HS * p.sc_P <= sms)
-            p.vtile = 64;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        sms = 0;
+    }
+    p.vtile = sms > 0 ? state_vtile(*d, p.sc_P, sms) : d->K;
+    const char *log = getenv("GDN2_LOG");
+    if (log && log[0] == '1') {  // the launch plan on stderr (diagnostics)
+        char plan[1024];
+        describe_plan(*d, sms > 0 ? sms : 152, plan, sizeof(plan));
+        fprintf(stderr, "gdn2: %s\n", plan);
     }
     // tensor maps for the intra kernel's g / v / w tiles (GDN2_ROW_COPIES=1
     // forces the row-by-row copies)

@@ -979,11 +979,12 @@ cudaError_t launch_intra_pass(const Params &p, cudaStream_t s) {
 }
 
 // Both passes: every item, then the exact pass over the items the first one
-// listed (its CTAs return at once when the list is empty).
+// listed (its CTAs return at once when the list is empty).  Without g there
+// is no decay, so no item can be listed and the exact pass is not launched.
 template <int D, bool F16>
 cudaError_t launch_intra(const Params &p, cudaStream_t s) {
     const cudaError_t e = launch_intra_pass<D, F16, false>(p, s);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || !p.has_g) return e;
     return launch_intra_pass<D, F16, true>(p, s);
 }
 

@@ -28,6 +28,7 @@ _DTYPE_CODE = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16, torch.float
 
 EXPORTS = ("gdn2_workspace_bytes", "gdn2_dims_init", "gdn2_check_args", "gdn2_chunk_fwd",
            "gdn2_chunk_fwd_staged", "gdn2_num_stages", "gdn2_stage_name", "gdn2_launch_count",
+           "gdn2_launch_plan",
            "gdn2_device_status", "gdn2_chunk_fwd_noalloc", "gdn2_noalloc_device_status",
            "gdn2_recurrent_workspace_bytes",
            "gdn2_recurrent_fwd", "gdn2_selftest_wait_timeout", "gdn2_status_string", "gdn2_version")
@@ -89,6 +90,8 @@ def load(path: Optional[str] = None):
     lib.gdn2_stage_name.restype = ctypes.c_char_p
     lib.gdn2_launch_count.argtypes = [ctypes.POINTER(Dims)]
     lib.gdn2_launch_count.restype = i32
+    lib.gdn2_launch_plan.argtypes = [ctypes.POINTER(Dims), i32, ctypes.c_char_p, sz]
+    lib.gdn2_launch_plan.restype = i32
     lib.gdn2_chunk_fwd_noalloc.argtypes = [vp] * 6 + [ctypes.c_float, vp, vp, vp, vp,
                                                       ctypes.POINTER(Dims), vp]
     lib.gdn2_chunk_fwd_noalloc.restype = ctypes.c_int
@@ -447,6 +450,15 @@ def stage_names(dims: Dims):
     lib = load()
     return [lib.gdn2_stage_name(ctypes.byref(dims), i).decode()
             for i in range(lib.gdn2_num_stages(ctypes.byref(dims)))]
+
+
+def launch_plan(dims: Dims, sm_count: int = 0) -> str:
+    """The launch sequence of one call for ``dims`` as text (host only)."""
+    lib = load()
+    n = lib.gdn2_launch_plan(ctypes.byref(dims), sm_count, None, 0)
+    buf = ctypes.create_string_buffer(n + 1)
+    lib.gdn2_launch_plan(ctypes.byref(dims), sm_count, buf, n + 1)
+    return buf.value.decode()
 
 
 def launch_count(dims: Dims) -> int:

@@ -245,9 +245,21 @@ GDN2_API int32_t gdn2_num_stages(const gdn2_dims *dims);
  * Host-only. */
 GDN2_API const char *gdn2_stage_name(const gdn2_dims *dims, int32_t i);
 
-/* Number of kernel launches one gdn2_chunk_fwd call makes for `dims`
- * (0 if invalid).  Host-only. */
+/* Number of kernel launches one gdn2_chunk_fwd call makes for `dims` when g
+ * is given (0 if invalid); without g the tensor-core path makes one fewer
+ * (no exact pass of the intra kernel).  Host-only. */
 GDN2_API int32_t gdn2_launch_count(const gdn2_dims *dims);
+
+/*
+ * The launch sequence gdn2_chunk_fwd runs for `dims` on a GPU with
+ * `sm_count` SMs (<= 0: 152, a GB300), as one line of text: each launch,
+ * its grid, the state-pass tile width and segments, the workspace size.
+ * Writes at most `len` bytes including the terminating NUL into `buf` (buf
+ * may be NULL with len 0) and returns the full length, as snprintf does; 0
+ * if dims is NULL or invalid.  Host-only.  With the environment variable
+ * GDN2_LOG=1, gdn2_chunk_fwd prints the same line to stderr at each call.
+ */
+GDN2_API int32_t gdn2_launch_plan(const gdn2_dims *dims, int32_t sm_count, char *buf, size_t len);
 
 /*
  * Workspace bytes of gdn2_recurrent_fwd for `dims` (a 64-byte status area; 0

@@ -151,6 +151,34 @@ def test_head_count_rules(lib):
     assert lib.gdn2_workspace_bytes(ctypes.byref(d)) == lib.gdn2_workspace_bytes(ctypes.byref(d44))
 
 
+def test_launch_plan(lib):
+    """The host-side description of the launch sequence (also printed with
+    GDN2_LOG=1) names the kernels and grids each shape gets."""
+    def plan(T, N, H, HV, K, impl=0, segments=0, sms=152):
+        d = gdn2.Dims()
+        assert lib.gdn2_dims_init(ctypes.byref(d), T, N, H, HV, K, K) == 0
+        d.impl, d.state_segments = impl, segments
+        return gdn2.launch_plan(d, sms)
+
+    long5 = plan(4 * 32768, 4, 32, 32, 128)
+    assert "intra first pass 304 x256" in long5 and "gdn2_tc_state_la128_kernel 128 CTAs of 128 columns" in long5
+    few = plan(16384 * 2, 2, 16, 32, 128)
+    assert "gdn2_tc_state_la_kernel 128 CTAs of 64 columns" in few
+    seg = plan(4096, 1, 16, 16, 128)
+    assert "chunk-parallel state pass, 4 segments" in seg
+    assert "simt_intra" in plan(256, 1, 2, 2, 64, impl=1)
+    assert "state_kernel<64>" in plan(256, 1, 2, 2, 64)
+    d = gdn2.Dims()
+    assert lib.gdn2_dims_init(ctypes.byref(d), 256, 1, 2, 3, 64, 64) != 0
+    assert lib.gdn2_launch_plan(ctypes.byref(d), 152, None, 0) == 0
+    small = ctypes.create_string_buffer(8)
+    assert lib.gdn2_launch_plan(ctypes.byref(gdn2.Dims()), 0, None, 0) == 0
+    d = gdn2.Dims()
+    lib.gdn2_dims_init(ctypes.byref(d), 256, 1, 2, 2, 64, 64)
+    n = lib.gdn2_launch_plan(ctypes.byref(d), 0, small, 8)
+    assert n > 8 and len(small.value) == 7  # truncated like snprintf
+
+
 def test_chunk_fwd_rejects_before_launch(lib):
     """gdn2_chunk_fwd returns the argument error without any CUDA call."""
     d = _dims(lib)
