@@ -18,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgdn2.so")
+# the checked build: the same sources with the device-side index checks on
+# (-DGDN2_CHECK_BOUNDS); built on request only (tests), never the product path
+LIB_CHECKED = os.path.join(BUILD, "libgdn2_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
@@ -33,20 +36,26 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib=LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     return any(os.path.getmtime(f) > t for f in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    """Build libgdn2.so (or, with checked=True, libgdn2_checked.so: the
+    device-side index checks compiled in) and return its path."""
+    lib = LIB_CHECKED if checked else LIB
+    if not force and not _stale(lib):
+        return lib
+    odir = os.path.join(BUILD, "checked") if checked else BUILD
+    os.makedirs(odir, exist_ok=True)
+    if checked:
+        extra_flags = tuple(extra_flags) + ("-DGDN2_CHECK_BOUNDS",)
     srcs = sources()
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(odir, os.path.basename(s)[:-3] + ".o") for s in srcs]
 
     def compile_one(pair):
         src, obj = pair
@@ -60,14 +69,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         list(ex.map(compile_one, zip(srcs, objs)))
-    tmp = LIB + ".%d.tmp" % os.getpid()
+    tmp = lib + ".%d.tmp" % os.getpid()
     cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         print(" ".join(cmd)); print(r.stdout + r.stderr)
         raise RuntimeError("link failed")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -189,6 +189,7 @@ const char *gdn2_status_string(int status) {
         case GDN2_ERR_TIMEOUT: return "a tensor-core kernel timed out waiting on its own pipeline (outputs invalid)";
         case GDN2_ERR_NOALLOC_LIMIT: return "problem needs more scratch than the allocation-free entry point holds (GDN2_NOALLOC_SCRATCH_BYTES)";
         case GDN2_ERR_RANGE: return "a value passed the range of the fp16 intermediates and was clipped (outputs invalid)";
+        case GDN2_ERR_BOUNDS: return "an index check of the checked build failed (outputs invalid; a library defect)";
         default: return "unknown status";
     }
 }
@@ -561,14 +562,19 @@ gdn2_status gdn2_device_status(const void *workspace, void *stream, int32_t *sta
     if (!workspace || !status) return GDN2_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // the status words sit at offset 0 of the workspace: [0] cu_seqlens,
-    // [1] chunk count, [2] wait timeout, [3] 16-bit range
-    int32_t host[4] = {0, 0, 0, 0};
+    // [1] chunk count, [2] wait timeout, [3] 16-bit range, [4] exact-list
+    // length, [5] failed index check (checked builds)
+    int32_t host[6] = {0, 0, 0, 0, 0, 0};
     if (cudaMemcpyAsync(host, workspace, sizeof(host), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
         return GDN2_ERR_CUDA;
     }
-    *status = host[0] != GDN2_OK ? host[0] : host[2] != GDN2_OK ? host[2] : host[3];
+    *status = host[0] != GDN2_OK   ? host[0]
+              : host[2] != GDN2_OK ? host[2]
+              : host[3] != GDN2_OK ? host[3]
+              : host[5] != 0       ? static_cast<int32_t>(GDN2_ERR_BOUNDS)
+                                   : static_cast<int32_t>(GDN2_OK);
     return GDN2_OK;
 }
 

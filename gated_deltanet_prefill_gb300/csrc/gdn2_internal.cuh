@@ -49,7 +49,8 @@ struct Params {
     int NCmax;                  // upper bound on the chunk count: T_tot/64 + N
     // ---- workspace ----
     int *status;                // [0] cu_seqlens status, [1] chunk count NC, [2] wait timeout,
-                                // [3] 16-bit range, [4] length of exact_list
+                                // [3] 16-bit range, [4] length of exact_list,
+                                // [5] first failed index check (checked builds)
     int *chunk_seq;             // [NCmax]  sequence of chunk c, -1 past NC
     int *chunk_len;             // [NCmax]  tokens in chunk c (1..64)
     int64_t *chunk_start;       // [NCmax]  first token of chunk c
@@ -137,6 +138,25 @@ __device__ __forceinline__ void state_st(void *base, size_t i, float x, bool is_
         static_cast<bf16 *>(base)[i] = __float2bfloat16_rn(x);
     else
         static_cast<float *>(base)[i] = x;
+}
+
+// Checked builds (compiled with -DGDN2_CHECK_BOUNDS, build.py's checked
+// library): device-side index checks.  An index outside [lo, hi) is recorded
+// in status word 5 (the site of the first failure) and clamped into range, so
+// the access it guards stays inside its buffer and the control flow is that
+// of the normal build; gdn2_device_status then reports GDN2_ERR_BOUNDS.
+// Normal builds compile the checks away.
+template <typename T>
+__device__ __forceinline__ T chk(T x, T lo, T hi, int site, int *status) {
+#ifdef GDN2_CHECK_BOUNDS
+    if (x < lo || x >= hi) {
+        atomicCAS(status + 5, 0, site);
+        return x < lo ? lo : hi - 1;
+    }
+#else
+    (void)lo; (void)hi; (void)site; (void)status;
+#endif
+    return x;
 }
 
 // Status word 3 of the workspace: a kernel converted a value past the range of

@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(kMapThreads) gdn2_chunk_map_kernel(Params p) {
         p.status[2] = GDN2_OK;
         p.status[3] = GDN2_OK;
         p.status[4] = 0;
+        p.status[5] = 0;
     }
     __syncthreads();
     for (int n = tid; n < p.N; n += kMapThreads)

@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(256) gdn2_recurrent_check_kernel(RecParams p) 
         p.status[1] = 0;
         p.status[2] = 0;
         p.status[3] = 0;
+        p.status[5] = 0;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < p.N; i += blockDim.x)

@@ -21,6 +21,7 @@ __global__ void gdn2_wait_selftest_kernel(int *status, uint64_t limit_ns) {
         status[1] = 0;
         status[2] = GDN2_OK;
         status[3] = GDN2_OK;
+        status[5] = 0;
     }
     __syncthreads();
     if (threadIdx.x == 0 && !tc::mbar_wait_ns(&bar, 0, limit_ns))

@@ -307,11 +307,11 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     uint4 nk = z4, nq = z4, nb = z4;
     int nitem = 0;  // item index c * HV + hv of the staged item
     auto meta = [&](int it) {
-        nitem = EXACT ? p.exact_list[it] : it;
+        nitem = chk(EXACT ? p.exact_list[it] : it, 0, p.status[1] * p.HV, 101, p.status);
         nc = nitem / p.HV;
         nhv = nitem - nc * p.HV;
-        nstart = p.chunk_start[nc];
-        nlen = p.chunk_len[nc];
+        nlen = chk(p.chunk_len[nc], 1, kChunk + 1, 102, p.status);
+        nstart = chk(p.chunk_start[nc], int64_t(0), p.T_tot - nlen + 1, 103, p.status);
     };
     float *Gs = reinterpret_cast<float *>(sm + C::oG);
     uint8_t *raw_v = sm + C::oBWU;
@@ -498,7 +498,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     // this item: its diagonal blocks take the exact path (CTA-uniform)
     const bool exact = *exact_flag != 0u;
     const uint32_t hmax_in = hmax;
-    if (!EXACT && exact && tid == 0) p.exact_list[atomicAdd(p.status + 4, 1)] = item;
+    if (!EXACT && exact && tid == 0)
+        p.exact_list[chk(atomicAdd(p.status + 4, 1), 0, p.NCmax * p.HV, 104, p.status)] = item;
     if (EXACT && exact) exact_diag_sums<D, F16>(p, Gs, gE, ks_row, rec, kp, qp, bp, start, h, t, seg, live);
 
     // ---- 1. cumsum (g is in the G scratch) ----------------------------------------

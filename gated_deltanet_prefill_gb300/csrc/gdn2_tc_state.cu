@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
     const int tile = blockIdx.x % tiles;
     const int hv = (blockIdx.x / tiles) % p.HV;
     const int rs = blockIdx.x / (tiles * p.HV);
-    const int seg = rs % segs, n = p.seq_order[rs / segs];
+    const int seg = rs % segs, n = chk(p.seq_order[rs / segs], 0, p.N, 201, p.status);
     const bool trans = mode == 1;
     const int col0 = tile * VT;                     // first column of this tile
     const bool is_m = trans && col0 < D;            // a tile of M
@@ -141,7 +141,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
                     ok = false;
                     break;
                 }
-                const uint8_t *rec = p.rec + (static_cast<size_t>(first + i) * p.HV + hv) * Rec<D>::bytes;
+                const uint8_t *rec =
+                    p.rec + (static_cast<size_t>(chk(first + i, 0, p.status[1], 202, p.status)) * p.HV + hv) *
+                                Rec<D>::bytes;
                 uint8_t *st = sm + s * C::kStage;
                 mbar_arrive_expect_tx(&full_bar[s], C::kLoadBytes);
                 bulk_g2s(st + C::sP, rec + Rec<D>::P, Rec<D>::mma_prefix, &full_bar[s]);

@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
     // one CTA per (sequence in longest-first order, value head, 64-column tile)
     const int tile = blockIdx.x % 2;
     const int hv = (blockIdx.x / 2) % p.HV;
-    const int n = p.seq_order[blockIdx.x / (2 * p.HV)];
+    const int n = chk(p.seq_order[blockIdx.x / (2 * p.HV)], 0, p.N, 301, p.status);
     const int v0 = tile * VT;
     const int first = p.seq_first[n], nck = p.seq_first[n + 1] - first;
 
@@ -128,7 +128,9 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
                     ok = false;
                     break;
                 }
-                const uint8_t *rec = p.rec + (static_cast<size_t>(first + i) * p.HV + hv) * Rec<D>::bytes;
+                const uint8_t *rec =
+                    p.rec + (static_cast<size_t>(chk(first + i, 0, p.status[1], 302, p.status)) * p.HV + hv) *
+                                Rec<D>::bytes;
                 mbar_arrive_expect_tx(&full_bar[s], C::kLoadBytes);
                 bulk_g2s(stage(i) + C::sP, rec + Rec<D>::P, Rec<D>::mma_prefix, &full_bar[s]);
                 bulk_g2s(stage(i) + C::sUt, rec + Rec<D>::Ut + tile * 8192, 8192, &full_bar[s]);
@@ -470,7 +472,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // one CTA per (sequence in longest-first order, value head)
     const int hv = blockIdx.x % p.HV;
-    const int n = p.seq_order[blockIdx.x / p.HV];
+    const int n = chk(p.seq_order[blockIdx.x / p.HV], 0, p.N, 401, p.status);
     const int first = p.seq_first[n], nck = p.seq_first[n + 1] - first;
 
     if (threadIdx.x == 0) {
@@ -504,7 +506,8 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
     auto stage = [&](int c) { return sm + (c % NSTAGE) * C::kStage; };
     auto ubuf = [&](int c) { return sm + C::oU + (c & 1) * C::kUBytes; };
     auto rec_of = [&](int c) {
-        return p.rec + (static_cast<size_t>(first + c) * p.HV + hv) * Rec<D>::bytes;
+        return p.rec + (static_cast<size_t>(chk(first + c, 0, p.status[1], 402, p.status)) * p.HV + hv) *
+                           Rec<D>::bytes;
     };
 
     if (warp == 0) {

@@ -20,7 +20,7 @@ GDN2_OK = 0
 STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_STRIDE", 4: "ERR_ALIAS",
                 5: "ERR_WORKSPACE", 6: "ERR_ARCH", 7: "ERR_LAUNCH", 8: "ERR_DTYPE",
                 9: "ERR_CU_SEQLENS", 10: "ERR_CUDA", 11: "ERR_IMPL", 12: "ERR_TIMEOUT",
-                13: "ERR_NOALLOC_LIMIT", 14: "ERR_RANGE"}
+                13: "ERR_NOALLOC_LIMIT", 14: "ERR_RANGE", 15: "ERR_BOUNDS"}
 NOALLOC_SCRATCH_BYTES = 64 << 20
 IMPL = {"tc": 0, "simt": 1}
 DTYPE_BF16, DTYPE_F16, DTYPE_F32 = 0, 1, 2

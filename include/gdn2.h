@@ -63,9 +63,12 @@ typedef enum gdn2_status {
                               /* own pipeline barriers (see gdn2_device_status)       */
     GDN2_ERR_NOALLOC_LIMIT = 13, /* the problem needs more scratch than               */
                               /* gdn2_chunk_fwd_noalloc holds                         */
-    GDN2_ERR_RANGE = 14       /* device-side: a value passed the range of the fp16    */
+    GDN2_ERR_RANGE = 14,      /* device-side: a value passed the range of the fp16    */
                               /* intermediates and was clipped; outputs are invalid   */
                               /* (see gdn2_device_status)                             */
+    GDN2_ERR_BOUNDS = 15      /* device-side, checked builds only (compiled with      */
+                              /* GDN2_CHECK_BOUNDS): an index left its buffer; a      */
+                              /* library defect, outputs invalid                      */
 } gdn2_status;
 
 typedef enum gdn2_dtype {
@@ -296,9 +299,10 @@ GDN2_API gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void
  * Read the device-side status that the last gdn2_chunk_fwd or
  * gdn2_recurrent_fwd on this workspace wrote into *status: GDN2_OK,
  * GDN2_ERR_CU_SEQLENS, GDN2_ERR_TIMEOUT (a tensor-core kernel waited more
- * than 2 s on one of its own barriers and unwound), or GDN2_ERR_RANGE (an
- * fp16 intermediate was clipped); with any of the last two the outputs are
- * invalid.  If several apply, the first in that order is reported.  This call
+ * than 2 s on one of its own barriers and unwound), GDN2_ERR_RANGE (an fp16
+ * intermediate was clipped) or, in a checked build only, GDN2_ERR_BOUNDS (an
+ * index check failed); with any of the last three the outputs are invalid.
+ * If several apply, the first in that order is reported.  This call
  * SYNCHRONISES `stream`.  Returns GDN2_ERR_CUDA if the copy fails.
  */
 GDN2_API gdn2_status gdn2_device_status(const void *workspace, void *stream, int32_t *status);

@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_version_and_strings(lib):
     assert lib.gdn2_version() >> 16 == 1
-    for code in range(15):  # GDN2_OK .. GDN2_ERR_RANGE
+    for code in range(16):  # GDN2_OK .. GDN2_ERR_BOUNDS
         s = lib.gdn2_status_string(code).decode()
         assert s and s != "unknown status"
         assert code in gdn2.STATUS_NAMES
