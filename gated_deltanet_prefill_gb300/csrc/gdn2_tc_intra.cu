@@ -1,7 +1,7 @@
 // Tensor-core intra-chunk kernel: everything of a 64-token chunk that does
 // not depend on the incoming state, written as the record the state kernel
 // consumes (gdn2_record.cuh).  Persistent: two CTAs of 256 threads per SM walk
-// the (chunk, value head) items.  While an item is being processed the next
+// the (chunk, state head) items.  While an item is being processed the next
 // one is prepared: its g, v, w tiles arrive by TMA (tensor maps built on the
 // host, row copies when a layout cannot be mapped), its k, q, beta tiles are
 // prefetched into L2, and the four warps idle in the W/U epilogue compute its
@@ -10,7 +10,7 @@
 // Steps (FlashRT gated-delta-attention page: norm/cumsum, kkt, solve_tril,
 // recompute_wu; fused into one kernel here, with GDN-2's channel-wise gates):
 //  1. G = chunk-local inclusive cumsum of g (log2-scaled, in shared memory);
-//     k, q (key head), beta (value head) read per thread one channel chunk
+//     k, q (key and query heads), beta (state head) read per thread one channel chunk
 //     ahead; optional q/k L2 norm; w v formed from the staged v, w tiles.
 //  2. decay factors through 16-token sub-chunk references (burn-gdn2 README,
 //     "Numerical stability"): with B_I the row before sub-chunk I and E_J the
@@ -249,7 +249,7 @@ __device__ __noinline__ void exact_diag_apply(float *Af, uint8_t *rec, int tid) 
 
 // F16: q, k, v, beta, w are fp16 (else bf16); a template parameter so that the
 // operand-image loop carries no dtype branch.  EXACT = false: the pass over
-// every (chunk, value head) item; an item with a wide-decay channel gets its
+// every (chunk, state head) item; an item with a wide-decay channel gets its
 // record without that channel's diagonal terms and is appended to the exact
 // list.  EXACT = true: the second launch, over the listed items only, with the
 // exact path; it rewrites their records.  Two instantiations keep the exact
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     // first pass has completed and its exact list is visible.
     if (EXACT) asm volatile("griddepcontrol.wait;" ::: "memory");
     else asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // (chunk, value head) items: all of them, or the exact list
+    // (chunk, state head) items: all of them, or the exact list
     const int total = p.status[0] != GDN2_OK ? 0 : EXACT ? p.status[4] : p.status[1] * p.HV;
     if (static_cast<int>(blockIdx.x) >= total) return;  // before any barrier or TMEM allocation
 
@@ -534,8 +534,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         qscale = 1.f / fmaxf(sqrtf(sq), 1e-12f);
     }
     // G' prefix sums and tables are ready (computed during the previous item's
-    // W/U epilogue, or before the loop).
-    // raw v and w are in the B operand area
+    // W/U epilogue, or before the loop); raw v and w are in the B operand area
     if (!mbar_wait(&bar_vw, vph)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
     vph ^= 1u;
     // w v for this thread's chunks, stored to its operand image after the
