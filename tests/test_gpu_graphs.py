@@ -86,3 +86,28 @@ def test_decode_step_in_a_graph(cuda_lib):
     wl = inputs.small("graphdec", [1] * 16, H=2, HV=4, K=128, V=128, g_max=0.5, beta_max=2.0, h0_std=0.05,
                       seed=88)
     replay_and_check(*captured(cuda_lib.recurrent_gdn2_fwd, wl), wl, seeds=(89, 90, 91))
+
+
+def test_exact_pass_in_a_graph(cuda_lib):
+    """The intra kernel's exact pass (a programmatic dependent launch) inside a
+    graph: captured on slow decays (an empty exact list), then replayed with
+    decays of up to 30 nats per token (most items listed) and slow ones again.
+    The list is rebuilt on the device at every replay."""
+    wl = inputs.small("graphwide", [130, 64, 1, 200], H=2, HV=4, K=128, V=128, g_max=0.5, beta_max=2.0,
+                      h0_std=0.05, seed=92)
+    graph, st, out, fs = captured(cuda_lib.chunk_gdn2_fwd, wl)
+    for seed, wide in ((93, True), (94, False), (95, True)):
+        d = inputs.generate(inputs.with_seed(wl, seed))
+        if wide:
+            gen = torch.Generator().manual_seed(seed)
+            d["g"] = torch.rand(d["g"].shape, generator=gen).mul_(-30.0)
+        for k in KEYS:
+            if torch.is_tensor(d[k]):
+                st[k].copy_(d[k])
+        graph.replay()
+        torch.cuda.synchronize()
+        o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                                           initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
+        eo = rel_max(out.float().cpu().numpy(), o_ref)
+        eh = rel_max(fs.cpu().numpy(), h_ref)
+        assert eo <= TOL and eh <= TOL, "seed %d (wide %s): o err %.3e, state err %.3e" % (seed, wide, eo, eh)

@@ -88,3 +88,20 @@ def test_head_counts_recurrent(cuda_lib, heads):
     d = problem(H, HK, HV, 128, [1, 20, 33], seed=74)
     eo, eh = run(cuda_lib, d, fn="recurrent")
     assert eo <= TOL and eh <= TOL, (heads, eo, eh)
+
+
+def test_head_counts_host_runner(cuda_lib):
+    """HostRunner (pinned host buffers, pieces pipelined over three streams)
+    with more query than value heads and fewer key heads: outputs and states
+    are allocated per state head and match the oracle."""
+    d = problem(4, 2, 2, 128, [100, 1, 0, 257, 64], seed=75)
+    host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in d.items()}
+    o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                                       initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
+    for slices in (0, 4):
+        runner = cuda_lib.HostRunner(host, groups=2, slices=slices)
+        o, hT = runner()
+        torch.cuda.synchronize()
+        assert o.shape == o_ref.shape and hT.shape == h_ref.shape
+        assert rel_max(o.float().numpy(), o_ref) <= TOL, slices
+        assert rel_max(hT.float().numpy(), h_ref) <= TOL, slices
