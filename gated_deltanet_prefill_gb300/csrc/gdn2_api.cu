@@ -315,7 +315,7 @@ int describe_plan(const gdn2_dims &d, int sms, char *buf, size_t len) {
     auto add = [&](const char *fmt, auto... a) {
         if (n >= 0 && static_cast<size_t>(n) < sizeof(tmp)) n += snprintf(tmp + n, sizeof(tmp) - n, fmt, a...);
     };
-    add("chunk_map 1x1024");
+    add("%s", "chunk_map 1x1024");
     if (d.N > 0 && d.impl == GDN2_IMPL_SIMT) {
         if (d.use_qk_l2norm && d.T_tot > 0) add("; l2norm %lld warps", static_cast<long long>(d.T_tot) * (d.H + dims_hk(d)));
         add("; cumsum %lldx%d; simt_intra %lldx%d x256; simt_state %dx%dx%d x%d; simt_output %lldx%d x256",

@@ -140,6 +140,13 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t 
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Close the thread's pending cp.async copies into a group; wait until at
+// most N of its groups are still in flight.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Named barrier `id` (1..15) over `nthreads` threads of the block (a
 // multiple of 32, whole warps); id 0 is __syncthreads.

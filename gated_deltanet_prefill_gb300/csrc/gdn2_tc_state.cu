@@ -440,53 +440,96 @@ cudaError_t launch_state(const Params &p, cudaStream_t s) {
 // S_in(s + 1) = M_s S_in(s) + B_s for s = 0 .. P - 2, S_in(0) = the initial
 // state (or 0), into sc_si.  One CTA per (sequence, value head, CW value
 // columns); fp32 on CUDA cores, the running 128 x CW tile in shared memory.
-// CW = 16: the chain of P - 1 dependent steps is latency-bound, so narrower
-// tiles (more CTAs) finish it sooner (32 columns: 13 % slower state stage at
-// T = 4096, H = 16; 8 columns: 4 % slower).
+// The chain of P - 1 dependent steps is latency-bound: each step's M_s
+// (128 x 128 fp32, shared by the head's column tiles) is copied into shared
+// memory one step ahead by per-thread 16-byte asynchronous copies (rows
+// padded to 132 floats: the 16 rows a warp reads at once start 4 banks
+// apart), so a step waits on shared memory only.
+constexpr int kCombineLd = 132;
 template <int CW>
-__global__ void __launch_bounds__(256) gdn2_scan_combine_kernel(Params p) {
+constexpr size_t combine_smem() {
+    return (2 * 128 * kCombineLd + 128 * CW) * sizeof(float);
+}
+template <int CW>
+__global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
     constexpr int D = 128, NX = CW / 2;  // two threads per row, NX columns each
-    __shared__ float Ssm[D][CW + 1];
+    extern __shared__ float4 combine_smem_raw[];
+    float *Ms = reinterpret_cast<float *>(combine_smem_raw);  // [2][D][kCombineLd]
+    float *Ss = Ms + 2 * D * kCombineLd;                      // [D][CW]
     if (p.status[0] != GDN2_OK) return;
     const int n = blockIdx.x, hv = blockIdx.y, c0 = CW * blockIdx.z;
-    const int r = threadIdx.x >> 1, hx = NX * (threadIdx.x & 1);
+    const int tid = threadIdx.x, r = tid >> 1, hx = NX * (tid & 1);
     const int P = p.sc_P;
     const size_t sblk = (static_cast<size_t>(n) * p.HV + hv) * D * D;
+    auto unit = [&](int sg) { return (static_cast<size_t>(n) * (P - 1) + sg) * p.HV + hv; };
+    auto load_m = [&](int sg) {  // M_sg: the first D columns of [M | B]
+        const float *tr = p.sc_tr + unit(sg) * D * (2 * D);
+        float *dst = Ms + (sg & 1) * D * kCombineLd;
+#pragma unroll 4
+        for (int i = tid; i < D * D / 4; i += 256) {
+            const int row = i / (D / 4), c4 = i % (D / 4);
+            cp_async16(dst + row * kCombineLd + 4 * c4, tr + static_cast<size_t>(row) * (2 * D) + 4 * c4, 16);
+        }
+        cp_async_commit();
+    };
+    if (P > 1) load_m(0);
 #pragma unroll
     for (int x = 0; x < NX; ++x)
-        Ssm[r][hx + x] = p.h0 ? state_ld(p.h0, sblk + state_off(r, c0 + hx + x, D, D, p.state_vmajor), p.state_bf16)
-                              : 0.f;
-    __syncthreads();
+        Ss[r * CW + hx + x] =
+            p.h0 ? state_ld(p.h0, sblk + state_off(r, c0 + hx + x, D, D, p.state_vmajor), p.state_bf16) : 0.f;
     for (int sg = 0; sg < P - 1; ++sg) {
-        const size_t u = (static_cast<size_t>(n) * (P - 1) + sg) * p.HV + hv;
-        const float *tr = p.sc_tr + u * D * (2 * D) + static_cast<size_t>(r) * (2 * D);  // row r of [M | B]
+        const bool ahead = sg + 1 < P - 1;
+        if (ahead) load_m(sg + 1);  // its buffer was last read in step sg - 1
+        const float *tr = p.sc_tr + unit(sg) * D * (2 * D) + static_cast<size_t>(r) * (2 * D);  // row r
         float acc[NX];
 #pragma unroll
-        for (int x = 0; x < NX; ++x) acc[x] = tr[D + c0 + hx + x];
+        for (int x = 0; x < NX; x += 4) {
+            const float4 b = *reinterpret_cast<const float4 *>(tr + D + c0 + hx + x);
+            acc[x] = b.x; acc[x + 1] = b.y; acc[x + 2] = b.z; acc[x + 3] = b.w;
+        }
+        if (ahead)
+            cp_async_wait_group<1>();
+        else
+            cp_async_wait_group<0>();
+        __syncthreads();  // M_sg and S_in(sg) are in shared memory
+        const float *mrow = Ms + (sg & 1) * D * kCombineLd + r * kCombineLd;
 #pragma unroll 4
         for (int c = 0; c < D; c += 4) {
-            const float4 m4 = *reinterpret_cast<const float4 *>(tr + c);
+            const float4 m4 = *reinterpret_cast<const float4 *>(mrow + c);
             const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
+            for (int k = 0; k < 4; ++k) {
 #pragma unroll
-                for (int x = 0; x < NX; ++x) acc[x] += mv[k] * Ssm[c + k][hx + x];
+                for (int x = 0; x < NX; x += 4) {
+                    const float4 sv = *reinterpret_cast<const float4 *>(Ss + (c + k) * CW + hx + x);
+                    acc[x] += mv[k] * sv.x;
+                    acc[x + 1] += mv[k] * sv.y;
+                    acc[x + 2] += mv[k] * sv.z;
+                    acc[x + 3] += mv[k] * sv.w;
+                }
+            }
         }
-        __syncthreads();
-        float *si = p.sc_si + u * D * D + static_cast<size_t>(r) * D + c0 + hx;
+        __syncthreads();  // every read of S_in(sg) and of M_sg is done
+        float *si = p.sc_si + unit(sg) * D * D + static_cast<size_t>(r) * D + c0 + hx;
 #pragma unroll
-        for (int x = 0; x < NX; ++x) {
-            Ssm[r][hx + x] = acc[x];
-            si[x] = acc[x];
+        for (int x = 0; x < NX; x += 4) {
+            const float4 o = make_float4(acc[x], acc[x + 1], acc[x + 2], acc[x + 3]);
+            *reinterpret_cast<float4 *>(Ss + r * CW + hx + x) = o;
+            *reinterpret_cast<float4 *>(si + x) = o;
         }
-        __syncthreads();
     }
 }
 
 }  // namespace
 
 cudaError_t launch_tc_scan_combine(const Params &p, cudaStream_t s) {
-    if (p.N > 0 && p.sc_P > 1) gdn2_scan_combine_kernel<16><<<dim3(p.N, p.HV, 128 / 16), 256, 0, s>>>(p);
+    constexpr int CW = 16;
+    if (p.N <= 0 || p.sc_P <= 1) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(gdn2_scan_combine_kernel<CW>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(combine_smem<CW>()));
+    if (e != cudaSuccess) return e;
+    gdn2_scan_combine_kernel<CW><<<dim3(p.N, p.HV, 128 / CW), 256, combine_smem<CW>(), s>>>(p);
     return cudaGetLastError();
 }
 
