@@ -773,6 +773,18 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         tma_prefetch_3d(&p.tm_q, 0, p.tm_order_q ? t0 : nq_h, p.tm_order_q ? nq_h : t0);
         if (p.has_beta) tma_prefetch_3d(&p.tm_b, 0, p.tm_order_b ? t0 : nhv, p.tm_order_b ? nhv : t0);
     }
+    // The fp16 T image (K-major [64 t][64 s]) is written as its blocks are
+    // computed: zeros above the diagonal blocks here, each diagonal block by
+    // its inverse, each off-diagonal block by its merge.
+    uint8_t *timg = sm + C::oTimg;
+    if (tid >= 64) {  // 16-byte zero chunks: rows of block I, chunks 2 (I + 1) .. 7
+        for (int e = tid - 64; e < 192; e += kIntraThreads - 64) {
+            const int Ib = e < 96 ? 0 : e < 160 ? 1 : 2;
+            const int e0 = e - (Ib == 0 ? 0 : Ib == 1 ? 96 : 160), nz = 6 - 2 * Ib;
+            const int row = 16 * Ib + e0 / nz, chunk = 2 * (Ib + 1) + e0 % nz;
+            *reinterpret_cast<uint4 *>(timg + swz(row, chunk)) = make_uint4(0, 0, 0, 0);
+        }
+    }
     if (tid < 64) {  // diagonal 16x16 blocks, one thread per (block, column)
         const int Ib = tid / 16, j = tid % 16, o = 16 * Ib;
         float x[16];
@@ -813,6 +825,14 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
             }
         }
         *reinterpret_cast<float2 *>(Yb + b * 256 + i * 16 + j0) = make_float2(y0, y1);
+        // row i, columns j0, j0 + 1 of the diagonal blocks I and I + 1 into the image
+#pragma unroll
+        for (int d = 0; d < 2; ++d) {
+            const int o = d ? r0 : c0;
+            const float2 tv = *reinterpret_cast<const float2 *>(Tf + (o + i) * kLD + o + j0);
+            *reinterpret_cast<uint32_t *>(timg + swz(o + i, (o + j0) / 8) + ((o + j0) % 8) * 2) =
+                pack_h2m(tv.x, tv.y, hmax);
+        }
         __syncthreads();
         float z0 = 0.f, z1 = 0.f;
 #pragma unroll
@@ -827,6 +847,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
             }
         }
         *reinterpret_cast<float2 *>(Tf + (r0 + i) * kLD + c0 + j0) = make_float2(z0, z1);
+        *reinterpret_cast<uint32_t *>(timg + swz(r0 + i, (c0 + j0) / 8) + ((c0 + j0) % 8) * 2) = pack_h2m(z0, z1, hmax);
     }
     __syncthreads();
     // 32 -> 64 merge on the 32 x 32 halves a (rows/cols 0-31) and b (32-63):
@@ -864,22 +885,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         }
         *reinterpret_cast<float2 *>(Tf + (32 + i0) * kLD + j0) = make_float2(z00, z01);
         *reinterpret_cast<float2 *>(Tf + (33 + i0) * kLD + j0) = make_float2(z10, z11);
-    }
-    __syncthreads();
-    // T -> fp16 K-major image [64 t][64 s]; zeros above the diagonal.  An
-    // eight-lane group takes chunks 0-3 of row 2m and 4-7 of row 2m + 1 (or
-    // the other halves): fp32 rows kLD = 68 floats apart start 4 banks apart,
-    // so its 16-byte loads cover all 32 banks, and so do its swizzled stores.
-    for (int e = tid; e < 64 * 8; e += kIntraThreads) {
-        const int l = e % 16, hb = (l / 4) & 1;
-        const int tt = 2 * (e / 16) + hb, chunk = (l % 4) + 4 * (hb ^ (l / 8));
-        const float4 lo = *reinterpret_cast<const float4 *>(Tf + tt * kLD + 8 * chunk);
-        const float4 hi = *reinterpret_cast<const float4 *>(Tf + tt * kLD + 8 * chunk + 4);
-        const float tv8[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        float f[8];
-#pragma unroll
-        for (int x = 0; x < 8; ++x) f[x] = 8 * chunk + x <= tt ? tv8[x] : 0.f;
-        *reinterpret_cast<uint4 *>(sm + C::oTimg + swz(tt, chunk)) = pack8_hm(f, hmax);
+        *reinterpret_cast<uint32_t *>(timg + swz(32 + i0, j0 / 8) + (j0 % 8) * 2) = pack_h2m(z00, z01, hmax);
+        *reinterpret_cast<uint32_t *>(timg + swz(33 + i0, j0 / 8) + (j0 % 8) * 2) = pack_h2m(z10, z11, hmax);
     }
     fence_proxy_async();
     tc_fence_before();
