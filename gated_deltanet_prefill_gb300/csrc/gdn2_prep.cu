@@ -16,14 +16,40 @@ namespace gdn2 {
 namespace {
 
 constexpr int kMapThreads = 1024;
+constexpr int kSeqCache = 4096;  // seq_first entries kept in shared memory
+
+// Inclusive prefix sum of x over the CTA's 1024 threads: a shuffle scan in
+// each warp, then one over the 32 warp totals.  sums: 32 ints of shared
+// memory, free again after the call's second barrier.
+__device__ __forceinline__ int block_scan(int x, int *sums) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) sums[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int t = sums[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, off);
+            if (lane >= off) t += y;
+        }
+        sums[lane] = t;
+    }
+    __syncthreads();
+    return w > 0 ? x + sums[w - 1] : x;
+}
 
 // One CTA: validate cu_seqlens, scan the per-sequence chunk counts, fill the
 // per-chunk table.  Invalid cu_seqlens -> status word set, zero chunks.
 __global__ void __launch_bounds__(kMapThreads) gdn2_chunk_map_kernel(Params p) {
     __shared__ int s_bad;
-    __shared__ int s_scan[kMapThreads];
+    __shared__ int s_sums[32];
     __shared__ int s_pos[kMapThreads];  // chunk-count buckets of the sequence order
-    __shared__ int s_total;
+    __shared__ int s_first[kSeqCache];  // seq_first[0 .. N] when N < kSeqCache
     const int tid = threadIdx.x;
     if (tid == 0) {
         s_bad = 0;
@@ -46,53 +72,43 @@ __global__ void __launch_bounds__(kMapThreads) gdn2_chunk_map_kernel(Params p) {
         for (int n = tid; n <= p.N; n += kMapThreads) p.seq_first[n] = 0;
         return;
     }
+    const bool cached = p.N < kSeqCache;
     int running = 0;
     for (int base = 0; base < p.N; base += kMapThreads) {
         const int n = base + tid;
         int cnt = 0;
         if (n < p.N) cnt = static_cast<int>((cu_at(p, n + 1) - cu_at(p, n) + kChunk - 1) / kChunk);
-        s_scan[tid] = cnt;
-        __syncthreads();
-        for (int off = 1; off < kMapThreads; off <<= 1) {  // inclusive Hillis-Steele scan
-            const int x = tid >= off ? s_scan[tid - off] : 0;
-            __syncthreads();
-            s_scan[tid] += x;
-            __syncthreads();
+        const int incl = block_scan(cnt, s_sums);
+        if (n < p.N) {
+            p.seq_first[n] = running + incl - cnt;
+            if (cached) s_first[n] = running + incl - cnt;
         }
-        if (n < p.N) p.seq_first[n] = running + s_scan[tid] - cnt;
-        if (tid == kMapThreads - 1) s_total = s_scan[tid];
-        __syncthreads();
-        running += s_total;
-        __syncthreads();
+        running += s_sums[31];  // the batch total
+        __syncthreads();        // read by every thread before the next batch's scan writes s_sums
     }
     const int NC = running;
     if (tid == 0) {
         p.seq_first[p.N] = NC;
+        if (cached) s_first[p.N] = NC;
         p.status[0] = GDN2_OK;
         p.status[1] = NC;
     }
     s_pos[tid] = 0;
-    __syncthreads();  // seq_first (global, written above by this CTA) is now visible to it
+    __syncthreads();  // seq_first (global, and its shared copy) is now visible to the CTA
+    auto first = [&](int n) { return cached ? s_first[n] : p.seq_first[n]; };
     // Sequence order for the state pass: longest first, so that the longest
     // chunk chains start in the first wave of CTAs.  A counting sort over
     // chunk counts (kMapThreads buckets, the last one open-ended); the order
     // inside a bucket follows the shared-memory atomics and only decides
     // which CTA starts first, never a result.
-    auto bucket = [&](int n) { return min(p.seq_first[n + 1] - p.seq_first[n], kMapThreads - 1); };
+    auto bucket = [&](int n) { return min(first(n + 1) - first(n), kMapThreads - 1); };
     for (int n = tid; n < p.N; n += kMapThreads) atomicAdd(&s_pos[bucket(n)], 1);
     __syncthreads();
     {  // s_pos[b] = number of sequences in buckets above b (descending exclusive scan)
         const int b = kMapThreads - 1 - tid;
         const int cnt = s_pos[b];
-        s_scan[tid] = cnt;
-        __syncthreads();
-        for (int off = 1; off < kMapThreads; off <<= 1) {
-            const int x = tid >= off ? s_scan[tid - off] : 0;
-            __syncthreads();
-            s_scan[tid] += x;
-            __syncthreads();
-        }
-        s_pos[b] = s_scan[tid] - cnt;
+        const int incl = block_scan(cnt, s_sums);
+        s_pos[b] = incl - cnt;
     }
     __syncthreads();
     for (int n = tid; n < p.N; n += kMapThreads) p.seq_order[atomicAdd(&s_pos[bucket(n)], 1)] = n;
@@ -106,9 +122,9 @@ __global__ void __launch_bounds__(kMapThreads) gdn2_chunk_map_kernel(Params p) {
         int lo = 0, hi = p.N - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (p.seq_first[mid] <= c) lo = mid; else hi = mid - 1;
+            if (first(mid) <= c) lo = mid; else hi = mid - 1;
         }
-        const int64_t start = cu_at(p, lo) + static_cast<int64_t>(c - p.seq_first[lo]) * kChunk;
+        const int64_t start = cu_at(p, lo) + static_cast<int64_t>(c - first(lo)) * kChunk;
         const int64_t end = cu_at(p, lo + 1);
         p.chunk_seq[c] = lo;
         p.chunk_start[c] = start;

@@ -372,13 +372,15 @@ def test_state_kernels_128_column_tiles(cuda_lib, monkeypatch, lookahead, varian
     assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
 
 
-def test_many_short_sequences(cuda_lib):
-    """2,500 ragged sequences of 0-130 tokens (more than the chunk map's 1024
-    threads: its scans and its longest-first counting sort loop), grouped
-    value heads, an initial state; every output row and final state against
-    the oracle."""
+@pytest.mark.parametrize("n_seq", [2500, 5000])
+def test_many_short_sequences(cuda_lib, n_seq):
+    """2,500 or 5,000 ragged sequences of 0-130 tokens (more than the chunk
+    map's 1024 threads: its scans and its longest-first counting sort loop;
+    5,000 is past the 4,095 sequences whose chunk offsets it keeps in shared
+    memory), grouped value heads, an initial state; every output row and
+    final state against the oracle."""
     rng = np.random.default_rng(99)
-    lens = [int(x) for x in rng.integers(0, 131, size=2500)]
+    lens = [int(x) for x in rng.integers(0, 131, size=n_seq)]
     lens[::97] = [0] * len(lens[::97])  # some empty sequences
     wl = inputs.small("many", lens, H=1, HV=2, K=64, V=64, g_max=1.0, beta_max=2.0, h0_std=0.05, seed=98)
     d = inputs.generate(wl)
