@@ -155,26 +155,42 @@ def strip_comments(src):
     return "\n".join(ln for ln in lines if ln.strip())
 
 
-def kernel_source_sha(read=None):
-    """Hash of the CUDA sources' code (comments and blank lines ignored), to
-    tell whether a committed ncu summary was taken on the current kernels."""
+# The source files of the kernels each profiled stage runs (besides every
+# shared header): a committed ncu summary stays valid while these are unchanged.
+STAGE_SOURCES = {
+    "intra": ["gdn2_tc_intra.cu"],
+    "state_output": ["gdn2_tc_state_la.cu", "gdn2_tc_state.cu"],
+    "recurrent": ["gdn2_recurrent.cu"],
+}
+
+
+def kernel_source_sha(read=None, files=None):
+    """Hash of the CUDA sources' code (comments and blank lines ignored): of
+    every source, or of the headers and the named .cu files.  It tells whether
+    a committed ncu summary was taken on the current kernels."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_deltanet_prefill_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
+        if f.endswith(".cuh") or (f.endswith(".cu") and (files is None or f in files)):
             txt = read(f) if read else open(os.path.join(csrc, f), encoding="utf-8").read()
             h.update(f.encode() + b"\0" + strip_comments(txt).encode() + b"\0")
     return h.hexdigest()[:16]
 
 
+def stage_source_sha(stage):
+    """kernel_source_sha over the headers and the stage's own kernel sources."""
+    return kernel_source_sha(files=STAGE_SOURCES.get(stage))
+
+
 def ncu_traffic(stage, impl, workload_name):
     """DRAM bytes per launch of a stage's kernel from a committed ncu summary
     (profiles/*.md with lines 'traffic_bytes_per_launch: <n>' and
-    'source_sha: <sha>'); None when absent or taken on other kernel sources."""
+    'source_sha: <sha>', the stage_source_sha of the sources it was taken
+    on); None when absent or taken on other kernel sources."""
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
-    sha = kernel_source_sha()
+    sha = stage_source_sha(stage)
     for f in sorted(os.listdir(pdir)):
         if not f.endswith(".md"):
             continue
