@@ -66,6 +66,9 @@ __device__ __forceinline__ void set_timeout_la(const Params &p) {
     atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
 }
 
+// SCAN: the chunk-parallel modes, as in the 128-column kernel below (the
+// transitions on four 64-column tiles: two of M, two of B).
+template <bool SCAN>
 __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params p) {
     using C = LaCfg;
     constexpr int D = C::D, VT = C::VT, NSTAGE = C::NSTAGE;
@@ -78,12 +81,34 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
 
     if (p.status[0] != GDN2_OK) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // one CTA per (sequence in longest-first order, value head, 64-column tile)
-    const int tile = blockIdx.x % 2;
-    const int hv = (blockIdx.x / 2) % p.HV;
-    const int n = chk(p.seq_order[blockIdx.x / (2 * p.HV)], 0, p.N, 301, p.status);
-    const int v0 = tile * VT;
-    const int first = p.seq_first[n], nck = p.seq_first[n + 1] - first;
+    // one CTA per (sequence in longest-first order, segment, value head,
+    // 64-column tile), the tile fastest; the sequential pass has one segment
+    int mode = 0, P = 1, tile, seg = 0, hv, n, first, nck, c_lo = 0;
+    if constexpr (SCAN) {
+        mode = p.sc_mode;
+        P = p.sc_P;
+        const int segs = mode == 1 ? P - 1 : P;
+        const int tiles = mode == 1 ? 4 : 2;
+        tile = blockIdx.x % tiles;
+        hv = (blockIdx.x / tiles) % p.HV;
+        const int rs = blockIdx.x / (tiles * p.HV);
+        seg = rs % segs;
+        n = chk(p.seq_order[rs / segs], 0, p.N, 301, p.status);
+        const int seq0 = p.seq_first[n], nck_all = p.seq_first[n + 1] - seq0;
+        const int L = (nck_all + P - 1) / P;
+        c_lo = min(seg * L, nck_all);
+        first = seq0 + c_lo;
+        nck = min(c_lo + L, nck_all) - c_lo;
+    } else {
+        tile = blockIdx.x % 2;
+        hv = (blockIdx.x / 2) % p.HV;
+        n = chk(p.seq_order[blockIdx.x / (2 * p.HV)], 0, p.N, 301, p.status);
+        first = p.seq_first[n];
+        nck = p.seq_first[n + 1] - first;
+    }
+    const bool trans = SCAN && mode == 1, is_m = trans && tile < 2;  // is_m: columns of M (no Ut)
+    // columns of this tile: of M (is_m), else of V (the state, or B)
+    const int v0 = (trans && !is_m ? tile - 2 : tile) * VT;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -133,7 +158,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
                                 Rec<D>::bytes;
                 mbar_arrive_expect_tx(&full_bar[s], C::kLoadBytes);
                 bulk_g2s(stage(i) + C::sP, rec + Rec<D>::P, Rec<D>::mma_prefix, &full_bar[s]);
-                bulk_g2s(stage(i) + C::sUt, rec + Rec<D>::Ut + tile * 8192, 8192, &full_bar[s]);
+                bulk_g2s(stage(i) + C::sUt, rec + Rec<D>::Ut + (v0 / VT) * 8192, 8192, &full_bar[s]);  // unread for M
                 bulk_g2s(sm + C::oEGL + s * D * 4, rec + Rec<D>::eGL, D * 4, &full_bar[s]);
                 ++issued;
             }
@@ -255,7 +280,23 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
             }
         };
         uint32_t r[32];
-        if (p.h0 && plain) {
+        // the segment's incoming state: [I | 0] (transitions), the combined
+        // state (a later replay segment) or the initial state
+        const float *si = SCAN && mode == 2 && seg > 0
+                              ? p.sc_si + ((static_cast<size_t>(n) * (P - 1) + seg - 1) * p.HV + hv) * D * D
+                              : nullptr;
+        if (SCAN && trans) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(is_m && row == col0 + e ? 1.f : 0.f);
+        } else if (SCAN && si) {
+            const float *src = si + static_cast<size_t>(row) * D + col0;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(src + e);
+                r[e] = __float_as_uint(x.x); r[e + 1] = __float_as_uint(x.y);
+                r[e + 2] = __float_as_uint(x.z); r[e + 3] = __float_as_uint(x.w);
+            }
+        } else if (p.h0 && plain) {
             const float *h0 = static_cast<const float *>(p.h0) + sblk + static_cast<size_t>(row) * D + col0;
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
@@ -303,12 +344,23 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
             ok = false;
         }
         tc_fence_after();
-        if (ok && p.hT) {
+        // the transitions write [M | B]; the replay writes the final state from
+        // the last segment only
+        const bool write_final = (SCAN && trans) || (p.hT && (mode != 2 || seg == P - 1));
+        if (ok && write_final) {
             if (nck > 0) {  // S_nck (with no chunk, S_0 is still in registers)
                 tmem_ld32(tS + lane_base + 32 * g, r);
                 tmem_ld_wait();
             }
-            if (plain) {
+            if (SCAN && trans) {
+                float *tr = p.sc_tr + ((static_cast<size_t>(n) * (P - 1) + seg) * p.HV + hv) * D * (2 * D) +
+                            static_cast<size_t>(row) * (2 * D) + tile * VT + 32 * g;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4 *>(tr + e) = make_float4(
+                        __uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                        __uint_as_float(r[e + 3]));
+            } else if (plain) {
                 float *hT = static_cast<float *>(p.hT) + sblk + static_cast<size_t>(row) * D + col0;
 #pragma unroll
                 for (int e = 0; e < 32; e += 4)
@@ -357,8 +409,8 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
                 break;
             }
             tc_fence_after();
-            const int64_t tok = seq_start + static_cast<int64_t>(c) * kChunk + t;
-            const bool valid = tok < seq_end;
+            const int64_t tok = seq_start + static_cast<int64_t>(c_lo + c) * kChunk + t;
+            const bool valid = !trans && tok < seq_end;
             bf16 *orow = p.o + tok * p.so_t + static_cast<int64_t>(hv) * p.so_h + v0;
 #pragma unroll 1
             for (int j = 0; j < VT / 32; ++j) {
@@ -401,7 +453,8 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
             tmem_ld_wait();
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(ut + swz(t, 4 * g + cc));
+                const uint4 u = SCAN && is_m ? make_uint4(0, 0, 0, 0)
+                                             : *reinterpret_cast<const uint4 *>(ut + swz(t, 4 * g + cc));
                 const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
                 uint32_t ow[4];
 #pragma unroll
@@ -458,6 +511,11 @@ struct La128Cfg {
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
+// SCAN = false: the sequential pass.  SCAN = true: the chunk-parallel modes of
+// the plain state kernel (sc_mode 1: the transitions [M | B] of segments
+// 0 .. P - 2 on two 128-column tiles, M from the identity with no Ut and no
+// output; sc_mode 2: every segment from its incoming state).
+template <bool SCAN>
 __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Params p) {
     using C = La128Cfg;
     constexpr int D = C::D, NSTAGE = C::NSTAGE;
@@ -470,10 +528,33 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
 
     if (p.status[0] != GDN2_OK) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // one CTA per (sequence in longest-first order, value head)
-    const int hv = blockIdx.x % p.HV;
-    const int n = chk(p.seq_order[blockIdx.x / p.HV], 0, p.N, 401, p.status);
-    const int first = p.seq_first[n], nck = p.seq_first[n + 1] - first;
+    // one CTA per (sequence in longest-first order, segment, value head, tile),
+    // the tile fastest; the sequential pass has one segment and one tile.  A
+    // segment's chunks are [seg L, seg L + L) of the sequence's, L =
+    // ceil(chunks / P).
+    int mode = 0, P = 1, tile = 0, seg = 0, hv, n, first, nck, c_lo = 0;
+    if constexpr (SCAN) {
+        mode = p.sc_mode;
+        P = p.sc_P;
+        const int segs = mode == 1 ? P - 1 : P;
+        const int tiles = mode == 1 ? 2 : 1;
+        tile = blockIdx.x % tiles;
+        hv = (blockIdx.x / tiles) % p.HV;
+        const int rs = blockIdx.x / (tiles * p.HV);
+        seg = rs % segs;
+        n = chk(p.seq_order[rs / segs], 0, p.N, 401, p.status);
+        const int seq0 = p.seq_first[n], nck_all = p.seq_first[n + 1] - seq0;
+        const int L = (nck_all + P - 1) / P;
+        c_lo = min(seg * L, nck_all);
+        first = seq0 + c_lo;
+        nck = min(c_lo + L, nck_all) - c_lo;
+    } else {
+        hv = blockIdx.x % p.HV;
+        n = chk(p.seq_order[blockIdx.x / p.HV], 0, p.N, 401, p.status);
+        first = p.seq_first[n];
+        nck = p.seq_first[n + 1] - first;
+    }
+    const bool trans = SCAN && mode == 1, is_m = trans && tile == 0;  // is_m: columns of M (no Ut)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -520,6 +601,10 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
                 bulk_g2s(sm + C::oEGL + s * D * 4, rec_of(i) + Rec<D>::eGL, D * 4, &full_bar[s]);
             };
             auto load_ut = [&](int c) {
+                if (SCAN && is_m) {  // Ut = 0: the U epilogue writes -Wt S without reading the buffer
+                    mbar_arrive(&ut_full[c & 1]);
+                    return;
+                }
                 mbar_arrive_expect_tx(&ut_full[c & 1], C::kUBytes);
                 bulk_g2s(ubuf(c), rec_of(c) + Rec<D>::Ut, C::kUBytes, &ut_full[c & 1]);
             };
@@ -671,9 +756,25 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
                 *reinterpret_cast<uint4 *>(blk + swz(row, 4 * (gcol & 1) + cc)) = v;
             }
         };
+        // the segment's incoming state: [I | 0] (transitions), the combined
+        // state (a later replay segment) or the initial state
+        const float *si = SCAN && mode == 2 && seg > 0
+                              ? p.sc_si + ((static_cast<size_t>(n) * (P - 1) + seg - 1) * p.HV + hv) * D * D
+                              : nullptr;
         auto load_h0 = [&](int gcol, uint32_t (&r)[32]) {
             const int col0 = 32 * gcol;
-            if (p.h0 && plain) {
+            if (SCAN && trans) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(is_m && row == col0 + e ? 1.f : 0.f);
+            } else if (SCAN && si) {
+                const float *src = si + static_cast<size_t>(row) * D + col0;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src + e);
+                    r[e] = __float_as_uint(x.x); r[e + 1] = __float_as_uint(x.y);
+                    r[e + 2] = __float_as_uint(x.z); r[e + 3] = __float_as_uint(x.w);
+                }
+            } else if (p.h0 && plain) {
                 const float *h0 = static_cast<const float *>(p.h0) + sblk + static_cast<size_t>(row) * D + col0;
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
@@ -733,17 +834,28 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
             ok = false;
         }
         tc_fence_after();
-        if (ok && p.hT) {
+        // the transitions write [M | B]; the replay writes the final state from
+        // the last segment only
+        const bool write_final = (SCAN && trans) || (p.hT && (mode != 2 || seg == P - 1));
+        if (ok && write_final) {
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 const int col0 = 32 * (2 * g2 + h);
-                if (nck > 0) {  // S_nck (with no chunk, S_0 = h0)
+                if (nck > 0) {  // S_nck (with no chunk, S_0)
                     tmem_ld32(tS + lane_base + col0, r);
                     tmem_ld_wait();
                 } else {
                     load_h0(2 * g2 + h, r);
                 }
-                if (plain) {
+                if (SCAN && trans) {
+                    float *tr = p.sc_tr + ((static_cast<size_t>(n) * (P - 1) + seg) * p.HV + hv) * D * (2 * D) +
+                                static_cast<size_t>(row) * (2 * D) + tile * D + col0;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(tr + e) = make_float4(
+                            __uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                            __uint_as_float(r[e + 3]));
+                } else if (plain) {
                     float *hT = static_cast<float *>(p.hT) + sblk + static_cast<size_t>(row) * D + col0;
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
@@ -793,8 +905,8 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
                 break;
             }
             tc_fence_after();
-            const int64_t tok = seq_start + static_cast<int64_t>(c) * kChunk + t;
-            const bool valid = tok < seq_end;
+            const int64_t tok = seq_start + static_cast<int64_t>(c_lo + c) * kChunk + t;
+            const bool valid = !trans && tok < seq_end;
             bf16 *orow = p.o + tok * p.so_t + static_cast<int64_t>(hv) * p.so_h;
 #pragma unroll 1
             for (int j = 0; j < D / 32; ++j) {
@@ -839,7 +951,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     uint4 *at = reinterpret_cast<uint4 *>(blk + swz(t, 4 * h + cc));
-                    const uint4 u = *at;
+                    const uint4 u = SCAN && is_m ? make_uint4(0, 0, 0, 0) : *at;
                     const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
                     uint32_t ow[4];
 #pragma unroll
@@ -869,20 +981,22 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
 }  // namespace
 
 cudaError_t launch_tc_state_la(const Params &p, cudaStream_t s) {
-    auto kern = gdn2_tc_state_la_kernel;
+    auto kern = p.sc_mode == 0 ? gdn2_tc_state_la_kernel<false> : gdn2_tc_state_la_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LaCfg::kSmem);
     if (e != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(p.N) * p.HV * 2;
+    const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
+    const long long ctas = static_cast<long long>(p.N) * segs * p.HV * (p.sc_mode == 1 ? 4 : 2);
     if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
     if (ctas > 0) kern<<<static_cast<unsigned>(ctas), kLaThreads, LaCfg::kSmem, s>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_tc_state_la128(const Params &p, cudaStream_t s) {
-    auto kern = gdn2_tc_state_la128_kernel;
+    auto kern = p.sc_mode == 0 ? gdn2_tc_state_la128_kernel<false> : gdn2_tc_state_la128_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, La128Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(p.N) * p.HV;
+    const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
+    const long long ctas = static_cast<long long>(p.N) * segs * p.HV * (p.sc_mode == 1 ? 2 : 1);
     if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
     if (ctas > 0) kern<<<static_cast<unsigned>(ctas), kLaThreads, La128Cfg::kSmem, s>>>(p);
     return cudaGetLastError();

@@ -1,8 +1,9 @@
 """GPU parity of the chunk-parallel state pass (tensor-core path, K = V =
 128): each sequence's chunks in P segments; segment transitions [M | B] of
 S_out = M S_in + B in parallel, a combine over segments, then every segment
-replayed from its incoming state.  Checked against the FP64 oracle and
-against the sequential pass.
+replayed from its incoming state.  The transitions and the replay run on the
+lookahead state kernels (on the plain one with GDN2_STATE_LOOKAHEAD=0).
+Checked against the FP64 oracle and against the sequential pass.
 
 Bar: max|x - x_ref| / max|x_ref| <= 1e-2 for o and for the final state.
 """
@@ -48,6 +49,22 @@ def test_forced_segments_match_oracle(cuda_lib, segments):
     o1, h1 = run(cuda_lib, d, 1)  # sequential pass
     assert rel_max(o.float().cpu().numpy(), o1.float().cpu().numpy()) <= TOL
     assert rel_max(hT.cpu().numpy(), h1.cpu().numpy()) <= TOL
+
+
+@pytest.mark.parametrize("segments", [3, 5])
+def test_forced_segments_plain_kernel(cuda_lib, monkeypatch, segments):
+    """The same with the transitions and the replay on the plain state kernel
+    (GDN2_STATE_LOOKAHEAD=0); the default runs them on the lookahead kernels.
+    P = 3 takes 64-column tiles, P = 5 128-column ones."""
+    monkeypatch.setenv("GDN2_STATE_LOOKAHEAD", "0")
+    wl = inputs.small("scanplain", [700, 1, 129, 2000], H=2, HV=4, K=128, V=128, g_max=2.0, beta_max=2.0,
+                      h0_std=0.05, seed=73)
+    d = inputs.generate(wl)
+    o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                                       initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
+    o, hT = run(cuda_lib, d, segments)
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
 
 
 def test_automatic_segments(cuda_lib):
