@@ -540,7 +540,7 @@ cudaError_t launch_tc_state(const Params &p, cudaStream_t s) {
     // both tile widths, =64 for 128-column tiles only; for comparison)
     const char *la = getenv("GDN2_STATE_LOOKAHEAD");
     const bool la_off = la && la[0] == '0', la128_off = la_off || (la && la[0] == '6' && la[1] == '4');
-    if (p.vtile == 64 && !la_off) return launch_tc_state_la(p, s);
+    if (p.vtile == 64 && p.sc_mode != 1 && !la_off) return launch_tc_state_la(p, s);
     if (p.vtile == 128 && !la128_off) return launch_tc_state_la128(p, s);
     if (p.sc_mode != 0)
         return p.vtile == 64 ? launch_state<128, 64, 3, true>(p, s) : launch_state<128, 128, 2, true>(p, s);

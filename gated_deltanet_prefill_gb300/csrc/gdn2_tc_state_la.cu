@@ -66,8 +66,8 @@ __device__ __forceinline__ void set_timeout_la(const Params &p) {
     atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
 }
 
-// SCAN: the chunk-parallel modes, as in the 128-column kernel below (the
-// transitions on four 64-column tiles: two of M, two of B).
+// SCAN: the replay of the chunk-parallel pass (sc_mode 2), as in the
+// 128-column kernel below; the transitions always take 128-column tiles.
 template <bool SCAN>
 __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params p) {
     using C = LaCfg;
@@ -83,17 +83,14 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // one CTA per (sequence in longest-first order, segment, value head,
     // 64-column tile), the tile fastest; the sequential pass has one segment
-    int mode = 0, P = 1, tile, seg = 0, hv, n, first, nck, c_lo = 0;
+    int P = 1, tile, seg = 0, hv, n, first, nck, c_lo = 0;
     if constexpr (SCAN) {
-        mode = p.sc_mode;
         P = p.sc_P;
-        const int segs = mode == 1 ? P - 1 : P;
-        const int tiles = mode == 1 ? 4 : 2;
-        tile = blockIdx.x % tiles;
-        hv = (blockIdx.x / tiles) % p.HV;
-        const int rs = blockIdx.x / (tiles * p.HV);
-        seg = rs % segs;
-        n = chk(p.seq_order[rs / segs], 0, p.N, 301, p.status);
+        tile = blockIdx.x % 2;
+        hv = (blockIdx.x / 2) % p.HV;
+        const int rs = blockIdx.x / (2 * p.HV);
+        seg = rs % P;
+        n = chk(p.seq_order[rs / P], 0, p.N, 301, p.status);
         const int seq0 = p.seq_first[n], nck_all = p.seq_first[n + 1] - seq0;
         const int L = (nck_all + P - 1) / P;
         c_lo = min(seg * L, nck_all);
@@ -106,9 +103,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
         first = p.seq_first[n];
         nck = p.seq_first[n + 1] - first;
     }
-    const bool trans = SCAN && mode == 1, is_m = trans && tile < 2;  // is_m: columns of M (no Ut)
-    // columns of this tile: of M (is_m), else of V (the state, or B)
-    const int v0 = (trans && !is_m ? tile - 2 : tile) * VT;
+    const int v0 = tile * VT;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -158,7 +153,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
                                 Rec<D>::bytes;
                 mbar_arrive_expect_tx(&full_bar[s], C::kLoadBytes);
                 bulk_g2s(stage(i) + C::sP, rec + Rec<D>::P, Rec<D>::mma_prefix, &full_bar[s]);
-                bulk_g2s(stage(i) + C::sUt, rec + Rec<D>::Ut + (v0 / VT) * 8192, 8192, &full_bar[s]);  // unread for M
+                bulk_g2s(stage(i) + C::sUt, rec + Rec<D>::Ut + tile * 8192, 8192, &full_bar[s]);
                 bulk_g2s(sm + C::oEGL + s * D * 4, rec + Rec<D>::eGL, D * 4, &full_bar[s]);
                 ++issued;
             }
@@ -280,15 +275,12 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
             }
         };
         uint32_t r[32];
-        // the segment's incoming state: [I | 0] (transitions), the combined
-        // state (a later replay segment) or the initial state
-        const float *si = SCAN && mode == 2 && seg > 0
+        // the segment's incoming state: the combined state (a later replay
+        // segment) or the initial state
+        const float *si = SCAN && seg > 0
                               ? p.sc_si + ((static_cast<size_t>(n) * (P - 1) + seg - 1) * p.HV + hv) * D * D
                               : nullptr;
-        if (SCAN && trans) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(is_m && row == col0 + e ? 1.f : 0.f);
-        } else if (SCAN && si) {
+        if (SCAN && si) {
             const float *src = si + static_cast<size_t>(row) * D + col0;
 #pragma unroll
             for (int e = 0; e < 32; e += 4) {
@@ -344,23 +336,13 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
             ok = false;
         }
         tc_fence_after();
-        // the transitions write [M | B]; the replay writes the final state from
-        // the last segment only
-        const bool write_final = (SCAN && trans) || (p.hT && (mode != 2 || seg == P - 1));
-        if (ok && write_final) {
+        // the replay writes the final state from the last segment only
+        if (ok && p.hT && (!SCAN || seg == P - 1)) {
             if (nck > 0) {  // S_nck (with no chunk, S_0 is still in registers)
                 tmem_ld32(tS + lane_base + 32 * g, r);
                 tmem_ld_wait();
             }
-            if (SCAN && trans) {
-                float *tr = p.sc_tr + ((static_cast<size_t>(n) * (P - 1) + seg) * p.HV + hv) * D * (2 * D) +
-                            static_cast<size_t>(row) * (2 * D) + tile * VT + 32 * g;
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4 *>(tr + e) = make_float4(
-                        __uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
-                        __uint_as_float(r[e + 3]));
-            } else if (plain) {
+            if (plain) {
                 float *hT = static_cast<float *>(p.hT) + sblk + static_cast<size_t>(row) * D + col0;
 #pragma unroll
                 for (int e = 0; e < 32; e += 4)
@@ -410,7 +392,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
             }
             tc_fence_after();
             const int64_t tok = seq_start + static_cast<int64_t>(c_lo + c) * kChunk + t;
-            const bool valid = !trans && tok < seq_end;
+            const bool valid = tok < seq_end;
             bf16 *orow = p.o + tok * p.so_t + static_cast<int64_t>(hv) * p.so_h + v0;
 #pragma unroll 1
             for (int j = 0; j < VT / 32; ++j) {
@@ -453,8 +435,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
             tmem_ld_wait();
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                const uint4 u = SCAN && is_m ? make_uint4(0, 0, 0, 0)
-                                             : *reinterpret_cast<const uint4 *>(ut + swz(t, 4 * g + cc));
+                const uint4 u = *reinterpret_cast<const uint4 *>(ut + swz(t, 4 * g + cc));
                 const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
                 uint32_t ow[4];
 #pragma unroll
@@ -981,11 +962,11 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
 }  // namespace
 
 cudaError_t launch_tc_state_la(const Params &p, cudaStream_t s) {
+    if (p.sc_mode == 1) return cudaErrorInvalidValue;  // transitions: 128-column tiles only
     auto kern = p.sc_mode == 0 ? gdn2_tc_state_la_kernel<false> : gdn2_tc_state_la_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LaCfg::kSmem);
     if (e != cudaSuccess) return e;
-    const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
-    const long long ctas = static_cast<long long>(p.N) * segs * p.HV * (p.sc_mode == 1 ? 4 : 2);
+    const long long ctas = static_cast<long long>(p.N) * (p.sc_mode == 2 ? p.sc_P : 1) * p.HV * 2;
     if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
     if (ctas > 0) kern<<<static_cast<unsigned>(ctas), kLaThreads, LaCfg::kSmem, s>>>(p);
     return cudaGetLastError();
