@@ -1,7 +1,8 @@
-// Tensor-core state-passing kernels with a one-chunk lookahead (K = V = 128,
-// the sequential pass): gdn2_tc_state_la_kernel for 64-column V tiles and
-// gdn2_tc_state_la128_kernel for 128-column tiles (its layout at the second
-// kernel).
+// Tensor-core state-passing kernels with a one-chunk lookahead (K = V = 128):
+// gdn2_tc_state_la_kernel for 64-column V tiles and gdn2_tc_state_la128_kernel
+// for 128-column tiles (its layout at the second kernel).  They run the
+// sequential pass and, instantiated with SCAN, the transition and replay
+// launches of the chunk-parallel pass.
 //
 // The plain state kernel runs one dependent chain per chunk: S image ->
 // [Qe ; Wt] S -> U = Ut - Wt S -> S += Kd^T U -> next S image.  Here the next
