@@ -329,8 +329,10 @@ int describe_plan(const gdn2_dims &d, int sms, char *buf, size_t len) {
         if (d.K == 64) {
             add("; state_output gdn2_tc_state_kernel<64> %dx%d", d.N, HS);
         } else if (P > 1) {
-            add("; chunk-parallel state pass, %d segments: transitions %lld CTAs of 128 columns; combine %dx%dx8; "
-                "replay %lld CTAs of %d columns", P, 2ll * d.N * (P - 1) * HS, d.N, HS, 1ll * d.N * P * HS * (128 / vt), vt);
+            add("; chunk-parallel state pass, %d segments: transitions gdn2_tc_state_la128_kernel %lld CTAs of 128 "
+                "columns; combine %dx%dx8; replay %s %lld CTAs of %d columns",
+                P, 2ll * d.N * (P - 1) * HS, d.N, HS, vt == 64 ? "gdn2_tc_state_la_kernel" : "gdn2_tc_state_la128_kernel",
+                1ll * d.N * P * HS * (128 / vt), vt);
         } else {
             add("; state_output %s %lld CTAs of %d columns", vt == 64 ? "gdn2_tc_state_la_kernel" : "gdn2_tc_state_la128_kernel",
                 1ll * d.N * HS * (128 / vt), vt);
