@@ -280,3 +280,37 @@ def test_selftest_wait_timeout_argument_checks(lib):
     assert lib.gdn2_selftest_wait_timeout(ws, 64, 10**9, None) == 2            # limit above 100 ms
     if not torch.cuda.is_available():
         assert lib.gdn2_selftest_wait_timeout(ws, 64, 1_000_000, None) == 6    # ERR_ARCH
+
+
+def test_sliced_host_runner_plan():
+    """The piece bounds the pinned-host runner cuts sequences into (host
+    logic, no device): whole 64-token chunks, increasing, covering every
+    sequence, sized by the slice weights (by default the last two pieces are
+    half and a quarter of the others), and bad weights refused."""
+    g = gdn2
+
+    def plan(lens, slices, weights):
+        r = g._SlicedRunner.__new__(g._SlicedRunner)
+        r.S, r.N = slices, len(lens)
+        r.weights = weights
+        cu = [0]
+        for n in lens:
+            cu.append(cu[-1] + n)
+        return r._plan(cu)
+
+    lens = [32768, 32768 - 100, 1, 0, 640]
+    for weights in ([1] * 8, [4, 4, 4, 4, 4, 4, 2, 1], [1, 3, 2, 5, 1, 1, 1, 1]):
+        b, rows = plan(lens, 8, weights)
+        for n, L in enumerate(lens):
+            assert b[n][0] == 0 and b[n][-1] == L
+            assert all(x % 64 == 0 for x in b[n][:-1])
+            assert all(x <= y for x, y in zip(b[n], b[n][1:]))
+        assert sum(rows) == sum(lens)
+        w = sum(weights)
+        for j in range(8):  # piece j of the long sequence: its share within one chunk
+            assert abs((b[0][j + 1] - b[0][j]) - 32768 * weights[j] / w) <= 64
+    dummy = {"v": torch.zeros(4, 1, 64), "q": torch.zeros(4, 1, 64), "cu_seqlens": torch.tensor([0, 4])}
+    with pytest.raises(ValueError):
+        g._SlicedRunner(dummy, "tc", False, True, 4, slice_weights=[1, 1, 1])
+    with pytest.raises(ValueError):
+        g._SlicedRunner(dummy, "tc", False, True, 2, slice_weights=[1, 0])
