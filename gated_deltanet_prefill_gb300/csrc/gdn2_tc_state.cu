@@ -443,8 +443,9 @@ cudaError_t launch_state(const Params &p, cudaStream_t s) {
 // The chain of P - 1 dependent steps is latency-bound: each step's M_s
 // (128 x 128 fp32, shared by the head's column tiles) is copied into shared
 // memory one step ahead by per-thread 16-byte asynchronous copies (rows
-// padded to 132 floats: the 16 rows a warp reads at once start 4 banks
-// apart), so a step waits on shared memory only.
+// padded to 132 floats, so that rows read together start 4 banks apart), so
+// a step waits on shared memory only.  (Bulk copies of the 128 rows, 512 bytes
+// each, were slower.)
 constexpr int kCombineLd = 132;
 template <int CW>
 constexpr size_t combine_smem() {
@@ -452,13 +453,17 @@ constexpr size_t combine_smem() {
 }
 template <int CW>
 __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
-    constexpr int D = 128, NX = CW / 2;  // two threads per row, NX columns each
+    // thread: rows r0, r0 + 1 and 4 columns c0 .. c0 + 3 of the CTA's 128 x CW
+    // tile (CW = 16): per 4 steps of k, 2 + 4 16-byte shared loads feed 32
+    // multiply-adds into 8 independent accumulators
+    constexpr int D = 128, NC = 4;
+    static_assert(CW == 16, "256 threads cover 128 rows x 16 columns");
     extern __shared__ float4 combine_smem_raw[];
     float *Ms = reinterpret_cast<float *>(combine_smem_raw);  // [2][D][kCombineLd]
     float *Ss = Ms + 2 * D * kCombineLd;                      // [D][CW]
     if (p.status[0] != GDN2_OK) return;
-    const int n = blockIdx.x, hv = blockIdx.y, c0 = CW * blockIdx.z;
-    const int tid = threadIdx.x, r = tid >> 1, hx = NX * (tid & 1);
+    const int n = blockIdx.x, hv = blockIdx.y, cbase = CW * blockIdx.z;
+    const int tid = threadIdx.x, r0 = 2 * (tid / 4), c0 = NC * (tid % 4);
     const int P = p.sc_P;
     const size_t sblk = (static_cast<size_t>(n) * p.HV + hv) * D * D;
     auto unit = [&](int sg) { return (static_cast<size_t>(n) * (P - 1) + sg) * p.HV + hv; };
@@ -474,48 +479,49 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
     };
     if (P > 1) load_m(0);
 #pragma unroll
-    for (int x = 0; x < NX; ++x)
-        Ss[r * CW + hx + x] =
-            p.h0 ? state_ld(p.h0, sblk + state_off(r, c0 + hx + x, D, D, p.state_vmajor), p.state_bf16) : 0.f;
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int x = 0; x < NC; ++x)
+            Ss[(r0 + rr) * CW + c0 + x] =
+                p.h0 ? state_ld(p.h0, sblk + state_off(r0 + rr, cbase + c0 + x, D, D, p.state_vmajor), p.state_bf16)
+                     : 0.f;
     for (int sg = 0; sg < P - 1; ++sg) {
         const bool ahead = sg + 1 < P - 1;
         if (ahead) load_m(sg + 1);  // its buffer was last read in step sg - 1
-        const float *tr = p.sc_tr + unit(sg) * D * (2 * D) + static_cast<size_t>(r) * (2 * D);  // row r
-        float acc[NX];
+        const float *tr = p.sc_tr + unit(sg) * D * (2 * D);
+        float acc[2][NC];
 #pragma unroll
-        for (int x = 0; x < NX; x += 4) {
-            const float4 b = *reinterpret_cast<const float4 *>(tr + D + c0 + hx + x);
-            acc[x] = b.x; acc[x + 1] = b.y; acc[x + 2] = b.z; acc[x + 3] = b.w;
+        for (int rr = 0; rr < 2; ++rr) {
+            const float4 b = *reinterpret_cast<const float4 *>(tr + static_cast<size_t>(r0 + rr) * (2 * D) + D + cbase + c0);
+            acc[rr][0] = b.x; acc[rr][1] = b.y; acc[rr][2] = b.z; acc[rr][3] = b.w;
         }
         if (ahead)
             cp_async_wait_group<1>();
         else
             cp_async_wait_group<0>();
         __syncthreads();  // M_sg and S_in(sg) are in shared memory
-        const float *mrow = Ms + (sg & 1) * D * kCombineLd + r * kCombineLd;
+        const float *m0 = Ms + (sg & 1) * D * kCombineLd + r0 * kCombineLd;
+        const float *m1 = m0 + kCombineLd;
 #pragma unroll 4
-        for (int c = 0; c < D; c += 4) {
-            const float4 m4 = *reinterpret_cast<const float4 *>(mrow + c);
-            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+        for (int k = 0; k < D; k += 4) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(m0 + k);
+            const float4 a1 = *reinterpret_cast<const float4 *>(m1 + k);
+            const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-#pragma unroll
-                for (int x = 0; x < NX; x += 4) {
-                    const float4 sv = *reinterpret_cast<const float4 *>(Ss + (c + k) * CW + hx + x);
-                    acc[x] += mv[k] * sv.x;
-                    acc[x + 1] += mv[k] * sv.y;
-                    acc[x + 2] += mv[k] * sv.z;
-                    acc[x + 3] += mv[k] * sv.w;
-                }
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 sv = *reinterpret_cast<const float4 *>(Ss + (k + kk) * CW + c0);
+                acc[0][0] += av0[kk] * sv.x; acc[0][1] += av0[kk] * sv.y;
+                acc[0][2] += av0[kk] * sv.z; acc[0][3] += av0[kk] * sv.w;
+                acc[1][0] += av1[kk] * sv.x; acc[1][1] += av1[kk] * sv.y;
+                acc[1][2] += av1[kk] * sv.z; acc[1][3] += av1[kk] * sv.w;
             }
         }
         __syncthreads();  // every read of S_in(sg) and of M_sg is done
-        float *si = p.sc_si + unit(sg) * D * D + static_cast<size_t>(r) * D + c0 + hx;
 #pragma unroll
-        for (int x = 0; x < NX; x += 4) {
-            const float4 o = make_float4(acc[x], acc[x + 1], acc[x + 2], acc[x + 3]);
-            *reinterpret_cast<float4 *>(Ss + r * CW + hx + x) = o;
-            *reinterpret_cast<float4 *>(si + x) = o;
+        for (int rr = 0; rr < 2; ++rr) {
+            const float4 o = make_float4(acc[rr][0], acc[rr][1], acc[rr][2], acc[rr][3]);
+            *reinterpret_cast<float4 *>(Ss + (r0 + rr) * CW + c0) = o;
+            *reinterpret_cast<float4 *>(p.sc_si + unit(sg) * D * D + static_cast<size_t>(r0 + rr) * D + cbase + c0) = o;
         }
     }
 }
