@@ -103,11 +103,11 @@ bool shape_ok(const gdn2_dims &d) {
 // steps and a replay pass.  P is the minimum of a time model per chunk of the
 // longest pass, counted in waves of a GB300's 152 SMs (one CTA per SM):
 // 2.2 us for a 64-column tile, 2.3 us for a transition tile, 3.1 us for a
-// 128-column tile, 8 us per combine step and 10 us per launch, fitted to the
-// plain state kernel and the first combine.  The lookahead kernels and the
-// staged combine are faster by similar factors in every pass, and the P this
-// picks stays within 3 % of the best measured P on few-head shapes.
-// Segments keep at least 8 chunks.
+// 128-column tile and 10 us per launch, fitted to the plain state kernel
+// (the lookahead kernels are faster by similar factors in every pass), and
+// 3.5 us per step of the tensor-core combine.  On few-head shapes the P this
+// picks is the best measured one or within 3 % of it.  Segments keep at
+// least 8 chunks.
 int scan_segments(const gdn2_dims &d) {
     if (d.impl != GDN2_IMPL_TC || d.K != 128 || d.V != 128 || d.N <= 0) return 1;
     if (d.state_segments > 0) return d.state_segments;
@@ -122,7 +122,7 @@ int scan_segments(const gdn2_dims &d) {
     int best_P = 1;
     for (int64_t P = 2; P <= 16 && chunks >= 8 * P; ++P) {
         const double L = static_cast<double>((chunks + P - 1) / P);
-        const double t = 3 * 10.0 + 8.0 * (P - 1) + L * (2.3 * waves(2 * units * (P - 1)) + pass(P));
+        const double t = 3 * 10.0 + 3.5 * (P - 1) + L * (2.3 * waves(2 * units * (P - 1)) + pass(P));
         if (t < best) {
             best = t;
             best_P = static_cast<int>(P);

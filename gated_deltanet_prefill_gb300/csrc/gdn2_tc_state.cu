@@ -526,11 +526,193 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
     }
 }
 
+// The same combine on the tensor cores, one CTA per (sequence, value head,
+// 16 value columns) as above.  The CTA's product M_s S (128 x 128 x 16) is
+// three bf16 products with fp32 accumulation, M_hi S_hi + M_hi S_lo +
+// M_lo S_hi, where x_hi = bf16(x) and x_lo = bf16(x - x_hi): about 16
+// mantissa bits per operand, the fp32 combine's accuracy (the dropped
+// M_lo S_lo term is below 2^-16 of the product).  Both operands are K-major:
+// M as A (128 rows), the 16 state columns as B (16 rows, K = the 128 state
+// rows).  Per step: one thread issues the 24 MMAs; warps 0-3 (one TMEM lane
+// quarter each) add B_s to the product, write S_in(s + 1) and split it into
+// the next B operand; warps 4-7 copy M two steps ahead (per-thread 16-byte
+// asynchronous copies) and split M_{s + 1} into the next A operand.
+struct CombineTcCfg {
+    static constexpr uint32_t kRawLd = 528;            // bytes per raw M row: 512 + 16
+    static constexpr uint32_t kRaw = 128 * kRawLd;     // one raw M buffer
+    static constexpr uint32_t oMh = 2 * kRaw;          // A: [2 blocks of 64 K][128 rows][128 B]
+    static constexpr uint32_t oMl = oMh + 32768;
+    static constexpr uint32_t oSh = oMl + 32768;       // B: [2 blocks of 64 K][16 rows][128 B]
+    static constexpr uint32_t oSl = oSh + 4096;
+    static constexpr uint32_t kSmem = oSl + 4096 + 1024;  // + alignment slack
+    static constexpr uint32_t kTmemCols = 32;
+    static_assert(oMh % 1024 == 0, "128B-swizzle operands");
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ uint32_t split_bf(float x, float &lo) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    lo = x - __bfloat162float(h);
+    return static_cast<uint32_t>(__bfloat16_as_ushort(h));
+}
+
+__global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) {
+    using C = CombineTcCfg;
+    constexpr int D = 128, CW = 16;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ uint64_t mma_done;
+    __shared__ uint32_t tmem_slot;
+    if (p.status[0] != GDN2_OK) return;
+    const int n = blockIdx.x, hv = blockIdx.y, cbase = CW * blockIdx.z;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int P = p.sc_P, steps = P - 1;
+    const size_t sblk = (static_cast<size_t>(n) * p.HV + hv) * D * D;
+    auto unit = [&](int sg) { return (static_cast<size_t>(n) * (P - 1) + sg) * p.HV + hv; };
+    if (tid == 0) {
+        mbar_init(&mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tD = tmem_slot;
+    bool ok = true;
+    const int mt = tid - 128;  // warps 4-7: M's copies and splits, thread mt takes row mt
+    auto load_m = [&](int sg) {  // M_sg into raw buffer sg & 1 (warps 4-7)
+        const float *tr = p.sc_tr + unit(sg) * D * (2 * D);
+        uint8_t *dst = sm + (sg & 1) * C::kRaw;
+#pragma unroll 4
+        for (int i = mt; i < D * D / 4; i += 128) {
+            const int row = i / (D / 4), c4 = i % (D / 4);
+            cp_async16(dst + row * C::kRawLd + 16 * c4, tr + static_cast<size_t>(row) * (2 * D) + 4 * c4, 16);
+        }
+        cp_async_commit();
+    };
+    auto split_m = [&](int sg) {  // row mt of M_sg into the A operands
+        const float *row = reinterpret_cast<const float *>(sm + (sg & 1) * C::kRaw + mt * C::kRawLd);
+#pragma unroll 2
+        for (int c = 0; c < 16; ++c) {  // 8-column chunk c
+            const float4 a = *reinterpret_cast<const float4 *>(row + 8 * c);
+            const float4 b = *reinterpret_cast<const float4 *>(row + 8 * c + 4);
+            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            uint32_t h[4], l[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                h[e] = pack_bf2(v[2 * e], v[2 * e + 1]);
+                const float2 hb = unpack_bf2(h[e]);
+                l[e] = pack_bf2(v[2 * e] - hb.x, v[2 * e + 1] - hb.y);
+            }
+            const uint32_t off = (c / 8) * 16384u + swz(mt, c % 8);
+            *reinterpret_cast<uint4 *>(sm + C::oMh + off) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4 *>(sm + C::oMl + off) = make_uint4(l[0], l[1], l[2], l[3]);
+        }
+    };
+    // state row r (the K index), column j (0..15) of the B operands: row j of a
+    // K-major [16][128] tile, element r
+    auto put_s = [&](int r, int j, float x) {
+        float lo;
+        const uint32_t hi = split_bf(x, lo);
+        const uint32_t off = (r / 64) * 2048u + swz(j, (r % 64) / 8) + (r % 8) * 2;
+        *reinterpret_cast<unsigned short *>(sm + C::oSh + off) = static_cast<unsigned short>(hi);
+        *reinterpret_cast<unsigned short *>(sm + C::oSl + off) = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    };
+    {  // S_in(0): the initial state (or 0), two threads per row, 8 columns each
+        const int r = tid / 2, j0 = 8 * (tid % 2);
+#pragma unroll
+        for (int x = 0; x < 8; ++x)
+            put_s(r, j0 + x,
+                  p.h0 ? state_ld(p.h0, sblk + state_off(r, cbase + j0 + x, D, D, p.state_vmajor), p.state_bf16) : 0.f);
+    }
+    if (warp >= 4) {
+        load_m(0);
+        if (steps > 1) load_m(1);
+        if (steps > 1) cp_async_wait_group<1>(); else cp_async_wait_group<0>();
+        named_sync(1, 128);  // every copy of M_0 has landed
+        split_m(0);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    for (int s = 0; s < steps; ++s) {
+        const bool next = s + 1 < steps;
+        if (tid == 0) {
+            constexpr uint32_t id = idesc_bf16(128, CW, false, false);
+            const uint32_t mh = smem_u32(sm + C::oMh), ml = smem_u32(sm + C::oMl);
+            const uint32_t sh = smem_u32(sm + C::oSh), sl = smem_u32(sm + C::oSl);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_f16(tD, desc_kmajor(mh, 128, kk), desc_kmajor(sh, CW, kk), id, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) mma_f16(tD, desc_kmajor(mh, 128, kk), desc_kmajor(sl, CW, kk), id, 1);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) mma_f16(tD, desc_kmajor(ml, 128, kk), desc_kmajor(sh, CW, kk), id, 1);
+            mma_commit(&mma_done);
+        }
+        if (warp < 4) {
+            // S_in(s + 1) = M_s S_in(s) + B_s: row r of the product is TMEM lane r
+            const int r = 32 * warp + lane;
+            const float *brow = p.sc_tr + unit(s) * D * (2 * D) + static_cast<size_t>(r) * (2 * D) + D + cbase;
+            float bv[CW];
+#pragma unroll
+            for (int x = 0; x < CW; x += 4) {
+                const float4 b = *reinterpret_cast<const float4 *>(brow + x);
+                bv[x] = b.x; bv[x + 1] = b.y; bv[x + 2] = b.z; bv[x + 3] = b.w;
+            }
+            if (!warp_wait(&mma_done, s & 1)) ok = false;
+            tc_fence_after();
+            uint32_t acc[16];
+            tmem_ld16(tD + (static_cast<uint32_t>(32 * warp) << 16), acc);
+            tmem_ld_wait();
+            float v[CW];
+#pragma unroll
+            for (int x = 0; x < CW; ++x) v[x] = __uint_as_float(acc[x]) + bv[x];
+            float *si = p.sc_si + unit(s) * D * D + static_cast<size_t>(r) * D + cbase;
+#pragma unroll
+            for (int x = 0; x < CW; x += 4) *reinterpret_cast<float4 *>(si + x) = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+            if (next) {
+#pragma unroll
+                for (int x = 0; x < CW; ++x) put_s(r, x, v[x]);
+            }
+        } else if (next) {
+            if (s + 2 < steps) load_m(s + 2);  // raw buffer s & 1 was split in the previous step
+            if (!mbar_wait(&mma_done, s & 1)) ok = false;  // the A operands are read
+            if (s + 2 < steps) cp_async_wait_group<1>(); else cp_async_wait_group<0>();
+            named_sync(1, 128);  // every copy of M_{s+1} has landed
+            split_m(s + 1);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    }
+    if (!ok) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc(tD, C::kTmemCols);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_tc_scan_combine(const Params &p, cudaStream_t s) {
     constexpr int CW = 16;
     if (p.N <= 0 || p.sc_P <= 1) return cudaSuccess;
+    // the tensor-core combine; GDN2_SCAN_COMBINE=cuda keeps the CUDA-core one
+    const char *cmb = getenv("GDN2_SCAN_COMBINE");
+    if (!(cmb && cmb[0] == 'c')) {
+        const cudaError_t e = cudaFuncSetAttribute(gdn2_scan_combine_tc_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(CombineTcCfg::kSmem));
+        if (e != cudaSuccess) return e;
+        gdn2_scan_combine_tc_kernel<<<dim3(p.N, p.HV, 128 / CW), 256, CombineTcCfg::kSmem, s>>>(p);
+        return cudaGetLastError();
+    }
     const cudaError_t e = cudaFuncSetAttribute(gdn2_scan_combine_kernel<CW>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(combine_smem<CW>()));

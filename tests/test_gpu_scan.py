@@ -67,6 +67,28 @@ def test_forced_segments_plain_kernel(cuda_lib, monkeypatch, segments):
     assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
 
 
+@pytest.mark.parametrize("combine", ["cuda", "tc"])
+def test_combine_kernels(cuda_lib, monkeypatch, combine):
+    """Both combine kernels (the tensor-core one by default, the CUDA-core
+    one with GDN2_SCAN_COMBINE=cuda) at 9 segments (8 dependent steps), with
+    slow decay so that every step's M S_in term matters, and a bf16 V-major
+    initial state read by the first step."""
+    if combine == "cuda":
+        monkeypatch.setenv("GDN2_SCAN_COMBINE", "cuda")
+    wl = inputs.small("comb", [1500, 700], H=2, HV=2, K=128, V=128, g_max=0.02, beta_max=1.0, h0_std=0.5,
+                      seed=74)
+    d = inputs.generate(wl)
+    d["h0"] = d["h0"].to(torch.bfloat16)
+    o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                                       initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
+    dd = dict(d)
+    dd["h0"] = d["h0"].transpose(-1, -2).contiguous()  # V-major
+    o, hT = run(cuda_lib, dd, 9, state_v_major=True)
+    hT = hT.float().transpose(-1, -2)
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
+
+
 def test_automatic_segments(cuda_lib):
     """A few long heads: the library picks P > 1 (visible in the launch
     count) and the result matches the oracle."""
