@@ -161,6 +161,7 @@ WsLayout workspace_layout(const gdn2_dims &d) {
             const size_t units = static_cast<size_t>(d.N) * (P - 1) * HS;
             L.sc_tr = take(units * d.K * (d.K + d.V) * 4);
             L.sc_si = take(units * d.K * d.V * 4);
+            L.sc_mimg = take(units * d.K * d.K * 4);  // hi and lo bf16 parts of M
         }
     }
     L.total = off;
@@ -435,6 +436,7 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
     p.sc_mode = 0;
     p.sc_tr = p.sc_P > 1 ? reinterpret_cast<float *>(ws + L.sc_tr) : nullptr;
     p.sc_si = p.sc_P > 1 ? reinterpret_cast<float *>(ws + L.sc_si) : nullptr;
+    p.sc_mimg = p.sc_P > 1 ? reinterpret_cast<uint8_t *>(ws + L.sc_mimg) : nullptr;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         cudaGetLastError();

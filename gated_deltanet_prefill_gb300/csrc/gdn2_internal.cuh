@@ -68,9 +68,13 @@ struct Params {
     // chunks in sc_P segments.  sc_mode 0: one sequential pass (sc_P = 1);
     // 1: segment transitions [M | B] of S_out = M S_in + B for segments
     // 0 .. P-2 into sc_tr [N, P-1, HV, K, K+V]; 2: every segment from its
-    // incoming state (h0, or sc_si [N, P-1, HV, K, V] from the combine kernel)
+    // incoming state (h0, or sc_si [N, P-1, HV, K, V] from the combine kernel).
+    // sc_mimg [N, P-1, HV]: each transition's M split into bf16 hi and lo parts,
+    // as K-major 128B-swizzled operand images (64 KB each; written by the
+    // lookahead transitions, read by the tensor-core combine)
     int sc_P, sc_mode;
     float *sc_tr, *sc_si;
+    uint8_t *sc_mimg;
     // TMA tensor maps over the rows of g, v, w (tensor-core intra kernel): a
     // box is 64 tokens x D channels of one head.  tm_order = 0: coordinates
     // (channel, head, token); 1: (channel, token, head).  tmap = 0: the maps
@@ -88,7 +92,7 @@ struct Params {
 // Workspace layout (byte offsets), a function of the problem only.
 struct WsLayout {
     size_t status, chunk_seq, chunk_len, chunk_start, seq_first, seq_order, G, qn, kn, Wt, Ut, hbuf, vnew, rec,
-        exact_list, sc_tr, sc_si;
+        exact_list, sc_tr, sc_si, sc_mimg;
     size_t total;
 };
 

@@ -532,21 +532,18 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
 // M_lo S_hi, where x_hi = bf16(x) and x_lo = bf16(x - x_hi): about 16
 // mantissa bits per operand, the fp32 combine's accuracy (the dropped
 // M_lo S_lo term is below 2^-16 of the product).  Both operands are K-major:
-// M as A (128 rows), the 16 state columns as B (16 rows, K = the 128 state
-// rows).  Per step: one thread issues the 24 MMAs; warps 0-3 (one TMEM lane
-// quarter each) add B_s to the product, write S_in(s + 1) and split it into
-// the next B operand; warps 4-7 copy M two steps ahead (per-thread 16-byte
-// asynchronous copies) and split M_{s + 1} into the next A operand.
+// M as A (128 rows; the transitions write its hi and lo images, sc_mimg),
+// the 16 state columns as B (16 rows, K = the 128 state rows).  Per step:
+// one thread issues the 24 MMAs; warps 0-3 (one TMEM lane quarter each) add
+// B_s to the product, write S_in(s + 1) and split it into the next B
+// operand; warps 4-7 copy the M images two steps ahead (per-thread 16-byte
+// asynchronous copies into two buffers).
 struct CombineTcCfg {
-    static constexpr uint32_t kRawLd = 528;            // bytes per raw M row: 512 + 16
-    static constexpr uint32_t kRaw = 128 * kRawLd;     // one raw M buffer
-    static constexpr uint32_t oMh = 2 * kRaw;          // A: [2 blocks of 64 K][128 rows][128 B]
-    static constexpr uint32_t oMl = oMh + 32768;
-    static constexpr uint32_t oSh = oMl + 32768;       // B: [2 blocks of 64 K][16 rows][128 B]
+    static constexpr uint32_t kMimg = 65536;           // hi (32 KB) then lo: [2 blocks of 64 K][128 rows][128 B]
+    static constexpr uint32_t oSh = 2 * kMimg;         // B: [2 blocks of 64 K][16 rows][128 B]
     static constexpr uint32_t oSl = oSh + 4096;
     static constexpr uint32_t kSmem = oSl + 4096 + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 32;
-    static_assert(oMh % 1024 == 0, "128B-swizzle operands");
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
@@ -582,35 +579,12 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
     tc_fence_after();
     const uint32_t tD = tmem_slot;
     bool ok = true;
-    const int mt = tid - 128;  // warps 4-7: M's copies and splits, thread mt takes row mt
-    auto load_m = [&](int sg) {  // M_sg into raw buffer sg & 1 (warps 4-7)
-        const float *tr = p.sc_tr + unit(sg) * D * (2 * D);
-        uint8_t *dst = sm + (sg & 1) * C::kRaw;
+    auto load_m = [&](int sg) {  // the M_sg images into buffer sg & 1 (warps 4-7)
+        const uint8_t *src = p.sc_mimg + unit(sg) * C::kMimg;
+        uint8_t *dst = sm + (sg & 1) * C::kMimg;
 #pragma unroll 4
-        for (int i = mt; i < D * D / 4; i += 128) {
-            const int row = i / (D / 4), c4 = i % (D / 4);
-            cp_async16(dst + row * C::kRawLd + 16 * c4, tr + static_cast<size_t>(row) * (2 * D) + 4 * c4, 16);
-        }
+        for (int i = tid - 128; i < static_cast<int>(C::kMimg / 16); i += 128) cp_async16(dst + 16 * i, src + 16 * i, 16);
         cp_async_commit();
-    };
-    auto split_m = [&](int sg) {  // row mt of M_sg into the A operands
-        const float *row = reinterpret_cast<const float *>(sm + (sg & 1) * C::kRaw + mt * C::kRawLd);
-#pragma unroll 2
-        for (int c = 0; c < 16; ++c) {  // 8-column chunk c
-            const float4 a = *reinterpret_cast<const float4 *>(row + 8 * c);
-            const float4 b = *reinterpret_cast<const float4 *>(row + 8 * c + 4);
-            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            uint32_t h[4], l[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                h[e] = pack_bf2(v[2 * e], v[2 * e + 1]);
-                const float2 hb = unpack_bf2(h[e]);
-                l[e] = pack_bf2(v[2 * e] - hb.x, v[2 * e + 1] - hb.y);
-            }
-            const uint32_t off = (c / 8) * 16384u + swz(mt, c % 8);
-            *reinterpret_cast<uint4 *>(sm + C::oMh + off) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4 *>(sm + C::oMl + off) = make_uint4(l[0], l[1], l[2], l[3]);
-        }
     };
     // state row r (the K index), column j (0..15) of the B operands: row j of a
     // K-major [16][128] tile, element r
@@ -632,18 +606,16 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
         load_m(0);
         if (steps > 1) load_m(1);
         if (steps > 1) cp_async_wait_group<1>(); else cp_async_wait_group<0>();
-        named_sync(1, 128);  // every copy of M_0 has landed
-        split_m(0);
     }
     fence_proxy_async();
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // M_0's images (each thread's own copies waited for) and S_in(0) are in place
     tc_fence_after();
     for (int s = 0; s < steps; ++s) {
         const bool next = s + 1 < steps;
         if (tid == 0) {
             constexpr uint32_t id = idesc_bf16(128, CW, false, false);
-            const uint32_t mh = smem_u32(sm + C::oMh), ml = smem_u32(sm + C::oMl);
+            const uint32_t mh = smem_u32(sm + (s & 1) * C::kMimg), ml = mh + 32768;
             const uint32_t sh = smem_u32(sm + C::oSh), sl = smem_u32(sm + C::oSl);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
@@ -680,11 +652,15 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
                 for (int x = 0; x < CW; ++x) put_s(r, x, v[x]);
             }
         } else if (next) {
-            if (s + 2 < steps) load_m(s + 2);  // raw buffer s & 1 was split in the previous step
-            if (!mbar_wait(&mma_done, s & 1)) ok = false;  // the A operands are read
-            if (s + 2 < steps) cp_async_wait_group<1>(); else cp_async_wait_group<0>();
-            named_sync(1, 128);  // every copy of M_{s+1} has landed
-            split_m(s + 1);
+            // M_{s+2} into the buffer M_s leaves once its products are done;
+            // then this thread's copies of M_{s+1} must have landed
+            if (s + 2 < steps) {
+                if (!mbar_wait(&mma_done, s & 1)) ok = false;
+                load_m(s + 2);
+                cp_async_wait_group<1>();
+            } else {
+                cp_async_wait_group<0>();
+            }
         }
         fence_proxy_async();
         tc_fence_before();
@@ -700,12 +676,21 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
 
 }  // namespace
 
+// The 128-column lookahead kernel runs unless GDN2_STATE_LOOKAHEAD is 0 or 64
+// (the plain kernel, for comparison).
+bool lookahead128_on() {
+    const char *la = getenv("GDN2_STATE_LOOKAHEAD");
+    return !(la && (la[0] == '0' || (la[0] == '6' && la[1] == '4')));
+}
+
 cudaError_t launch_tc_scan_combine(const Params &p, cudaStream_t s) {
     constexpr int CW = 16;
     if (p.N <= 0 || p.sc_P <= 1) return cudaSuccess;
-    // the tensor-core combine; GDN2_SCAN_COMBINE=cuda keeps the CUDA-core one
+    // the tensor-core combine reads the M images the lookahead transitions
+    // write; GDN2_SCAN_COMBINE=cuda (or the plain state kernel) keeps the
+    // CUDA-core one
     const char *cmb = getenv("GDN2_SCAN_COMBINE");
-    if (!(cmb && cmb[0] == 'c')) {
+    if (!(cmb && cmb[0] == 'c') && lookahead128_on()) {
         const cudaError_t e = cudaFuncSetAttribute(gdn2_scan_combine_tc_kernel,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(CombineTcCfg::kSmem));
@@ -727,7 +712,7 @@ cudaError_t launch_tc_state(const Params &p, cudaStream_t s) {
     // lookahead kernels (GDN2_STATE_LOOKAHEAD=0 selects the plain kernel for
     // both tile widths, =64 for 128-column tiles only; for comparison)
     const char *la = getenv("GDN2_STATE_LOOKAHEAD");
-    const bool la_off = la && la[0] == '0', la128_off = la_off || (la && la[0] == '6' && la[1] == '4');
+    const bool la_off = la && la[0] == '0', la128_off = !lookahead128_on();
     if (p.vtile == 64 && p.sc_mode != 1 && !la_off) return launch_tc_state_la(p, s);
     if (p.vtile == 128 && !la128_off) return launch_tc_state_la128(p, s);
     if (p.sc_mode != 0)

@@ -830,13 +830,31 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
                     load_h0(2 * g2 + h, r);
                 }
                 if (SCAN && trans) {
-                    float *tr = p.sc_tr + ((static_cast<size_t>(n) * (P - 1) + seg) * p.HV + hv) * D * (2 * D) +
-                                static_cast<size_t>(row) * (2 * D) + tile * D + col0;
+                    const size_t u = (static_cast<size_t>(n) * (P - 1) + seg) * p.HV + hv;
+                    float *tr = p.sc_tr + u * D * (2 * D) + static_cast<size_t>(row) * (2 * D) + tile * D + col0;
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
                         *reinterpret_cast<float4 *>(tr + e) = make_float4(
                             __uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
                             __uint_as_float(r[e + 3]));
+                    if (is_m) {  // M's bf16 hi and lo parts as the combine's A operand images (row = M row)
+                        uint8_t *img = p.sc_mimg + u * (2 * 32768);
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            uint32_t hi[4], lo[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float a = __uint_as_float(r[8 * cc + 2 * e]), b = __uint_as_float(r[8 * cc + 2 * e + 1]);
+                                hi[e] = pack_bf2(a, b);
+                                const float2 hb = unpack_bf2(hi[e]);
+                                lo[e] = pack_bf2(a - hb.x, b - hb.y);
+                            }
+                            const int chunk = col0 / 8 + cc;  // 8-column chunk of the K index
+                            const uint32_t off = (chunk / 8) * 16384u + swz(row, chunk % 8);
+                            *reinterpret_cast<uint4 *>(img + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                            *reinterpret_cast<uint4 *>(img + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                        }
+                    }
                 } else if (plain) {
                     float *hT = static_cast<float *>(p.hT) + sblk + static_cast<size_t>(row) * D + col0;
 #pragma unroll
