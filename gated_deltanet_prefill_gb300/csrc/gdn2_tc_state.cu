@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
     constexpr int D = 128, CW = 16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t mma_done;
+    __shared__ uint64_t mma_done, drain;
     __shared__ uint32_t tmem_slot;
     if (p.status[0] != GDN2_OK) return;
     const int n = blockIdx.x, hv = blockIdx.y, cbase = CW * blockIdx.z;
@@ -568,6 +568,7 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
     auto unit = [&](int sg) { return (static_cast<size_t>(n) * (P - 1) + sg) * p.HV + hv; };
     if (tid == 0) {
         mbar_init(&mma_done, 1);
+        mbar_init(&drain, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -667,7 +668,16 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
         __syncthreads();
         tc_fence_after();
     }
+    // every MMA has completed before Tensor Memory is released (after a timed
+    // out wait one may still run)
+    if (tid == 0) {
+        mma_commit(&drain);
+        if (!mbar_wait(&drain, 0)) ok = false;
+    }
     if (!ok) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     if (warp == 1) {
         __syncwarp();
         tmem_dealloc(tD, C::kTmemCols);
