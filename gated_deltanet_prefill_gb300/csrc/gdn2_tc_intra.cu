@@ -942,6 +942,12 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     tc_fence_after();
     }  // items
     report_range(p.status, half_clipped(hmax));
+    // every MMA has completed before Tensor Memory is released (after a timed
+    // out wait one may still run); each item completed two phases of bar_mma
+    if (tid == 0) {
+        mma_commit(&bar_mma);
+        if (!mbar_wait(&bar_mma, 0)) atomicExch(p.status + 2, static_cast<int>(GDN2_ERR_TIMEOUT));
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
