@@ -89,6 +89,27 @@ def test_combine_kernels(cuda_lib, monkeypatch, combine):
     assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
 
 
+@pytest.mark.parametrize("segments", [3, 5])
+def test_segments_with_head_counts_fp16_l2norm(cuda_lib, segments):
+    """The chunk-parallel pass with more query than value heads and fewer key
+    heads (H = 4, HK = HV = 2: four state heads), fp16 q/k/v/w/beta, the
+    fused L2 norm and an initial state; 64-column replay tiles at P = 3,
+    128-column ones at P = 5."""
+    wl = inputs.small("scanheads", [900, 2000, 1], H=4, HV=4, K=128, V=128, g_max=0.3, beta_max=2.0,
+                      h0_std=0.05, seed=75)
+    d = inputs.generate(wl)
+    d["k"] = d["k"][:, :2].contiguous()
+    d["v"] = d["v"][:, :2].contiguous()
+    for key in ("q", "k", "v", "beta", "w"):
+        d[key] = (d[key].float() * (2.0 if key == "q" else 1.0)).to(torch.float16)
+    o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                                       initial_state=d["h0"], cu_seqlens=d["cu_seqlens"], use_qk_l2norm=True)
+    o, hT = run(cuda_lib, d, segments, use_qk_l2norm=True)
+    assert o.shape == o_ref.shape and hT.shape == h_ref.shape
+    assert rel_max(o.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
+
+
 def test_automatic_segments(cuda_lib):
     """A few long heads: the library picks P > 1 (visible in the launch
     count) and the result matches the oracle."""
