@@ -72,6 +72,35 @@ def test_writes_stay_inside_outputs_and_workspace(cuda_lib, impl, D):
     assert rel_max(fs.t.cpu().numpy(), h_ref) <= 1e-2
 
 
+def test_chunk_parallel_writes_stay_inside(cuda_lib):
+    """The same check for the chunk-parallel state pass (transitions with
+    their M operand images, the tensor-core combine, the replay), 4
+    segments."""
+    wl = inputs.small("canary_scan", [900, 1, 700], H=2, HV=2, K=128, V=128, g_max=0.3, beta_max=2.0,
+                      h0_std=0.05, seed=84)
+    d = inputs.generate(wl)
+    ins = {k: Padded(tuple(v.shape), v.dtype, v.cuda()) for k, v in d.items() if torch.is_tensor(v)}
+    before = {k: p.raw.clone() for k, p in ins.items()}
+    out = Padded((wl.T_tot, wl.HV, wl.V), torch.bfloat16)
+    fs = Padded((wl.N, wl.HV, wl.K, wl.V), torch.float32)
+    args = [ins[k].t for k in ("q", "k", "v", "g", "beta", "w")]
+    dims = gdn2.make_dims(*args, out.t, ins["cu_seqlens"].t)
+    dims.state_segments = 4
+    ws = Padded((gdn2.workspace_bytes(dims),), torch.uint8)
+    cuda_lib.chunk_gdn2_fwd(*args, scale=d["scale"], initial_state=ins["h0"].t, cu_seqlens=ins["cu_seqlens"].t,
+                            out=out.t, final_state=fs.t, workspace=ws.t, state_segments=4)
+    torch.cuda.synchronize()
+    assert cuda_lib.device_status(ws.t) == 0
+    for k, p in ins.items():
+        assert torch.equal(p.raw, before[k]), "input %s was written" % k
+    for name, p in (("out", out), ("final_state", fs), ("workspace", ws)):
+        assert p.pads_intact(), "a write landed outside %s" % name
+    o_ref, h_ref = oracle.gdn2_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
+                                       initial_state=d["h0"], cu_seqlens=d["cu_seqlens"])
+    assert rel_max(out.t.float().cpu().numpy(), o_ref) <= 1e-2
+    assert rel_max(fs.t.cpu().numpy(), h_ref) <= 1e-2
+
+
 def test_exact_pass_writes_stay_inside(cuda_lib):
     """The same check with decays of up to 30 nats per token, so that the
     intra kernel's exact pass rewrites records."""
