@@ -530,8 +530,9 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
 // 16 value columns) as above.  The CTA's product M_s S (128 x 128 x 16) is
 // three bf16 products with fp32 accumulation, M_hi S_hi + M_hi S_lo +
 // M_lo S_hi, where x_hi = bf16(x) and x_lo = bf16(x - x_hi): about 16
-// mantissa bits per operand, the fp32 combine's accuracy (the dropped
-// M_lo S_lo term is below 2^-16 of the product).  Both operands are K-major:
+// mantissa bits per operand, far finer than the fp16 operand rounding the
+// state pass applies at every chunk (the dropped M_lo S_lo term is below
+// 2^-16 of the product).  Both operands are K-major:
 // M as A (128 rows; the transitions write its hi and lo images, sc_mimg),
 // the 16 state columns as B (16 rows, K = the 128 state rows).  Per step:
 // one thread issues the 24 MMAs; warps 0-3 (one TMEM lane quarter each) add
