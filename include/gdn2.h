@@ -138,9 +138,10 @@ typedef struct gdn2_dims {
  * state_segments (tensor-core path, K = V = 128): P > 1 splits each
  * sequence's chunks into P segments of ceil(chunks / P).  Every segment's
  * state map is affine, S_out = M S_in + B; the library computes [M | B] for
- * segments 0 .. P - 2 in parallel, combines them in order (fp32) into each
- * segment's incoming state, then replays all segments in parallel for o and
- * the final state.  This shortens the sequential chain for few (sequence,
+ * segments 0 .. P - 2 in parallel, combines them in order into each
+ * segment's incoming state (fp32 accumulation of products whose operands
+ * are split into bf16 high and low parts, about 16 mantissa bits each),
+ * then replays all segments in parallel for o and the final state.  This shortens the sequential chain for few (sequence,
  * head) pairs on long sequences (the FlashInfer docs, output_state: the
  * cuDNN engine splits one sequence across CTAs).  0 = the library chooses
  * P from a time model of the passes (P > 1 only for few (sequence, head)
