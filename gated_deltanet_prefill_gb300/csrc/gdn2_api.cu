@@ -286,6 +286,11 @@ gdn2_status check_args(const void *q, const void *k, const void *v, const void *
     return GDN2_OK;
 }
 
+bool pdl_on() {
+    const char *e = getenv("GDN2_PDL");
+    return !(e && e[0] == '0');
+}
+
 bool device_is_sm103(int *dev_out) {
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||

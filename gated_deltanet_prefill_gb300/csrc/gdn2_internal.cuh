@@ -175,6 +175,36 @@ __device__ __forceinline__ int64_t cu_at(const Params &p, int i) {
                   : static_cast<int64_t>(static_cast<const int32_t *>(p.cu)[i]);
 }
 
+// Programmatic dependent launches.  A forward call is a chain of kernels in
+// one stream; each kernel after the first is launched with the programmatic
+// serialization attribute, so it may be scheduled while its predecessor
+// drains and the launch gap between them disappears.  Every kernel of a chain
+// executes pdl_wait() in every thread before its first global access: the
+// wait returns once the predecessor grid has completed and its writes are
+// visible, and since the predecessor waited the same way, so have all earlier
+// kernels of the chain.  pdl_trigger() allows the successor to be launched
+// before this grid ends.  Both are no-ops for a kernel launched without the
+// attribute.  GDN2_PDL=0 launches every kernel plainly (for comparison).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+bool pdl_on();
+// Launch kern(p) as the next kernel of a chain (see above).
+template <typename P>
+cudaError_t launch_chained(void (*kern)(P), dim3 grid, dim3 block, size_t smem, cudaStream_t s, const P &p) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_on() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Launchers (each returns cudaGetLastError() of its launches).
 cudaError_t launch_chunk_map(const Params &p, cudaStream_t s);
 cudaError_t launch_prep(const Params &p, cudaStream_t s);

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(kMapThreads) gdn2_chunk_map_kernel(Params p) {
     __shared__ int s_pos[kMapThreads];  // chunk-count buckets of the sequence order
     __shared__ int s_first[kSeqCache];  // seq_first[0 .. N] when N < kSeqCache
     const int tid = threadIdx.x;
+    pdl_trigger();  // the chain's first kernel: the intra kernel may launch now and waits for this one
     if (tid == 0) {
         s_bad = 0;
         p.status[2] = GDN2_OK;

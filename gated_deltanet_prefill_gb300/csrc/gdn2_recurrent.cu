@@ -50,6 +50,7 @@ __device__ __forceinline__ int64_t rec_cu(const RecParams &p, int i) {
 // a bad cu_seqlens turns the recurrence kernel into a no-op.
 __global__ void __launch_bounds__(256) gdn2_recurrent_check_kernel(RecParams p) {
     __shared__ int bad;
+    pdl_trigger();  // the step kernel may launch now; it waits for this one
     if (threadIdx.x == 0) {
         bad = rec_cu(p, 0) != 0 || rec_cu(p, p.N) != p.T_tot;
         p.status[1] = 0;
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(K) gdn2_recurrent_kernel(RecParams p) {
     __shared__ float s_k[K], s_bk[K], s_q[K], s_eg[K];
     __shared__ float s_part[2][W][32];
     __shared__ float s_red[3][W];
+    pdl_wait();  // the check kernel's status is complete
     if (p.status[0] != GDN2_OK) return;
     const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
     const int n = blockIdx.x, hv = blockIdx.y, j = 32 * blockIdx.z + lane;
@@ -214,11 +216,13 @@ gdn2_status gdn2_recurrent_fwd(const void *q, const void *k, const void *v, cons
     if (d->N > 0) {
         const dim3 grid(d->N, p.HV, d->V / 32);
         const bool gen = p.in_f16 || p.g_dtype != GDN2_DTYPE_F32 || p.state_vmajor || p.state_bf16;
-        if (d->K == 64)
-            (gen ? gdn2_recurrent_kernel<64, true> : gdn2_recurrent_kernel<64, false>)<<<grid, 64, 0, s>>>(p);
-        else
-            (gen ? gdn2_recurrent_kernel<128, true> : gdn2_recurrent_kernel<128, false>)<<<grid, 128, 0, s>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return GDN2_ERR_LAUNCH;
+        const cudaError_t e =
+            d->K == 64
+                ? launch_chained(gen ? gdn2_recurrent_kernel<64, true> : gdn2_recurrent_kernel<64, false>, grid,
+                                 dim3(64), 0, s, p)
+                : launch_chained(gen ? gdn2_recurrent_kernel<128, true> : gdn2_recurrent_kernel<128, false>, grid,
+                                 dim3(128), 0, s, p);
+        if (e != cudaSuccess) return GDN2_ERR_LAUNCH;
     }
     return GDN2_OK;
 }

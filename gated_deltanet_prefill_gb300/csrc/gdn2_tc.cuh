@@ -316,11 +316,16 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
     return r;
 }
-// The same conversion, tracking in m the largest fp16 magnitude written (two
-// 16-bit lanes, sign bits cleared; unsigned order of those bit patterns is the
-// order of the magnitudes).  A lane at 0x7bff (65504, where the conversion
-// saturates) or above (inf, NaN) means a value was clipped: the kernel then
-// reports GDN2_ERR_RANGE in the device status instead of returning it silently.
+// The same conversion, tracking in m the largest fp16 magnitude written, so
+// that a clipped value can be reported: a lane whose magnitude bits are 0x7bff
+// (65504, where the conversion saturates) or above (inf, NaN) means a value was
+// clipped, and the kernel then reports GDN2_ERR_RANGE in the device status
+// instead of returning it silently.  Two forms, each where it measured faster:
+//  - pack_h2m: the sign bits cleared, then a 16-bit unsigned max (two integer
+//    instructions; the state kernels, whose epilogues keep the fp16 units busy);
+//  - pack_h2mh: one packed fp16 maximum of the magnitudes (max.xorsign.abs,
+//    whose sign is the xor of the operands' signs and is ignored; NaN
+//    propagated; the intra kernel, which is bound by its instruction count).
 __device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -331,8 +336,14 @@ __device__ __forceinline__ uint32_t pack_h2m(float a, float b, uint32_t &m) {
     m = umax16x2(m, r & 0x7fff7fffu);
     return r;
 }
+__device__ __forceinline__ uint32_t pack_h2mh(float a, float b, uint32_t &m) {
+    const uint32_t r = pack_h2(a, b);
+    asm("max.NaN.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(m) : "r"(m), "r"(r));
+    return r;
+}
+// either form's m: magnitude bits of each lane at or past the clipping point
 __device__ __forceinline__ bool half_clipped(uint32_t m) {
-    return (m & 0xffffu) >= 0x7bffu || (m >> 16) >= 0x7bffu;
+    return (m & 0x7fffu) >= 0x7bffu || ((m >> 16) & 0x7fffu) >= 0x7bffu;
 }
 // a -> low half, IEEE round-to-nearest (overflow gives inf, as a cast would)
 __device__ __forceinline__ uint32_t pack_f16_rn(float a, float b) {
@@ -352,9 +363,9 @@ __device__ __forceinline__ float2 unpack_bf2(uint32_t x) {
 __device__ __forceinline__ uint4 pack8_h(const float (&f)[8]) {
     return make_uint4(pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
 }
-__device__ __forceinline__ uint4 pack8_hm(const float (&f)[8], uint32_t &m) {
-    return make_uint4(pack_h2m(f[0], f[1], m), pack_h2m(f[2], f[3], m), pack_h2m(f[4], f[5], m),
-                      pack_h2m(f[6], f[7], m));
+__device__ __forceinline__ uint4 pack8_hm(const float (&f)[8], uint32_t &m) {  // pack_h2mh's tracking
+    return make_uint4(pack_h2mh(f[0], f[1], m), pack_h2mh(f[2], f[3], m), pack_h2mh(f[4], f[5], m),
+                      pack_h2mh(f[6], f[7], m));
 }
 __device__ __forceinline__ uint4 pack8_bf(const float (&f)[8]) {
     return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));

@@ -272,11 +272,18 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     const int seg = tid % 4;
     const int t = 8 * warp + (((lane >> 2) & 1) << 2) + (lane >> 3);
     const int I = t / 16;
-    // The exact pass is launched as a programmatic dependent of the first one
-    // (it may start while the first pass drains); it waits here until the
-    // first pass has completed and its exact list is visible.
-    if (EXACT) asm volatile("griddepcontrol.wait;" ::: "memory");
-    else asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Both passes are programmatic dependents of the kernel before them: the
+    // first pass of the chunk map, the exact pass of the first pass (the exact
+    // list).  Each waits here until its predecessor has completed.  The first
+    // pass lets the exact pass launch at once (its CTAs wait for this grid);
+    // the exact pass lets the state kernel launch once the first pass is done.
+    if (EXACT) {
+        pdl_wait();
+        pdl_trigger();
+    } else {
+        pdl_trigger();
+        pdl_wait();
+    }
     // (chunk, state head) items: all of them, or the exact list
     const int total = p.status[0] != GDN2_OK ? 0 : EXACT ? p.status[4] : p.status[1] * p.HV;
     if (static_cast<int>(blockIdx.x) >= total) return;  // before any barrier or TMEM allocation
@@ -660,9 +667,9 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
                 wr0[x2] = pack_bf2(r0[a], r0[a + 1]);
                 wr2[x2] = pack_bf2(r2[a], r2[a + 1]);
                 wr3[x2] = pack_bf2(r3[a], r3[a + 1]);
-                wX1[x2] = pack_h2m(x1[a], x1[a + 1], hmax);
-                wQe[x2] = pack_h2m(qe[a], qe[a + 1], hmax);
-                wKd[x2] = pack_h2m(kd[a], kd[a + 1], hmax);
+                wX1[x2] = pack_h2mh(x1[a], x1[a + 1], hmax);
+                wQe[x2] = pack_h2mh(qe[a], qe[a + 1], hmax);
+                wKd[x2] = pack_h2mh(kd[a], kd[a + 1], hmax);
             }
         }
         auto u4 = [](const uint32_t (&w)[4]) { return make_uint4(w[0], w[1], w[2], w[3]); };
@@ -831,7 +838,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
             const int o = d ? r0 : c0;
             const float2 tv = *reinterpret_cast<const float2 *>(Tf + (o + i) * kLD + o + j0);
             *reinterpret_cast<uint32_t *>(timg + swz(o + i, (o + j0) / 8) + ((o + j0) % 8) * 2) =
-                pack_h2m(tv.x, tv.y, hmax);
+                pack_h2mh(tv.x, tv.y, hmax);
         }
         __syncthreads();
         float z0 = 0.f, z1 = 0.f;
@@ -847,7 +854,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
             }
         }
         *reinterpret_cast<float2 *>(Tf + (r0 + i) * kLD + c0 + j0) = make_float2(z0, z1);
-        *reinterpret_cast<uint32_t *>(timg + swz(r0 + i, (c0 + j0) / 8) + ((c0 + j0) % 8) * 2) = pack_h2m(z0, z1, hmax);
+        *reinterpret_cast<uint32_t *>(timg + swz(r0 + i, (c0 + j0) / 8) + ((c0 + j0) % 8) * 2) = pack_h2mh(z0, z1, hmax);
     }
     __syncthreads();
     // 32 -> 64 merge on the 32 x 32 halves a (rows/cols 0-31) and b (32-63):
@@ -885,8 +892,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         }
         *reinterpret_cast<float2 *>(Tf + (32 + i0) * kLD + j0) = make_float2(z00, z01);
         *reinterpret_cast<float2 *>(Tf + (33 + i0) * kLD + j0) = make_float2(z10, z11);
-        *reinterpret_cast<uint32_t *>(timg + swz(32 + i0, j0 / 8) + (j0 % 8) * 2) = pack_h2m(z00, z01, hmax);
-        *reinterpret_cast<uint32_t *>(timg + swz(33 + i0, j0 / 8) + (j0 % 8) * 2) = pack_h2m(z10, z11, hmax);
+        *reinterpret_cast<uint32_t *>(timg + swz(32 + i0, j0 / 8) + (j0 % 8) * 2) = pack_h2mh(z00, z01, hmax);
+        *reinterpret_cast<uint32_t *>(timg + swz(33 + i0, j0 / 8) + (j0 % 8) * 2) = pack_h2mh(z10, z11, hmax);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -924,10 +931,10 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const uint32_t *w = v + 8 * cc;
-                const uint4 o = make_uint4(pack_h2m(__uint_as_float(w[0]), __uint_as_float(w[1]), hmax),
-                                           pack_h2m(__uint_as_float(w[2]), __uint_as_float(w[3]), hmax),
-                                           pack_h2m(__uint_as_float(w[4]), __uint_as_float(w[5]), hmax),
-                                           pack_h2m(__uint_as_float(w[6]), __uint_as_float(w[7]), hmax));
+                const uint4 o = make_uint4(pack_h2mh(__uint_as_float(w[0]), __uint_as_float(w[1]), hmax),
+                                           pack_h2mh(__uint_as_float(w[2]), __uint_as_float(w[3]), hmax),
+                                           pack_h2mh(__uint_as_float(w[4]), __uint_as_float(w[5]), hmax),
+                                           pack_h2mh(__uint_as_float(w[6]), __uint_as_float(w[7]), hmax));
                 uint8_t *dst = is_u ? rec + Rec<D>::Ut + kb * 8192 + swz(tt, c0 + cc)
                                     : rec + Rec<D>::A1 + kb * 16384 + swz(64 + tt, c0 + cc);
                 *reinterpret_cast<uint4 *>(dst) = o;
@@ -970,25 +977,7 @@ cudaError_t launch_intra_pass(const Params &p, cudaStream_t s) {
     const long long items = static_cast<long long>(p.NCmax) * p.HV;  // upper bound; the kernel reads the count
     const int grid = static_cast<int>(items < 2ll * sms ? items : 2ll * sms);
     if (grid <= 0) return cudaGetLastError();
-    if (!EXACT) {
-        kern<<<grid, kIntraThreads, C::kSmem, s>>>(p);
-        return cudaGetLastError();
-    }
-    // the exact pass: a programmatic dependent launch, so that its launch
-    // overlaps the first pass's tail (it waits for the first pass in-kernel)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kIntraThreads);
-    cfg.dynamicSmemBytes = C::kSmem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, p);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_chained(kern, dim3(grid), dim3(kIntraThreads), C::kSmem, s, p);
 }
 
 // Both passes: every item, then the exact pass over the items the first one

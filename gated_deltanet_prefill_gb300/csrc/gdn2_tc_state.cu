@@ -70,6 +70,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
     __shared__ uint64_t d1_full[2], o_full[2], d1_free[2];
     __shared__ uint32_t tmem_slot;
 
+    pdl_wait();  // the records (intra kernel) or incoming states (combine) are complete
+    if (SCAN && p.sc_mode == 1) pdl_trigger();  // the combine may launch and wait for the transitions
     if (p.status[0] != GDN2_OK) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // A CTA takes one (sequence, segment, value head, tile); the segment's
@@ -432,7 +434,7 @@ cudaError_t launch_state(const Params &p, cudaStream_t s) {
     const int tiles = p.sc_mode == 1 ? 2 * D / VT : D / VT;
     const long long ctas = static_cast<long long>(p.N) * segs * p.HV * tiles;
     if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-    if (ctas > 0) kern<<<static_cast<unsigned>(ctas), kStateThreads, C::kSmem, s>>>(p);
+    if (ctas > 0) return launch_chained(kern, dim3(static_cast<unsigned>(ctas)), dim3(kStateThreads), C::kSmem, s, p);
     return cudaGetLastError();
 }
 
@@ -461,6 +463,8 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
     extern __shared__ float4 combine_smem_raw[];
     float *Ms = reinterpret_cast<float *>(combine_smem_raw);  // [2][D][kCombineLd]
     float *Ss = Ms + 2 * D * kCombineLd;                      // [D][CW]
+    pdl_wait();     // the transitions are complete
+    pdl_trigger();  // the replay may launch and wait for this grid
     if (p.status[0] != GDN2_OK) return;
     const int n = blockIdx.x, hv = blockIdx.y, cbase = CW * blockIdx.z;
     const int tid = threadIdx.x, r0 = 2 * (tid / 4), c0 = NC * (tid % 4);
@@ -561,6 +565,8 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ uint64_t mma_done, drain;
     __shared__ uint32_t tmem_slot;
+    pdl_wait();     // the transitions are complete
+    pdl_trigger();  // the replay may launch and wait for this grid
     if (p.status[0] != GDN2_OK) return;
     const int n = blockIdx.x, hv = blockIdx.y, cbase = CW * blockIdx.z;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -706,15 +712,15 @@ cudaError_t launch_tc_scan_combine(const Params &p, cudaStream_t s) {
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(CombineTcCfg::kSmem));
         if (e != cudaSuccess) return e;
-        gdn2_scan_combine_tc_kernel<<<dim3(p.N, p.HV, 128 / CW), 256, CombineTcCfg::kSmem, s>>>(p);
-        return cudaGetLastError();
+        return launch_chained(gdn2_scan_combine_tc_kernel, dim3(p.N, p.HV, 128 / CW), dim3(256), CombineTcCfg::kSmem,
+                              s, p);
     }
     const cudaError_t e = cudaFuncSetAttribute(gdn2_scan_combine_kernel<CW>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(combine_smem<CW>()));
     if (e != cudaSuccess) return e;
-    gdn2_scan_combine_kernel<CW><<<dim3(p.N, p.HV, 128 / CW), 256, combine_smem<CW>(), s>>>(p);
-    return cudaGetLastError();
+    return launch_chained(gdn2_scan_combine_kernel<CW>, dim3(p.N, p.HV, 128 / CW), dim3(256), combine_smem<CW>(), s,
+                          p);
 }
 
 cudaError_t launch_tc_state(const Params &p, cudaStream_t s) {

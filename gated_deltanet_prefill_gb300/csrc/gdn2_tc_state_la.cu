@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
     __shared__ uint64_t d_full[3], o_full[3], d_free[3];
     __shared__ uint32_t tmem_slot;
 
+    pdl_wait();  // the records (intra kernel) or incoming states (combine) are complete
     if (p.status[0] != GDN2_OK) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // one CTA per (sequence in longest-first order, segment, value head,
@@ -508,6 +509,8 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
     __shared__ uint64_t d_full[2], o_full[2], d_free[2];
     __shared__ uint32_t tmem_slot;
 
+    pdl_wait();  // the records (intra kernel) or incoming states (combine) are complete
+    if (SCAN && p.sc_mode == 1) pdl_trigger();  // the combine may launch and wait for the transitions
     if (p.status[0] != GDN2_OK) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // one CTA per (sequence in longest-first order, segment, value head, tile),
@@ -987,7 +990,7 @@ cudaError_t launch_tc_state_la(const Params &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.N) * (p.sc_mode == 2 ? p.sc_P : 1) * p.HV * 2;
     if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-    if (ctas > 0) kern<<<static_cast<unsigned>(ctas), kLaThreads, LaCfg::kSmem, s>>>(p);
+    if (ctas > 0) return launch_chained(kern, dim3(static_cast<unsigned>(ctas)), dim3(kLaThreads), LaCfg::kSmem, s, p);
     return cudaGetLastError();
 }
 
@@ -998,7 +1001,7 @@ cudaError_t launch_tc_state_la128(const Params &p, cudaStream_t s) {
     const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
     const long long ctas = static_cast<long long>(p.N) * segs * p.HV * (p.sc_mode == 1 ? 2 : 1);
     if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-    if (ctas > 0) kern<<<static_cast<unsigned>(ctas), kLaThreads, La128Cfg::kSmem, s>>>(p);
+    if (ctas > 0) return launch_chained(kern, dim3(static_cast<unsigned>(ctas)), dim3(kLaThreads), La128Cfg::kSmem, s, p);
     return cudaGetLastError();
 }
 
