@@ -62,6 +62,8 @@ def parse():
                     help="skip the other D=128 workloads (2-4) in the line's `configs` object")
     ap.add_argument("--config-steps", type=int, default=20)
     ap.add_argument("--config-cpu-seconds", type=float, default=4.0)
+    ap.add_argument("--segments", type=int, default=0,
+                    help="segments per sequence of the chunk-parallel state pass (0: the library's choice)")
     ap.add_argument("--seqs", type=int, default=0,
                     help="keep only the workload's first SEQS sequences (a smaller case of the same "
                          "shape, for profiler captures); 0 = all")
@@ -400,6 +402,7 @@ def measure(wl, args, K, warmup, seed_rank=0, world=1, clocks_dev=None):
     fs = torch.empty((wl.N, HV, wl.K, V), dtype=torch.float32, device="cuda")
     dims = gdn2.make_dims(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], out, d["cu_seqlens"],
                           False, args.kernels)
+    dims.state_segments = args.segments
     ws = torch.empty(gdn2.workspace_bytes(dims), dtype=torch.uint8, device="cuda")
     names = gdn2.stage_names(dims)
     stream = torch.cuda.current_stream()
@@ -407,7 +410,7 @@ def measure(wl, args, K, warmup, seed_rank=0, world=1, clocks_dev=None):
     def step(evs=None):
         gdn2.chunk_gdn2_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["w"], scale=d["scale"],
                             initial_state=d["h0"], cu_seqlens=d["cu_seqlens"], out=out, final_state=fs,
-                            workspace=ws, impl=args.kernels, stage_events=evs)
+                            workspace=ws, impl=args.kernels, stage_events=evs, state_segments=args.segments)
 
     for _ in range(max(3, warmup)):
         step()

@@ -115,14 +115,16 @@ int scan_segments(const gdn2_dims &d) {
     const int64_t units = static_cast<int64_t>(d.N) * dims_hs(d);
     const int64_t chunks = d.T_tot / (static_cast<int64_t>(kChunk) * d.N);  // mean per sequence
     auto waves = [](int64_t ctas) { return static_cast<double>((ctas + kWave - 1) / kWave); };
-    auto pass = [&](int64_t P) {  // one state pass over P segments per (sequence, head)
-        return 2 * units * P <= kWave ? 2.2 * waves(2 * units * P) : 3.1 * waves(units * P);
+    auto pass = [&](int64_t S) {  // one state pass over S segments per (sequence, head)
+        return 2 * units * S <= kWave ? 2.2 * waves(2 * units * S) : 3.1 * waves(units * S);
     };
     double best = 10.0 + chunks * pass(1);
     int best_P = 1;
     for (int64_t P = 2; P <= 16 && chunks >= 8 * P; ++P) {
+        // segment 0 and the transitions of segments 1 .. P - 2 (128 columns),
+        // P - 2 combine steps, the replay of segments 1 .. P - 1
         const double L = static_cast<double>((chunks + P - 1) / P);
-        const double t = 3 * 10.0 + 3.5 * (P - 1) + L * (2.3 * waves(2 * units * (P - 1)) + pass(P));
+        const double t = (P > 2 ? 3 : 2) * 10.0 + 3.5 * (P - 2) + L * (2.3 * waves(units * (2 * P - 3)) + pass(P - 1));
         if (t < best) {
             best = t;
             best_P = static_cast<int>(P);
@@ -310,8 +312,11 @@ namespace {
 
 // The state-pass V tile the call uses: two 64-column tiles per (sequence,
 // head) when the untiled grid would leave more than half of the SMs idle.
-int state_vtile(const gdn2_dims &d, int P, int sms) {
-    return d.K == 128 && 2ll * d.N * dims_hs(d) * P <= sms ? 64 : d.K;
+// Columns per CTA of the sequential pass or the replay (segs segments per
+// sequence): 64 while two such tiles per (sequence, head, segment) fit one
+// wave on the SMs.
+int state_vtile(const gdn2_dims &d, int segs, int sms) {
+    return d.K == 128 && 2ll * d.N * dims_hs(d) * segs <= sms ? 64 : d.K;
 }
 
 // The launch sequence of one call as text (what each launch runs and its grid).
@@ -334,14 +339,17 @@ int describe_plan(const gdn2_dims &d, int sms, char *buf, size_t len) {
         add("; intra first pass %lld x256 (persistent, 2 CTAs/SM)", grid);
         add("; intra exact pass %lld x256 (programmatic dependent; only with g; runs the listed items)", grid);
         const int P = scan_segments(d);
-        const int vt = state_vtile(d, P, sms);
+        const int vt = state_vtile(d, P > 1 ? P - 1 : 1, sms);
         if (d.K == 64) {
             add("; state_output gdn2_tc_state_kernel<64> %dx%d", d.N, HS);
         } else if (P > 1) {
-            add("; chunk-parallel state pass, %d segments: transitions gdn2_tc_state_la128_kernel %lld CTAs of 128 "
-                "columns; combine %dx%dx8; replay %s %lld CTAs of %d columns",
-                P, 2ll * d.N * (P - 1) * HS, d.N, HS, vt == 64 ? "gdn2_tc_state_la_kernel" : "gdn2_tc_state_la128_kernel",
-                1ll * d.N * P * HS * (128 / vt), vt);
+            add("; chunk-parallel state pass, %d segments: segment 0 and the transitions of segments 1-%d "
+                "gdn2_tc_state_la128_kernel %lld CTAs of 128 columns",
+                P, P - 2, 1ll * d.N * HS * (1 + 2 * (P - 2)));
+            if (P > 2) add("; combine %dx%dx8, %d steps", d.N, HS, P - 2);
+            add("; replay of segments 1-%d %s %lld CTAs of %d columns", P - 1,
+                vt == 64 ? "gdn2_tc_state_la_kernel" : "gdn2_tc_state_la128_kernel", 1ll * d.N * (P - 1) * HS * (128 / vt),
+                vt);
         } else {
             add("; state_output %s %lld CTAs of %d columns", vt == 64 ? "gdn2_tc_state_la_kernel" : "gdn2_tc_state_la128_kernel",
                 1ll * d.N * HS * (128 / vt), vt);
@@ -447,7 +455,7 @@ gdn2_status run(const void *q, const void *k, const void *v, const void *g, cons
         cudaGetLastError();
         sms = 0;
     }
-    p.vtile = sms > 0 ? state_vtile(*d, p.sc_P, sms) : d->K;
+    p.vtile = sms > 0 ? state_vtile(*d, p.sc_P > 1 ? p.sc_P - 1 : 1, sms) : d->K;
     const char *log = getenv("GDN2_LOG");
     if (log && log[0] == '1') {  // the launch plan on stderr (diagnostics)
         char plan[1024];
@@ -542,8 +550,10 @@ int32_t gdn2_launch_count(const gdn2_dims *d) {
     if (!d || !shape_ok(*d)) return 0;
     if (d->N == 0) return 1;
     const int64_t ncmax = nc_max(*d);
-    if (d->impl != GDN2_IMPL_SIMT)  // map, intra (two passes), state (+ transitions and combine when segmented)
-        return 1 + (ncmax > 0 ? 2 : 0) + 1 + (scan_segments(*d) > 1 ? 2 : 0);
+    if (d->impl != GDN2_IMPL_SIMT) {  // map, intra (two passes), state; segmented: transitions, combine, replay
+        const int P = scan_segments(*d);
+        return 1 + (ncmax > 0 ? 2 : 0) + 1 + (P > 1 ? 1 : 0) + (P > 2 ? 1 : 0);
+    }
     int n = 1;                                          // chunk map
     n += (d->use_qk_l2norm && d->T_tot > 0) ? 1 : 0;    // q/k L2 norm
     n += ncmax > 0 ? 1 : 0;                             // cumsum

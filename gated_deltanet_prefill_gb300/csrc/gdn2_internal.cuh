@@ -66,9 +66,12 @@ struct Params {
     int vtile;                  // V columns per state CTA (tensor-core path)
     // chunk-parallel state pass (tensor-core path, K = V = 128): each sequence's
     // chunks in sc_P segments.  sc_mode 0: one sequential pass (sc_P = 1);
-    // 1: segment transitions [M | B] of S_out = M S_in + B for segments
-    // 0 .. P-2 into sc_tr [N, P-1, HV, K, K+V]; 2: every segment from its
-    // incoming state (h0, or sc_si [N, P-1, HV, K, V] from the combine kernel).
+    // 1: segment 0 replayed from the initial state, its final state into
+    // sc_si [N, P-1, HV, K, V] unit 0, and the transitions [M | B] of
+    // S_out = M S_in + B for segments 1 .. P-2 into sc_tr [N, P-1, HV, K, K+V]
+    // (unit 0 unused); the combine fills sc_si units 1 .. P-2 (sc_si unit s is
+    // the incoming state of segment s + 1); 2: segments 1 .. P-1 from their
+    // incoming states.
     // sc_mimg [N, P-1, HV]: each transition's M split into bf16 hi and lo parts,
     // as K-major 128B-swizzled operand images (64 KB each; written by the
     // lookahead transitions, read by the tensor-core combine)
@@ -88,6 +91,42 @@ struct Params {
     int tpre;
     int tm_order_k, tm_order_q, tm_order_b;
 };
+
+// The CTAs of one state launch, grouped by (sequence rank in the
+// longest-first order, state head), `per` CTAs per group, the group's CTAs
+// adjacent.  rt = V / VT column tiles cover one segment's state; a transition
+// covers the K + V columns of [M | B] in 2 rt tiles.  sc_mode 0 (the
+// sequential pass): rt tiles of the one segment.  sc_mode 1 (transitions):
+// segment 0 runs as a replay from the initial state (rt tiles; its final state
+// is the incoming state of segment 1), then 2 rt transition tiles for each of
+// segments 1 .. P - 2.  sc_mode 2 (replay): rt tiles for each of segments
+// 1 .. P - 1.
+__host__ __device__ inline int scan_ctas_per_group(int mode, int P, int rt) {
+    return mode == 1 ? rt + 2 * rt * (P - 2) : mode == 2 ? rt * (P - 1) : rt;
+}
+struct ScanCta {
+    int rank, hv, seg, tile;
+    bool trans;  // a transition tile (its tile indexes the 2 rt tiles of [M | B])
+};
+__device__ __forceinline__ ScanCta scan_cta(int b, int mode, int P, int HV, int rt) {
+    const int per = scan_ctas_per_group(mode, P, rt);
+    const int x = b % per, grp = b / per;
+    ScanCta c;
+    c.hv = grp % HV;
+    c.rank = grp / HV;
+    c.trans = mode == 1 && x >= rt;
+    if (c.trans) {
+        c.seg = 1 + (x - rt) / (2 * rt);
+        c.tile = (x - rt) % (2 * rt);
+    } else if (mode == 2) {
+        c.seg = 1 + x / rt;
+        c.tile = x % rt;
+    } else {
+        c.seg = 0;
+        c.tile = x;
+    }
+    return c;
+}
 
 // Workspace layout (byte offsets), a function of the problem only.
 struct WsLayout {

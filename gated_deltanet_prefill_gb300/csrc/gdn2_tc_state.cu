@@ -74,22 +74,17 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
     if (SCAN && p.sc_mode == 1) pdl_trigger();  // the combine may launch and wait for the transitions
     if (p.status[0] != GDN2_OK) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // A CTA takes one (sequence, segment, value head, tile); the segment's
-    // chunks are [seg L, seg L + L) of the sequence's, L = ceil(chunks /
-    // segments).  In the transition pass (sc_mode 1) the tiles cover the K + V
-    // columns of [M | B]: M columns start from the identity and take no Ut
+    // A CTA takes one (sequence, segment, value head, tile) (scan_cta); the
+    // segment's chunks are [seg L, seg L + L) of the sequence's, L =
+    // ceil(chunks / segments).  A transition's tiles cover the K + V columns
+    // of [M | B]: M columns start from the identity and take no Ut
     // (S_out = M S_in + B).
     const int mode = SCAN ? p.sc_mode : 0;
-    const int segs = mode == 1 ? p.sc_P - 1 : mode == 2 ? p.sc_P : 1;
     const int P = mode == 0 ? 1 : p.sc_P;
-    // one-dimensional grid: V tile fastest, then value head, then segment,
-    // then the sequence's rank in the longest-first order
-    const int tiles = mode == 1 ? 2 * D / VT : D / VT;
-    const int tile = blockIdx.x % tiles;
-    const int hv = (blockIdx.x / tiles) % p.HV;
-    const int rs = blockIdx.x / (tiles * p.HV);
-    const int seg = rs % segs, n = chk(p.seq_order[rs / segs], 0, p.N, 201, p.status);
-    const bool trans = mode == 1;
+    const ScanCta sc = scan_cta(blockIdx.x, mode, P, p.HV, D / VT);
+    const int tile = sc.tile, hv = sc.hv, seg = sc.seg;
+    const int n = chk(p.seq_order[sc.rank], 0, p.N, 201, p.status);
+    const bool trans = sc.trans;
     const int col0 = tile * VT;                     // first column of this tile
     const bool is_m = trans && col0 < D;            // a tile of M
     const int v0 = trans ? (is_m ? 0 : col0 - D) : col0;
@@ -295,9 +290,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             ok = false;
         }
         tc_fence_after();
-        // final state: the transition pass writes [M | B]; the replay pass only
+        // final state: a transition writes [M | B]; segment 0 of the
+        // transitions launch the incoming state of segment 1; the replay only
         // from the last segment
-        const bool write_final = trans || (p.hT && (mode != 2 || seg == P - 1));
+        const bool to_si = mode == 1 && !trans;
+        const bool write_final = trans || to_si || (p.hT && (mode == 0 || seg == P - 1));
         if (ok && active && write_final) {
 #pragma unroll 1
             for (int j = j0; j < j1; ++j) {
@@ -311,6 +308,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
 #pragma unroll
                     for (int e = 0; e < 32; e += 4)
                         *reinterpret_cast<float4 *>(tr + e) =
+                            make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                        __uint_as_float(r[e + 3]));
+                } else if (to_si) {  // sc_si unit (n, 0): fp32 [K][V]
+                    float *dst = p.sc_si + static_cast<size_t>(n) * (P - 1) * p.HV * D * D +
+                                 static_cast<size_t>(hv) * D * D + static_cast<size_t>(row) * D + v0 + 32 * j;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(dst + e) =
                             make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
                                         __uint_as_float(r[e + 3]));
                 } else if (plain) {
@@ -430,19 +435,18 @@ cudaError_t launch_state(const Params &p, cudaStream_t s) {
     auto kern = gdn2_tc_state_kernel<D, VT, NSTAGE, SCAN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
-    const int tiles = p.sc_mode == 1 ? 2 * D / VT : D / VT;
-    const long long ctas = static_cast<long long>(p.N) * segs * p.HV * tiles;
+    const long long ctas = static_cast<long long>(p.N) * p.HV * scan_ctas_per_group(p.sc_mode, p.sc_P, D / VT);
     if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
     if (ctas > 0) return launch_chained(kern, dim3(static_cast<unsigned>(ctas)), dim3(kStateThreads), C::kSmem, s, p);
     return cudaGetLastError();
 }
 
 // Chunk-parallel state pass, between the transition and the replay passes:
-// S_in(s + 1) = M_s S_in(s) + B_s for s = 0 .. P - 2, S_in(0) = the initial
-// state (or 0), into sc_si.  One CTA per (sequence, value head, CW value
-// columns); fp32 on CUDA cores, the running 128 x CW tile in shared memory.
-// The chain of P - 1 dependent steps is latency-bound: each step's M_s
+// S_in(s + 1) = M_s S_in(s) + B_s for s = 1 .. P - 2, into sc_si unit s,
+// starting from S_in(1), which the transitions launch wrote into unit 0 (it
+// replays segment 0 from the initial state).  One CTA per (sequence, value
+// head, CW value columns); fp32 on CUDA cores, the running 128 x CW tile in
+// shared memory.  The chain of P - 2 dependent steps is latency-bound: each step's M_s
 // (128 x 128 fp32, shared by the head's column tiles) is copied into shared
 // memory one step ahead by per-thread 16-byte asynchronous copies (rows
 // padded to 132 floats, so that rows read together start 4 banks apart), so
@@ -469,7 +473,6 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
     const int n = blockIdx.x, hv = blockIdx.y, cbase = CW * blockIdx.z;
     const int tid = threadIdx.x, r0 = 2 * (tid / 4), c0 = NC * (tid % 4);
     const int P = p.sc_P;
-    const size_t sblk = (static_cast<size_t>(n) * p.HV + hv) * D * D;
     auto unit = [&](int sg) { return (static_cast<size_t>(n) * (P - 1) + sg) * p.HV + hv; };
     auto load_m = [&](int sg) {  // M_sg: the first D columns of [M | B]
         const float *tr = p.sc_tr + unit(sg) * D * (2 * D);
@@ -481,15 +484,15 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
         }
         cp_async_commit();
     };
-    if (P > 1) load_m(0);
+    if (P > 2) load_m(1);
+    {  // S_in(1): sc_si unit 0, fp32 [K][V]
+        const float *s1 = p.sc_si + unit(0) * D * D;
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int x = 0; x < NC; ++x)
-            Ss[(r0 + rr) * CW + c0 + x] =
-                p.h0 ? state_ld(p.h0, sblk + state_off(r0 + rr, cbase + c0 + x, D, D, p.state_vmajor), p.state_bf16)
-                     : 0.f;
-    for (int sg = 0; sg < P - 1; ++sg) {
+        for (int rr = 0; rr < 2; ++rr)
+            *reinterpret_cast<float4 *>(Ss + (r0 + rr) * CW + c0) =
+                *reinterpret_cast<const float4 *>(s1 + static_cast<size_t>(r0 + rr) * D + cbase + c0);
+    }
+    for (int sg = 1; sg < P - 1; ++sg) {
         const bool ahead = sg + 1 < P - 1;
         if (ahead) load_m(sg + 1);  // its buffer was last read in step sg - 1
         const float *tr = p.sc_tr + unit(sg) * D * (2 * D);
@@ -531,7 +534,7 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
 }
 
 // The same combine on the tensor cores, one CTA per (sequence, value head,
-// 16 value columns) as above.  The CTA's product M_s S (128 x 128 x 16) is
+// 16 value columns) as above, from S_in(1) over segments 1 .. P - 2.  The CTA's product M_s S (128 x 128 x 16) is
 // three bf16 products with fp32 accumulation, M_hi S_hi + M_hi S_lo +
 // M_lo S_hi, where x_hi = bf16(x) and x_lo = bf16(x - x_hi): about 16
 // mantissa bits per operand, far finer than the fp16 operand rounding the
@@ -570,8 +573,7 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
     if (p.status[0] != GDN2_OK) return;
     const int n = blockIdx.x, hv = blockIdx.y, cbase = CW * blockIdx.z;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int P = p.sc_P, steps = P - 1;
-    const size_t sblk = (static_cast<size_t>(n) * p.HV + hv) * D * D;
+    const int P = p.sc_P, steps = P - 2;  // step s: segment s + 1
     auto unit = [&](int sg) { return (static_cast<size_t>(n) * (P - 1) + sg) * p.HV + hv; };
     if (tid == 0) {
         mbar_init(&mma_done, 1);
@@ -587,9 +589,9 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
     tc_fence_after();
     const uint32_t tD = tmem_slot;
     bool ok = true;
-    auto load_m = [&](int sg) {  // the M_sg images into buffer sg & 1 (warps 4-7)
-        const uint8_t *src = p.sc_mimg + unit(sg) * C::kMimg;
-        uint8_t *dst = sm + (sg & 1) * C::kMimg;
+    auto load_m = [&](int st) {  // step st's M images (segment st + 1) into buffer st & 1 (warps 4-7)
+        const uint8_t *src = p.sc_mimg + unit(st + 1) * C::kMimg;
+        uint8_t *dst = sm + (st & 1) * C::kMimg;
 #pragma unroll 4
         for (int i = tid - 128; i < static_cast<int>(C::kMimg / 16); i += 128) cp_async16(dst + 16 * i, src + 16 * i, 16);
         cp_async_commit();
@@ -603,21 +605,20 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
         *reinterpret_cast<unsigned short *>(sm + C::oSh + off) = static_cast<unsigned short>(hi);
         *reinterpret_cast<unsigned short *>(sm + C::oSl + off) = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
     };
-    {  // S_in(0): the initial state (or 0), two threads per row, 8 columns each
+    {  // S_in(1): sc_si unit 0 (fp32 [K][V]), two threads per row, 8 columns each
         const int r = tid / 2, j0 = 8 * (tid % 2);
+        const float *s1 = p.sc_si + unit(0) * D * D + static_cast<size_t>(r) * D + cbase + j0;
 #pragma unroll
-        for (int x = 0; x < 8; ++x)
-            put_s(r, j0 + x,
-                  p.h0 ? state_ld(p.h0, sblk + state_off(r, cbase + j0 + x, D, D, p.state_vmajor), p.state_bf16) : 0.f);
+        for (int x = 0; x < 8; ++x) put_s(r, j0 + x, s1[x]);
     }
-    if (warp >= 4) {
+    if (warp >= 4 && steps > 0) {
         load_m(0);
         if (steps > 1) load_m(1);
         if (steps > 1) cp_async_wait_group<1>(); else cp_async_wait_group<0>();
     }
     fence_proxy_async();
     tc_fence_before();
-    __syncthreads();  // M_0's images (each thread's own copies waited for) and S_in(0) are in place
+    __syncthreads();  // step 0's M images (each thread's own copies waited for) and S_in(1) are in place
     tc_fence_after();
     for (int s = 0; s < steps; ++s) {
         const bool next = s + 1 < steps;
@@ -635,9 +636,9 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
             mma_commit(&mma_done);
         }
         if (warp < 4) {
-            // S_in(s + 1) = M_s S_in(s) + B_s: row r of the product is TMEM lane r
+            // S_in(s + 2) = M_{s+1} S_in(s + 1) + B_{s+1}: row r of the product is TMEM lane r
             const int r = 32 * warp + lane;
-            const float *brow = p.sc_tr + unit(s) * D * (2 * D) + static_cast<size_t>(r) * (2 * D) + D + cbase;
+            const float *brow = p.sc_tr + unit(s + 1) * D * (2 * D) + static_cast<size_t>(r) * (2 * D) + D + cbase;
             float bv[CW];
 #pragma unroll
             for (int x = 0; x < CW; x += 4) {
@@ -652,7 +653,7 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_tc_kernel(Params p) 
             float v[CW];
 #pragma unroll
             for (int x = 0; x < CW; ++x) v[x] = __uint_as_float(acc[x]) + bv[x];
-            float *si = p.sc_si + unit(s) * D * D + static_cast<size_t>(r) * D + cbase;
+            float *si = p.sc_si + unit(s + 1) * D * D + static_cast<size_t>(r) * D + cbase;
 #pragma unroll
             for (int x = 0; x < CW; x += 4) *reinterpret_cast<float4 *>(si + x) = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
             if (next) {
@@ -702,7 +703,7 @@ bool lookahead128_on() {
 
 cudaError_t launch_tc_scan_combine(const Params &p, cudaStream_t s) {
     constexpr int CW = 16;
-    if (p.N <= 0 || p.sc_P <= 1) return cudaSuccess;
+    if (p.N <= 0 || p.sc_P <= 2) return cudaSuccess;  // two segments: nothing to combine
     // the tensor-core combine reads the M images the lookahead transitions
     // write; GDN2_SCAN_COMBINE=cuda (or the plain state kernel) keeps the
     // CUDA-core one

@@ -83,16 +83,17 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la_kernel(Params 
     pdl_wait();  // the records (intra kernel) or incoming states (combine) are complete
     if (p.status[0] != GDN2_OK) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // one CTA per (sequence in longest-first order, segment, value head,
-    // 64-column tile), the tile fastest; the sequential pass has one segment
+    // one CTA per (sequence in longest-first order, value head, segment,
+    // 64-column tile), the tile fastest (scan_cta); the sequential pass has
+    // one segment, the replay segments 1 .. P - 1
     int P = 1, tile, seg = 0, hv, n, first, nck, c_lo = 0;
     if constexpr (SCAN) {
         P = p.sc_P;
-        tile = blockIdx.x % 2;
-        hv = (blockIdx.x / 2) % p.HV;
-        const int rs = blockIdx.x / (2 * p.HV);
-        seg = rs % P;
-        n = chk(p.seq_order[rs / P], 0, p.N, 301, p.status);
+        const ScanCta sc = scan_cta(blockIdx.x, 2, P, p.HV, 2);
+        tile = sc.tile;
+        hv = sc.hv;
+        seg = sc.seg;
+        n = chk(p.seq_order[sc.rank], 0, p.N, 301, p.status);
         const int seq0 = p.seq_first[n], nck_all = p.seq_first[n + 1] - seq0;
         const int L = (nck_all + P - 1) / P;
         c_lo = min(seg * L, nck_all);
@@ -518,16 +519,16 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
     // segment's chunks are [seg L, seg L + L) of the sequence's, L =
     // ceil(chunks / P).
     int mode = 0, P = 1, tile = 0, seg = 0, hv, n, first, nck, c_lo = 0;
+    bool trans_cta = false;
     if constexpr (SCAN) {
         mode = p.sc_mode;
         P = p.sc_P;
-        const int segs = mode == 1 ? P - 1 : P;
-        const int tiles = mode == 1 ? 2 : 1;
-        tile = blockIdx.x % tiles;
-        hv = (blockIdx.x / tiles) % p.HV;
-        const int rs = blockIdx.x / (tiles * p.HV);
-        seg = rs % segs;
-        n = chk(p.seq_order[rs / segs], 0, p.N, 401, p.status);
+        const ScanCta sc = scan_cta(blockIdx.x, mode, P, p.HV, 1);
+        tile = sc.tile;
+        hv = sc.hv;
+        seg = sc.seg;
+        trans_cta = sc.trans;
+        n = chk(p.seq_order[sc.rank], 0, p.N, 401, p.status);
         const int seq0 = p.seq_first[n], nck_all = p.seq_first[n + 1] - seq0;
         const int L = (nck_all + P - 1) / P;
         c_lo = min(seg * L, nck_all);
@@ -539,7 +540,10 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
         first = p.seq_first[n];
         nck = p.seq_first[n + 1] - first;
     }
-    const bool trans = SCAN && mode == 1, is_m = trans && tile == 0;  // is_m: columns of M (no Ut)
+    const bool trans = SCAN && trans_cta, is_m = trans && tile == 0;  // is_m: columns of M (no Ut)
+    // segment 0 of the transitions launch: a replay whose final state is the
+    // incoming state of segment 1
+    const bool to_si = SCAN && mode == 1 && !trans;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -819,9 +823,10 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
             ok = false;
         }
         tc_fence_after();
-        // the transitions write [M | B]; the replay writes the final state from
-        // the last segment only
-        const bool write_final = (SCAN && trans) || (p.hT && (mode != 2 || seg == P - 1));
+        // a transition writes [M | B], segment 0 of the transitions launch
+        // sc_si unit (n, 0); the replay writes the final state from the last
+        // segment only
+        const bool write_final = (SCAN && trans) || to_si || (p.hT && (mode == 0 || seg == P - 1));
         if (ok && write_final) {
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
@@ -858,6 +863,14 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
                             *reinterpret_cast<uint4 *>(img + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
                         }
                     }
+                } else if (to_si) {  // fp32 [K][V]
+                    float *dst = p.sc_si + static_cast<size_t>(n) * (P - 1) * p.HV * D * D +
+                                 static_cast<size_t>(hv) * D * D + static_cast<size_t>(row) * D + col0;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(dst + e) = make_float4(
+                            __uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                            __uint_as_float(r[e + 3]));
                 } else if (plain) {
                     float *hT = static_cast<float *>(p.hT) + sblk + static_cast<size_t>(row) * D + col0;
 #pragma unroll
@@ -988,7 +1001,7 @@ cudaError_t launch_tc_state_la(const Params &p, cudaStream_t s) {
     auto kern = p.sc_mode == 0 ? gdn2_tc_state_la_kernel<false> : gdn2_tc_state_la_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LaCfg::kSmem);
     if (e != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(p.N) * (p.sc_mode == 2 ? p.sc_P : 1) * p.HV * 2;
+    const long long ctas = static_cast<long long>(p.N) * p.HV * scan_ctas_per_group(p.sc_mode, p.sc_P, 2);
     if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
     if (ctas > 0) return launch_chained(kern, dim3(static_cast<unsigned>(ctas)), dim3(kLaThreads), LaCfg::kSmem, s, p);
     return cudaGetLastError();
@@ -998,8 +1011,7 @@ cudaError_t launch_tc_state_la128(const Params &p, cudaStream_t s) {
     auto kern = p.sc_mode == 0 ? gdn2_tc_state_la128_kernel<false> : gdn2_tc_state_la128_kernel<true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, La128Cfg::kSmem);
     if (e != cudaSuccess) return e;
-    const int segs = p.sc_mode == 1 ? p.sc_P - 1 : p.sc_mode == 2 ? p.sc_P : 1;
-    const long long ctas = static_cast<long long>(p.N) * segs * p.HV * (p.sc_mode == 1 ? 2 : 1);
+    const long long ctas = static_cast<long long>(p.N) * p.HV * scan_ctas_per_group(p.sc_mode, p.sc_P, 1);
     if (ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
     if (ctas > 0) return launch_chained(kern, dim3(static_cast<unsigned>(ctas)), dim3(kLaThreads), La128Cfg::kSmem, s, p);
     return cudaGetLastError();

@@ -165,7 +165,12 @@ def test_launch_plan(lib):
     few = plan(16384 * 2, 2, 16, 32, 128)
     assert "gdn2_tc_state_la_kernel 128 CTAs of 64 columns" in few
     seg = plan(4096, 1, 16, 16, 128)
-    assert "chunk-parallel state pass, 4 segments" in seg
+    assert "chunk-parallel state pass, 5 segments" in seg
+    assert "gdn2_tc_state_la128_kernel 112 CTAs of 128 columns" in seg   # segment 0, transitions of 1-3
+    assert "combine 1x16x8, 3 steps" in seg
+    assert "replay of segments 1-4 gdn2_tc_state_la_kernel 128 CTAs of 64 columns" in seg
+    two = plan(4096, 1, 16, 16, 128, segments=2)
+    assert "combine" not in two and "replay of segments 1-1" in two
     assert "simt_intra" in plan(256, 1, 2, 2, 64, impl=1)
     assert "state_kernel<64>" in plan(256, 1, 2, 2, 64)
     d = gdn2.Dims()
@@ -260,6 +265,9 @@ def test_state_segments_host_logic(lib):
     # few (sequence, head) pairs on long sequences: P >= 3 chosen automatically
     few = _dims(lib, T=4096, N=1, H=16, HV=16, K=128, V=128)
     assert gdn2.launch_count(few) == 6            # map, intra (2 passes), transitions, combine, replay
+    two = _dims(lib, T=4096, N=1, H=16, HV=16, K=128, V=128)
+    two.state_segments = 2
+    assert gdn2.launch_count(two) == 5            # two segments: nothing to combine
     seq = _dims(lib, T=4096, N=1, H=16, HV=16, K=128, V=128)
     seq.state_segments = 1
     assert gdn2.launch_count(seq) == 4            # map, intra (2 passes), state

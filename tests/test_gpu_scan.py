@@ -1,7 +1,8 @@
 """GPU parity of the chunk-parallel state pass (tensor-core path, K = V =
-128): each sequence's chunks in P segments; segment transitions [M | B] of
-S_out = M S_in + B in parallel, a combine over segments, then every segment
-replayed from its incoming state.  The transitions and the replay run on the
+128): each sequence's chunks in P segments; segment 0 replayed from the
+initial state beside the transitions [M | B] of S_out = M S_in + B of
+segments 1 .. P - 2, a combine over those, then segments 1 .. P - 1 replayed
+from their incoming states.  The transitions and the replay run on the
 lookahead state kernels (on the plain one with GDN2_STATE_LOOKAHEAD=0).
 Checked against the FP64 oracle and against the sequential pass.
 
@@ -51,11 +52,12 @@ def test_forced_segments_match_oracle(cuda_lib, segments):
     assert rel_max(hT.cpu().numpy(), h1.cpu().numpy()) <= TOL
 
 
-@pytest.mark.parametrize("segments", [3, 5])
+@pytest.mark.parametrize("segments", [2, 3, 6])
 def test_forced_segments_plain_kernel(cuda_lib, monkeypatch, segments):
     """The same with the transitions and the replay on the plain state kernel
     (GDN2_STATE_LOOKAHEAD=0); the default runs them on the lookahead kernels.
-    P = 3 takes 64-column tiles, P = 5 128-column ones."""
+    The replay of P - 1 segments takes 64-column tiles at P = 2 and 3 (16
+    (sequence, head) pairs), 128-column ones at P = 6; P = 2 has no combine."""
     monkeypatch.setenv("GDN2_STATE_LOOKAHEAD", "0")
     wl = inputs.small("scanplain", [700, 1, 129, 2000], H=2, HV=4, K=128, V=128, g_max=2.0, beta_max=2.0,
                       h0_std=0.05, seed=73)
@@ -70,9 +72,10 @@ def test_forced_segments_plain_kernel(cuda_lib, monkeypatch, segments):
 @pytest.mark.parametrize("combine", ["cuda", "tc"])
 def test_combine_kernels(cuda_lib, monkeypatch, combine):
     """Both combine kernels (the tensor-core one by default, the CUDA-core
-    one with GDN2_SCAN_COMBINE=cuda) at 9 segments (8 dependent steps), with
-    slow decay so that every step's M S_in term matters, and a bf16 V-major
-    initial state read by the first step."""
+    one with GDN2_SCAN_COMBINE=cuda) at 9 segments (7 dependent steps from
+    segment 1's incoming state), with slow decay so that every step's M S_in
+    term matters, and a bf16 V-major initial state read by segment 0's
+    replay."""
     if combine == "cuda":
         monkeypatch.setenv("GDN2_SCAN_COMBINE", "cuda")
     wl = inputs.small("comb", [1500, 700], H=2, HV=2, K=128, V=128, g_max=0.02, beta_max=1.0, h0_std=0.5,
