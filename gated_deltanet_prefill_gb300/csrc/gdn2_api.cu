@@ -98,16 +98,19 @@ bool shape_ok(const gdn2_dims &d) {
 }
 
 // Segments of the chunk-parallel state pass.  The chain of a sequence's
-// chunks is cut into P segments; the price is a transition pass over K + V
-// columns (2 x 128-column tiles per segment but the last), a combine of P - 1
-// steps and a replay pass.  P is the minimum of a time model per chunk of the
-// longest pass, counted in waves of a GB300's 152 SMs (one CTA per SM):
-// 2.2 us for a 64-column tile, 2.3 us for a transition tile, 3.1 us for a
-// 128-column tile and 10 us per launch, fitted to the plain state kernel
-// (the lookahead kernels are faster by similar factors in every pass), and
-// 3.5 us per step of the tensor-core combine.  On few-head shapes the P this
-// picks is the best measured one or within 3 % of it.  Segments keep at
-// least 8 chunks.
+// chunks is cut into P equal segments; the price is a first launch that
+// replays segment 0 (128-column tiles) beside the transitions over K + V
+// columns of segments 1 .. P - 2 (2 x 128-column tiles each), a combine of
+// P - 2 steps and a replay of segments 1 .. P - 1.  P is the minimum of a
+// time model per chunk of the longest pass, counted in waves of a GB300's 152
+// SMs (one CTA per SM): 2.2 us for a 64-column tile, 3.1 us for a 128-column
+// tile (the first launch's replay of segment 0 bounds that launch; its
+// transition tiles take about 2.3 us) and 10 us per launch, fitted to the
+// plain state kernel (the lookahead kernels are faster by similar factors in
+// every pass), and 3.5 us per step of the tensor-core combine.  On the
+// 4096-token, 16-head shape it picks P = 5, the best measured (state stage
+// 0.080 ms, against 0.092 ms at P = 4 and 0.086 ms at P = 6).  Segments keep
+// at least 8 chunks.
 int scan_segments(const gdn2_dims &d) {
     if (d.impl != GDN2_IMPL_TC || d.K != 128 || d.V != 128 || d.N <= 0) return 1;
     if (d.state_segments > 0) return d.state_segments;
@@ -121,10 +124,10 @@ int scan_segments(const gdn2_dims &d) {
     double best = 10.0 + chunks * pass(1);
     int best_P = 1;
     for (int64_t P = 2; P <= 16 && chunks >= 8 * P; ++P) {
-        // segment 0 and the transitions of segments 1 .. P - 2 (128 columns),
-        // P - 2 combine steps, the replay of segments 1 .. P - 1
+        // segment 0 beside the transitions of segments 1 .. P - 2 (128
+        // columns), P - 2 combine steps, the replay of segments 1 .. P - 1
         const double L = static_cast<double>((chunks + P - 1) / P);
-        const double t = (P > 2 ? 3 : 2) * 10.0 + 3.5 * (P - 2) + L * (2.3 * waves(units * (2 * P - 3)) + pass(P - 1));
+        const double t = (P > 2 ? 3 : 2) * 10.0 + 3.5 * (P - 2) + L * (3.1 * waves(units * (2 * P - 3)) + pass(P - 1));
         if (t < best) {
             best = t;
             best_P = static_cast<int>(P);
