@@ -137,13 +137,15 @@ typedef struct gdn2_dims {
 /*
  * state_segments (tensor-core path, K = V = 128): P > 1 splits each
  * sequence's chunks into P segments of ceil(chunks / P).  Every segment's
- * state map is affine, S_out = M S_in + B; the library computes [M | B] for
- * segments 0 .. P - 2 in parallel, combines them in order into each
- * segment's incoming state (fp32 accumulation of products whose operands
- * are split into bf16 high and low parts, about 16 mantissa bits each),
- * then replays all segments in parallel for o and the final state.  This shortens the sequential chain for few (sequence,
- * head) pairs on long sequences (the FlashInfer docs, output_state: the
- * cuDNN engine splits one sequence across CTAs).  0 = the library chooses
+ * state map is affine, S_out = M S_in + B.  The library replays segment 0
+ * from the initial state while it computes [M | B] for segments 1 .. P - 2
+ * in parallel, combines those in order into each later segment's incoming
+ * state (fp32 accumulation of products whose operands are split into bf16
+ * high and low parts, about 16 mantissa bits each), then replays segments
+ * 1 .. P - 1 in parallel for o and the final state.  This shortens the
+ * sequential chain for few (sequence, head) pairs on long sequences (the
+ * FlashInfer docs, output_state: the cuDNN engine splits one sequence
+ * across CTAs).  0 = the library chooses
  * P from a time model of the passes (P > 1 only for few (sequence, head)
  * pairs on long sequences), 1 = one sequential pass, 2 .. 64 forced.
  * Out of range, or > 1 with the SIMT path or K != 128: GDN2_ERR_SHAPE.  M is
@@ -219,6 +221,12 @@ GDN2_API gdn2_status gdn2_check_args(const void *q, const void *k, const void *v
  * for 128-column tiles); GDN2_STATE_LOOKAHEAD=0 selects the plain state
  * kernel for both, =64 for the 128-column tiles only (diagnostics; same
  * results up to rounding).
+ *
+ * Every launch after the first is a programmatic dependent launch on
+ * `stream`: it may be scheduled while the kernel before it drains and waits
+ * in-kernel for that kernel's results, so the call has no launch gaps.  The
+ * first launch follows the stream's earlier work in the usual order.
+ * GDN2_PDL=0 makes every launch a plain one (diagnostics; same results).
  */
 GDN2_API gdn2_status gdn2_chunk_fwd(const void *q, const void *k, const void *v, const void *g,
                            const void *beta, const void *w, float scale,

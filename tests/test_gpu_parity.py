@@ -181,6 +181,29 @@ def test_tc_row_copies(cuda_lib, monkeypatch, D):
     assert rel_max(hT.cpu().numpy(), h_ref) <= TOL
 
 
+@pytest.mark.parametrize("segments", [1, 4])
+def test_plain_launches_match_chained(cuda_lib, monkeypatch, segments):
+    """Every launch after the first of a call is chained to its predecessor
+    (programmatic dependent launches); GDN2_PDL=0 launches them plainly.  The
+    kernels and their arithmetic are the same, so the two give bit-identical
+    results, here with the exact pass active (decays past its threshold in
+    some channels) and both state passes, and both match the oracle."""
+    wl = inputs.small("pdl", [700, 1, 129, 2000], H=2, HV=4, K=128, V=128, g_max=1.0, beta_max=2.0,
+                      h0_std=0.05, seed=38)
+    d = inputs.generate(wl)
+    g = d["g"].clone()
+    g[:, :, :8] *= 40.0  # 8 channels decaying up to 40 nats per token
+    d["g"] = g
+    o_ref, h_ref = run_oracle(d)
+    dd = to_dev(d)
+    o1, h1 = run_gpu(cuda_lib, dd, "tc", state_segments=segments)
+    monkeypatch.setenv("GDN2_PDL", "0")
+    o0, h0 = run_gpu(cuda_lib, dd, "tc", state_segments=segments)
+    assert torch.equal(o1, o0) and torch.equal(h1, h0)
+    assert rel_max(o1.float().cpu().numpy(), o_ref) <= TOL
+    assert rel_max(h1.cpu().numpy(), h_ref) <= TOL
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_split_sequence_matches_one_pass(cuda_lib, impl):
     """Prefill in two calls carrying the final state equals one call

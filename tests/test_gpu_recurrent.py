@@ -54,6 +54,20 @@ def test_decode_one_token(cuda_lib, D):
     check(cuda_lib, wl)
 
 
+def test_plain_launches_match_chained(cuda_lib, monkeypatch):
+    """The step kernel is chained to the check kernel (a programmatic
+    dependent launch); GDN2_PDL=0 launches it plainly, with bit-identical
+    results."""
+    wl = inputs.small("decpdl", [1] * 6 + [9, 40], H=2, HV=4, K=128, V=128, g_max=1.0, beta_max=2.0,
+                      h0_std=0.05, seed=53)
+    d = to_dev(inputs.generate(wl))
+    o1, h1 = run_rec(cuda_lib, d)
+    monkeypatch.setenv("GDN2_PDL", "0")
+    o0, h0 = run_rec(cuda_lib, d)
+    assert torch.equal(o1, o0) and torch.equal(h1, h0)
+    check(cuda_lib, wl)
+
+
 @pytest.mark.parametrize("D", [64, 128])
 def test_ragged_continuations(cuda_lib, D):
     """Sequences of 0 .. 70 tokens, grouped value heads, decay stress."""
