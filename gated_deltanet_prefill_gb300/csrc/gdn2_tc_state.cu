@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn2_tc_state_kernel(Params 
             }
             tc_fence_after();
             const int64_t tok = seq_start + static_cast<int64_t>(c_lo + i) * kChunk + t;
-            const bool valid = !trans && tok < seq_end;  // the transition pass writes no output
+            const bool valid = !trans && tok < seq_end;  // a transition writes no output
             bf16 *orow = p.o + tok * p.so_t + static_cast<int64_t>(hv) * p.so_h + v0;
 #pragma unroll 1
             for (int j = 0; j < VT / 32; ++j) {
@@ -534,8 +534,9 @@ __global__ void __launch_bounds__(256, 1) gdn2_scan_combine_kernel(Params p) {
 }
 
 // The same combine on the tensor cores, one CTA per (sequence, value head,
-// 16 value columns) as above, from S_in(1) over segments 1 .. P - 2.  The CTA's product M_s S (128 x 128 x 16) is
-// three bf16 products with fp32 accumulation, M_hi S_hi + M_hi S_lo +
+// 16 value columns) as above, from S_in(1) over segments 1 .. P - 2.  The
+// CTA's product M_s S (128 x 128 x 16) is three bf16 products with fp32
+// accumulation, M_hi S_hi + M_hi S_lo +
 // M_lo S_hi, where x_hi = bf16(x) and x_lo = bf16(x - x_hi): about 16
 // mantissa bits per operand, far finer than the fp16 operand rounding the
 // state pass applies at every chunk (the dropped M_lo S_lo term is below

@@ -496,9 +496,10 @@ struct La128Cfg {
 };
 
 // SCAN = false: the sequential pass.  SCAN = true: the chunk-parallel modes of
-// the plain state kernel (sc_mode 1: the transitions [M | B] of segments
-// 0 .. P - 2 on two 128-column tiles, M from the identity with no Ut and no
-// output; sc_mode 2: every segment from its incoming state).
+// the plain state kernel (sc_mode 1: segment 0 replayed from the initial
+// state beside the transitions [M | B] of segments 1 .. P - 2 on two
+// 128-column tiles, M from the identity with no Ut and no output; sc_mode 2:
+// segments 1 .. P - 1 from their incoming states).
 template <bool SCAN>
 __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Params p) {
     using C = La128Cfg;
@@ -514,10 +515,10 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
     if (SCAN && p.sc_mode == 1) pdl_trigger();  // the combine may launch and wait for the transitions
     if (p.status[0] != GDN2_OK) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // one CTA per (sequence in longest-first order, segment, value head, tile),
-    // the tile fastest; the sequential pass has one segment and one tile.  A
-    // segment's chunks are [seg L, seg L + L) of the sequence's, L =
-    // ceil(chunks / P).
+    // one CTA per (sequence in longest-first order, value head, segment,
+    // tile), the tile fastest (scan_cta); the sequential pass has one segment
+    // and one tile.  A segment's chunks are [seg L, seg L + L) of the
+    // sequence's, L = ceil(chunks / P).
     int mode = 0, P = 1, tile = 0, seg = 0, hv, n, first, nck, c_lo = 0;
     bool trans_cta = false;
     if constexpr (SCAN) {
