@@ -1,8 +1,10 @@
 """A seeded random sweep of the chunked forward against the FP64 oracle:
 ragged sequence sets (empty sequences included), D = 64 or 128, grouped value
-heads, decays up to 20 nats per token, absent gates, the fused L2 norm, initial states, fp16 inputs, 16-bit
-g, bf16 and V-major states, and the state pass forced sequential or
-chunk-parallel where the shape allows.  Each case is drawn from its own seed
+heads, decays up to 20 nats per token, absent gates, the fused L2 norm,
+initial states, fp16 inputs, 16-bit g, bf16 and V-major states, and the state
+pass forced sequential or chunk-parallel where the shape allows (a second
+draw covers the chunk-parallel pass on sequences of up to 25 chunks with 2 to
+8 segments).  Each case is drawn from its own seed
 and printed on failure.
 
 Bar: max|x - x_ref| / max|x_ref| <= 1e-2 for o and for the final state.
@@ -46,10 +48,39 @@ def draw(seed):
     return case
 
 
+def draw_segmented(seed):
+    """The chunk-parallel state pass: D = 128, sequences up to 1600 tokens (25
+    chunks), segment counts forced to 2 .. 8 or chosen by the library."""
+    rng = np.random.default_rng(seed)
+    H = int(rng.choice([1, 2]))
+    HV = H * int(rng.choice([1, 2]))
+    n = int(rng.integers(1, 6))
+    lens = [int(x) for x in rng.integers(0, 1600, size=n)]
+    if rng.random() < 0.3:
+        lens[int(rng.integers(0, n))] = int(rng.integers(0, 70))
+    if sum(lens) == 0:
+        lens[0] = 1
+    return dict(D=128, H=H, HV=HV, lens=lens, g_max=float(rng.choice([0.005, 0.05, 0.5, 2.0, 8.0, 20.0])),
+                beta_max=float(rng.choice([1.0, 2.0])), h0=bool(rng.random() < 0.6),
+                drop=[k for k in ("g", "beta", "w") if rng.random() < 0.15], l2=bool(rng.random() < 0.3),
+                qkv=[torch.bfloat16, torch.float16][int(rng.integers(0, 2))],
+                gdt=[torch.float32, torch.bfloat16, torch.float16][int(rng.integers(0, 3))],
+                sdt=[torch.float32, torch.bfloat16][int(rng.integers(0, 2))], vmajor=bool(rng.random() < 0.3),
+                segments=int(rng.choice([0, 2, 3, 4, 5, 8])))
+
+
 @pytest.mark.parametrize("seed", list(range(1000, 1020)))
 def test_random_case(cuda_lib, seed):
-    c = draw(seed)
-    wl = inputs.small("rand%d" % seed, c["lens"], H=c["H"], HV=c["HV"], K=c["D"], V=c["D"], g_max=c["g_max"],
+    run_case(cuda_lib, draw(seed), "rand%d" % seed, seed)
+
+
+@pytest.mark.parametrize("seed", list(range(3000, 3020)))
+def test_random_segmented_case(cuda_lib, seed):
+    run_case(cuda_lib, draw_segmented(seed), "srand%d" % seed, seed)
+
+
+def run_case(cuda_lib, c, name, seed):
+    wl = inputs.small(name, c["lens"], H=c["H"], HV=c["HV"], K=c["D"], V=c["D"], g_max=c["g_max"],
                       beta_max=c["beta_max"], h0_std=0.05 if c["h0"] else None, seed=seed)
     d = inputs.generate(wl)
     for k in c["drop"]:
