@@ -652,6 +652,7 @@ def run_ours(args):
                            "g": "-U(0,%g)" % wl.g_max, "beta": "U(0,%g)" % wl.beta_max,
                            "initial_state": "N(0,%g)" % wl.h0_std if wl.h0_std else "zero",
                            "output_final_state": True, "l2": l2_note(fmin),
+                           "state_segments": args.segments if args.segments else "chosen by the library",
                            "parallelism": "replicas x%d (independent batches)" % world},
                 "ms_per_step_staged": rec["staged_ms"],
                 "timing": "ms_per_step: steps with no event between their kernels (each launch overlaps its "
