@@ -258,6 +258,18 @@ template <int D, bool F16, bool EXACT>
 __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const __grid_constant__ Params p) {
     using C = IntraCfg<D>;
     constexpr int NJ = D / 32;         // 8-channel chunks per thread
+    // D = 128, first pass: the record's P and [Wt | Ut] images are staged in
+    // shared memory that is dead at that point and written by bulk copies
+    // (the tensor memory accelerator reads them out of shared memory, so the
+    // stores leave the LSU/L1 path; 2.93 -> 2.78 ms on the long workload).
+    // P (8 KB) goes past the solver matrices, below the T image, during the
+    // solve; [Wt | Ut] (32 KB) over the dead R operand and T image during the
+    // W/U epilogue.  D = 64 has no such room, and the exact pass rewrites P
+    // in the record with its own diagonal sums: both store from registers.
+    constexpr bool kBulk = D == 128 && !EXACT;
+    constexpr uint32_t oStg = 38912;
+    static_assert(!kBulk || (oStg >= IntraCfg<D>::oY + 4096 && oStg + 8192 <= IntraCfg<D>::oTimg &&
+                             oStg + 32768 <= IntraCfg<D>::kX), "staging area");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t &bar_mma = *reinterpret_cast<uint64_t *>(sm + C::oBar);
@@ -590,6 +602,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         Gr[8 * j + 0] = a.x; Gr[8 * j + 1] = a.y; Gr[8 * j + 2] = a.z; Gr[8 * j + 3] = a.w;
         Gr[8 * j + 4] = b.x; Gr[8 * j + 5] = b.y; Gr[8 * j + 6] = b.z; Gr[8 * j + 7] = b.w;
     }
+    if (kBulk && tid == 0) bulk_wait_read0();  // the [Wt | Ut] staging (the R operand area) is free
     __syncthreads();  // G scratch and raw v, w are dead from here on
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
@@ -742,7 +755,8 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
                             const int s = s0 + 8 * half + x;
                             f[x] = s <= tt ? __uint_as_float(v[8 * half + x]) : 0.f;
                         }
-                        *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, s0 / 8 + half)) = pack8_hm(f, hmax);
+                        *reinterpret_cast<uint4 *>((kBulk ? sm + oStg : rec + Rec<D>::P) + swz(tt, s0 / 8 + half)) =
+                            pack8_hm(f, hmax);
                     }
                 }
             }
@@ -756,8 +770,10 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         }
         if (r >= 64 && warp < 4) {  // P columns past this row's block are zero
             for (int chunk = 2 * (Ir + 1); chunk < 8; ++chunk)
-                *reinterpret_cast<uint4 *>(rec + Rec<D>::P + swz(tt, chunk)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>((kBulk ? sm + oStg : rec + Rec<D>::P) + swz(tt, chunk)) =
+                    make_uint4(0, 0, 0, 0);
         }
+        if (kBulk) fence_proxy_async();  // the staged P is read by a bulk copy after the next barrier
     }
     if (EXACT && exact) {  // the exact path's sums join the diagonal blocks of A and P
         __syncthreads();
@@ -813,6 +829,10 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         for (int i = 0; i < 16; ++i) Tf[(o + i) * kLD + o + j] = x[i];
     }
     __syncthreads();
+    if (kBulk && tid == 0) {  // the staged P image into the record
+        bulk_s2g(rec + Rec<D>::P, sm + oStg, 8192);
+        bulk_commit();
+    }
     // 16 -> 32 merges: T_{I+1,I} = -T_{I+1,I+1} (A_{I+1,I} T_{I,I}), I = 0 and 2,
     // a 1 x 2 tile per thread
     {
@@ -895,6 +915,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
         *reinterpret_cast<uint32_t *>(timg + swz(32 + i0, j0 / 8) + (j0 % 8) * 2) = pack_h2mh(z00, z01, hmax);
         *reinterpret_cast<uint32_t *>(timg + swz(33 + i0, j0 / 8) + (j0 % 8) * 2) = pack_h2mh(z10, z11, hmax);
     }
+    if (kBulk && tid == 0) bulk_wait_read0();  // the P staging is free for [Wt | Ut]
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -935,9 +956,20 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
                                            pack_h2mh(__uint_as_float(w[2]), __uint_as_float(w[3]), hmax),
                                            pack_h2mh(__uint_as_float(w[4]), __uint_as_float(w[5]), hmax),
                                            pack_h2mh(__uint_as_float(w[6]), __uint_as_float(w[7]), hmax));
-                uint8_t *dst = is_u ? rec + Rec<D>::Ut + kb * 8192 + swz(tt, c0 + cc)
-                                    : rec + Rec<D>::A1 + kb * 16384 + swz(64 + tt, c0 + cc);
+                uint8_t *dst = kBulk ? sm + oStg + (is_u ? 16384 : 0) + kb * 8192 + swz(tt, c0 + cc)
+                               : is_u ? rec + Rec<D>::Ut + kb * 8192 + swz(tt, c0 + cc)
+                                      : rec + Rec<D>::A1 + kb * 16384 + swz(64 + tt, c0 + cc);
                 *reinterpret_cast<uint4 *>(dst) = o;
+            }
+        }
+        if (kBulk) {  // Wt (rows 64-127 of each A1 block) and Ut into the record
+            fence_proxy_async();
+            named_sync(2, 128);
+            if (tid == 0) {
+                bulk_s2g(rec + Rec<D>::A1 + 8192, sm + oStg, 8192);
+                bulk_s2g(rec + Rec<D>::A1 + 16384 + 8192, sm + oStg + 8192, 8192);
+                bulk_s2g(rec + Rec<D>::Ut, sm + oStg + 16384, 16384);
+                bulk_commit();
             }
         }
     }
@@ -948,6 +980,7 @@ __global__ void __launch_bounds__(kIntraThreads, 2) gdn2_tc_intra_kernel(const _
     __syncthreads();  // the item's shared memory and TMEM are free for the next one
     tc_fence_after();
     }  // items
+    if (kBulk && tid == 0) bulk_wait0();  // the last record's bulk copies are complete
     report_range(p.status, half_clipped(hmax));
     // every MMA has completed before Tensor Memory is released (after a timed
     // out wait one may still run); each item completed two phases of bar_mma
