@@ -112,6 +112,21 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Contiguous shared -> global copy in a bulk async-group of the issuing
+// thread (addresses 16-byte aligned, size a multiple of 16).  The writers of
+// the shared source issue fence_proxy_async() before the barrier that
+// precedes the copy.  bulk_commit closes the group; bulk_wait_read0 returns
+// once every committed group has read its shared source (which may then be
+// overwritten), bulk_wait0 once every group's writes are complete.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Tile of a 3-D tensor map (box given by the map) -> shared memory, completing
 // on an mbarrier.  tmap: generic address of a CUtensorMap in kernel-parameter,
 // constant or global memory; c0 (innermost) .. c2: element coordinates, with

@@ -34,6 +34,8 @@
 #include "gdn2_record.cuh"
 #include "gdn2_tc.cuh"
 
+
+
 namespace gdn2 {
 
 namespace {
@@ -485,7 +487,12 @@ struct La128Cfg {
     static constexpr uint32_t oU = NSTAGE * kStage;             // two [64 t][128 columns] fp16 buffers
     static constexpr uint32_t kUBytes = 2 * 8192;
     static constexpr uint32_t oEGL = oU + 2 * kUBytes;          // eGL per stage, D fp32
-    static constexpr uint32_t kSmem = oEGL + NSTAGE * D * 4 + 1024;
+    // the output epilogue's token rows (256 bytes each), staged for bulk
+    // copies; the 272-byte stride puts the lanes' 16-byte stores in different
+    // banks
+    static constexpr uint32_t oO = oEGL + NSTAGE * D * 4;
+    static constexpr uint32_t kOStride = 272;
+    static constexpr uint32_t kSmem = oO + 64 * kOStride + 1024;
     static constexpr uint32_t kStageBytes = Rec<D>::mma_prefix + D * 4;
     static constexpr uint32_t cS = 0, cD = 128, cXY = 384, cXa = 448, kTmemCols = 512;
     static_assert(Rec<D>::mma_prefix == kStage, "P, A1 and Kd^T are one contiguous copy");
@@ -916,6 +923,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
         const int t = 32 * q + lane;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         const int64_t seq_start = cu_at(p, n), seq_end = cu_at(p, n + 1);
+        uint8_t *srow = sm + C::oO + t * C::kOStride;  // this lane's token row, staged
         for (int c = 0; c < nck; ++c) {
             if (!warp_wait(&o_full[c & 1], (c >> 1) & 1)) {
                 set_timeout_la(p);
@@ -925,6 +933,7 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
             const int64_t tok = seq_start + static_cast<int64_t>(c_lo + c) * kChunk + t;
             const bool valid = !trans && tok < seq_end;
             bf16 *orow = p.o + tok * p.so_t + static_cast<int64_t>(hv) * p.so_h;
+            bulk_wait_read0();  // the previous chunk's row copy has read the staging row
 #pragma unroll 1
             for (int j = 0; j < D / 32; ++j) {
                 uint32_t r[32];
@@ -939,13 +948,19 @@ __global__ void __launch_bounds__(kLaThreads, 1) gdn2_tc_state_la128_kernel(Para
                             const float b = __uint_as_float(r[8 * cc + e + 1]) * p.scale;
                             return p.in_f16 ? pack_f16_rn(a, b) : pack_bf2(a, b);
                         };
-                        reinterpret_cast<uint4 *>(orow + 32 * j)[cc] = make_uint4(pk(0), pk(2), pk(4), pk(6));
+                        *reinterpret_cast<uint4 *>(srow + 64 * j + 16 * cc) = make_uint4(pk(0), pk(2), pk(4), pk(6));
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&d_free[c & 1]);
+            if (valid) {  // the row (256 bytes) by one bulk copy of this lane, after the D buffer is released
+                fence_proxy_async();
+                bulk_s2g(orow, srow, D * 2);
+                bulk_commit();
+            }
         }
+        bulk_wait0();
     } else {
         // ------------------- U epilogue (D rows 64-127 = Wt S): U = Ut - Wt S in place
         uint32_t hmax = 0;  // largest magnitude converted to fp16 (range check)
