@@ -108,7 +108,7 @@ struct ScanCta {
     int rank, hv, seg, tile;
     bool trans;  // a transition tile (its tile indexes the 2 rt tiles of [M | B])
 };
-__device__ __forceinline__ ScanCta scan_cta(int b, int mode, int P, int HV, int rt) {
+__host__ __device__ __forceinline__ ScanCta scan_cta(int b, int mode, int P, int HV, int rt) {
     const int per = scan_ctas_per_group(mode, P, rt);
     const int x = b % per, grp = b / per;
     ScanCta c;
